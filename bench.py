@@ -1,0 +1,453 @@
+"""Benchmark: proportional PER sampling on GB300.
+
+One step = one PER "train call" of the minibatch workload: N=262144 fp32
+priorities |N(0,1)|+1e-6, alpha=0.6, 32 rounds of
+  build_cdf -> sample 8192 stratified -> IS weights (beta=0.4) ->
+  update the 8192 sampled items with new |N(0,1)|+1e-6 priorities
+through the library's C ABI.  value = sampled transitions per second over
+all ranks (device-resident inputs); e2e = the same with each step's new
+priorities copied in from pinned host memory and the step's indices and
+weights copied back, inside the timed region.
+
+--impl reference times the CPU oracle (serial C, fp64) on the same workload
+on this host's cores.  With torchrun, every rank runs an independent replica
+("replicas only": the method has no exchange step); rank 0 prints one JSON
+line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+W = workloads.MINIBATCH
+N, B, ROUNDS, ALPHA, BETA = W["N"], W["B"], W["rounds"], W["alpha"], W["beta"]
+METRIC = "PER samples/sec (minibatch: build_cdf + sample + IS weights + update, 32 rounds/step)"
+UNIT = "samples/s"
+WORKLOAD = (f"minibatch N={N} fp32 |N(0,1)|+1e-6, alpha={ALPHA}, {ROUNDS} rounds x "
+            f"(build_cdf, sample {B} stratified, IS weights beta={BETA}, update {B} at sampled indices)")
+L2_FLUSH_BYTES = 512 << 20
+
+# algorithmic bytes per unit: build_cdf reads p and writes cdf
+KERNEL_BYTES = {
+    "build_cdf": lambda: 8 * N,                 # 4 B read + 4 B write per item
+    "sample": lambda: 4 * N + 4 * B,            # every CDF item read once + index write
+    "is_weights": lambda: 12 * B,               # index read + pa gather + weight write
+    "update": lambda: 8 * B + 4 * B + 8 * B,    # idx + p read, priority write, winner slot
+}
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def config_dict(n_gpus):
+    return {"workload": WORKLOAD, "N": N, "B": B, "rounds_per_step": ROUNDS, "alpha": ALPHA, "beta": BETA,
+            "parallelism": f"replicas x{n_gpus}", "l2": "flushed (512 MiB write) between timed steps"}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = os.path.join("/tmp", f"per_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            t = [x.strip() for x in line.split(",")]
+            if len(t) < 10:
+                continue
+            if self.bus_id and self.bus_id[-12:] not in t[1].lower():
+                continue
+            rows.append(t)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def mhz(s):
+            try:
+                return float(s.split()[0])
+            except Exception:
+                return None
+        sm = [mhz(r[2]) for r in rows if mhz(r[2]) is not None]
+        mx = [mhz(r[3]) for r in rows if mhz(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ our arm -------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import cdf_scan_gb300 as per
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    seed = W["seed"] + 1000 * rank
+    p0 = workloads.minibatch_priorities(seed=seed)
+    newp = np.stack([workloads.minibatch_new_priorities(r, seed=seed) for r in range(ROUNDS)])
+    d_p0 = torch.from_numpy(p0).to(dev)
+    d_newp = torch.from_numpy(newp).to(dev)
+    idx = torch.empty((ROUNDS, B), dtype=torch.int32, device=dev)
+    wts = torch.empty((ROUNDS, B), dtype=torch.float32, device=dev)
+    h_newp = torch.from_numpy(newp).pin_memory()
+    h_idx = torch.empty((ROUNDS, B), dtype=torch.int32).pin_memory()
+    h_w = torch.empty((ROUNDS, B), dtype=torch.float32).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    ctx = per.PerContext(N, ALPHA, per.PER_SCAN)
+    h = ctx.handle
+    per.per_set_priorities(h, d_p0)
+    stream = torch.cuda.current_stream()
+    step_counter = [0]
+
+    def one_step(timer=None, e2e=False):
+        s = step_counter[0]
+        step_counter[0] += 1
+        if e2e:
+            d_newp.copy_(h_newp, non_blocking=True)
+        for r in range(ROUNDS):
+            off = (s * ROUNDS + r) * B
+            if timer:
+                timer.mark("build_cdf")
+            per.per_build_cdf(h)
+            if timer:
+                timer.mark("sample")
+            per.per_sample(h, B, seed, off, per.PER_SCAN, idx[r])
+            if timer:
+                timer.mark("is_weights")
+            per.per_is_weights(h, idx[r], BETA, wts[r])
+            if timer:
+                timer.mark("update")
+            per.per_update(h, idx[r], d_newp[r])
+        if timer:
+            timer.mark(None)
+        if e2e:
+            h_idx.copy_(idx, non_blocking=True)
+            h_w.copy_(wts, non_blocking=True)
+
+    class KernelTimer:
+        """CUDA events between consecutive library calls on the launching stream."""
+
+        def __init__(self):
+            self.events = []
+
+        def mark(self, name):
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(stream)
+            self.events.append((name, ev))
+
+        def totals(self):
+            out = {}
+            for (name, a), (_, b) in zip(self.events, self.events[1:]):
+                if name is None:
+                    continue
+                t, n = out.get(name, (0.0, 0))
+                out[name] = (t + a.elapsed_time(b), n + 1)
+            self.events = []
+            return out
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+            torch.cuda.synchronize()
+
+    def timed(steps, e2e=False, timer=None):
+        launches0 = per.per_launch_count()
+        total_ms = 0.0
+        per_kernel = {}
+        for _ in range(steps):
+            flush.zero_()
+            barrier()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one_step(timer=timer, e2e=e2e)
+            b.record(stream)
+            b.synchronize()
+            total_ms += a.elapsed_time(b)
+            if timer:
+                for k, (t, n) in timer.totals().items():
+                    pt, pn = per_kernel.get(k, (0.0, 0))
+                    per_kernel[k] = (pt + t, pn + n)
+        barrier()
+        return total_ms, per.per_launch_count() - launches0, per_kernel
+
+    for _ in range(args.warmup):
+        one_step()
+        one_step(e2e=True)
+    barrier()
+
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    clocks = ClockSampler(bus)
+    clocks.start()
+    timer = KernelTimer()
+    t_ms, launches, per_kernel = timed(args.steps, timer=timer)
+    clk = clocks.stop()
+    e2e_ms, _, _ = timed(args.steps, e2e=True)
+    status = per.per_check(h)
+    if status != 0:
+        raise RuntimeError(f"device status after timing: {per.per_status_str(status)}")
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    t_ms = max_over_ranks(t_ms)
+    e2e_ms = max_over_ranks(e2e_ms)
+    samples = args.steps * ROUNDS * B * world
+    result = None
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        name, (ktot, kn) = max(per_kernel.items(), key=lambda kv: kv[1][0])
+        avg_s = ktot / kn / 1e3
+        algo = KERNEL_BYTES[name]()
+        achieved = algo / avg_s / 1e9
+        roofline = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
+                    "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": traffic_for(name), "avg_launch_us": round(avg_s * 1e6, 3),
+                    "algorithmic_bytes_per_launch": algo}
+        result = {
+            "metric": METRIC, "value": samples / (t_ms / 1e3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded Philox draws; no dataset)", "config": config_dict(world),
+            "e2e": {"value": samples / (e2e_ms / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(ROUNDS * B * 4),
+                    "d2h_bytes_per_step": int(ROUNDS * B * 8)},
+            "gpu_launches": int(launches),
+            "roofline": roofline,
+            "kernel_us_per_step": {k: round(t / args.steps * 1e3, 2) for k, (t, n) in per_kernel.items()},
+            "build_cdf_gbs": round(KERNEL_BYTES["build_cdf"]() / (per_kernel["build_cdf"][0] /
+                                                                 per_kernel["build_cdf"][1] / 1e3) / 1e9, 1),
+            "clocks": clk,
+            "impl": "gb300",
+        }
+        if not args.no_extras:
+            result["extras"] = extras(per, torch, dev, peak)
+    ctx.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def traffic_for(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_name]
+        src = os.path.join(ROOT, "cdf_scan_gb300", "csrc", e["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != e["source_sha"]:
+            return None
+        return e["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def extras(per, torch, dev, peak):
+    """Other headline numbers of the metric, measured in the same run (not
+    the bench value): the 16M scan against HBM, and the tree sample+update
+    step at full fill."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def time_call(fn, reps, flush_l2=True):
+        ts = []
+        for _ in range(reps):
+            if flush_l2:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    S = workloads.STRESS
+    n = S["N"]
+    ctx = per.PerContext(n, S["alpha"], per.PER_SCAN)
+    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
+    for _ in range(3):
+        per.per_build_cdf(ctx.handle)
+    us = time_call(lambda: per.per_build_cdf(ctx.handle), 30)
+    gbs = 8 * n / (us * 1e-6) / 1e9
+    idx = torch.empty(S["B"], dtype=torch.int32, device=dev)
+    us_s = time_call(lambda: per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx), 20)
+    out["stress_build_cdf"] = {"N": n, "us": round(us, 2), "gbs": round(gbs, 1), "frac_of_measured_peak":
+                               round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+                               "l2": "flushed before each rep"}
+    out["stress_sample"] = {"B": S["B"], "us": round(us_s, 2), "samples_per_s": S["B"] / (us_s * 1e-6)}
+    ctx.close()
+
+    T = workloads.TREE
+    cap = T["capacity"]
+    ctx = per.PerContext(cap, T["alpha"], per.PER_TREE)
+    p = np.zeros(cap, np.float32)
+    p[:] = workloads.lognormal(cap, workloads.rng(T["seed"], 999))
+    per.per_set_priorities(ctx.handle, torch.from_numpy(p).to(dev))
+    tidx = torch.empty(T["B"], dtype=torch.int32, device=dev)
+    upd_idx = []
+    upd_p = []
+    for s in range(8):
+        per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE, tidx)
+        i, q = workloads.tree_update_batch(s, tidx.cpu().numpy())
+        upd_idx.append(torch.from_numpy(i).to(dev))
+        upd_p.append(torch.from_numpy(q).to(dev))
+    k = [0]
+
+    def tree_step():
+        s = k[0] % 8
+        k[0] += 1
+        per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE, tidx)
+        per.per_update(ctx.handle, upd_idx[s], upd_p[s])
+    for _ in range(5):
+        tree_step()
+    us_t = time_call(tree_step, 200, flush_l2=False)
+    out["tree_sample_update_step"] = {"capacity": cap, "B": T["B"], "us": round(us_t, 2),
+                                      "target_us": 20.0, "l2": "warm (tree is 4 MiB, resident across steps)"}
+    if per.per_check(ctx.handle) != 0:
+        out["tree_sample_update_step"]["status"] = "device status not clean"
+    ctx.close()
+    return out
+
+
+# -------------------------------------------------------- oracle arms -------
+
+def oracle_step(p, seed, step):
+    """One step of the workload on the CPU oracle (serial C, fp64)."""
+    import oracle
+    prio = p
+    for r in range(ROUNDS):
+        C = oracle.cdf64(prio, ALPHA)
+        idx, _ = oracle.sample_cdf_f64(C, B, seed, (step * ROUNDS + r) * B)
+        oracle.is_weights(prio, N, ALPHA, idx, BETA)
+        prio = oracle.apply_updates(prio, idx, workloads.minibatch_new_priorities(r, seed=seed))
+    return prio
+
+
+def cpu_baseline(seconds=10.0):
+    import oracle
+    oracle.build()
+    p = workloads.minibatch_priorities()
+    t0 = time.perf_counter()
+    rounds = 0
+    step = 0
+    while time.perf_counter() - t0 < seconds:
+        p = oracle_step(p, W["seed"], step)
+        step += 1
+        rounds += ROUNDS
+    dt = time.perf_counter() - t0
+    return {"value": rounds * B / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{step} full steps ({rounds} rounds) of the minibatch workload, {dt:.1f} s, single thread"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    p = workloads.minibatch_priorities()
+    for s in range(args.warmup):
+        p = oracle_step(p, W["seed"], s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        p = oracle_step(p, W["seed"], args.warmup + s)
+    dt = time.perf_counter() - t0
+    value = args.steps * ROUNDS * B / dt
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox draws; no dataset)", "config": config_dict(world),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} full steps of the minibatch workload, single thread"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    rank, world, local_rank = env_rank()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        from cdf_scan_gb300 import _build
+        if rank == 0 or world == 1:
+            _build.build()
+        res = run_ours(args, rank, world, local_rank)
+        if res is not None and world == 1:
+            res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,135 @@
+// common.cuh -- device helpers: relaxed/acquire memory accesses, mbarrier +
+// bulk-copy (TMA) wrappers, bounded waits, Philox4x32-10, thresholds.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define PER_FULL_MASK 0xffffffffu
+
+// Upper bound on polling iterations of any device-side wait.  Each poll
+// sleeps ~0.25-1 us, so a wait gives up after roughly one to a few seconds
+// and records ST_TIMEOUT instead of hanging.
+constexpr unsigned kSpinLimit = 1u << 22;
+
+// ---- memory access --------------------------------------------------------
+
+__device__ __forceinline__ void ld_relaxed_v2(const unsigned long long* p, unsigned long long& a,
+                                              unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v2(unsigned long long* p, unsigned long long a, unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+__device__ __forceinline__ void st_f4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+// ---- mbarrier + bulk copy (global -> shared, completes on an mbarrier) ------
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Plain (non-multicast) 1-D bulk copy; dst/src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of an mbarrier.  A bulk copy from valid
+// global memory always completes, so the limit is a safety net: on expiry
+// the caller's status word records ST_TIMEOUT.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+    for (unsigned i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i > 64) __nanosleep(256);
+    }
+    return false;
+}
+
+// ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) ----------------------
+// First output word for counter (ctr64 lo, ctr64 hi, 0, 0) under key
+// (seed lo, seed hi).
+
+__device__ __forceinline__ uint32_t philox_word(uint64_t seed, uint64_t ctr64) {
+    uint32_t c0 = static_cast<uint32_t>(ctr64), c1 = static_cast<uint32_t>(ctr64 >> 32);
+    uint32_t c2 = 0u, c3 = 0u;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t m0 = 0xD2511F53u, m1 = 0xCD9E8D57u;
+        uint32_t hi0 = __umulhi(m0, c0), lo0 = m0 * c0;
+        uint32_t hi1 = __umulhi(m1, c2), lo1 = m1 * c2;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c0;
+}
+
+// U in (0, 1]: ((x >> 8) + 1) * 2^-24 (exact).
+__device__ __forceinline__ float u01_open_closed(uint64_t seed, uint64_t ctr) {
+    return __uint2float_rn((philox_word(seed, ctr) >> 8) + 1u) * 5.9604644775390625e-8f;
+}
+
+// U in [0, 1): (x >> 8) * 2^-24 (exact).
+__device__ __forceinline__ float u01_closed_open(uint64_t seed, uint64_t ctr) {
+    return __uint2float_rn(philox_word(seed, ctr) >> 8) * 5.9604644775390625e-8f;
+}
+
+// Stratified threshold u_k = fl32(fl32(fl32(k + U) / B) * T), no contraction.
+__device__ __forceinline__ float stratified_threshold(int k, float U, float fB, float T) {
+    float a = __fadd_rn(__int2float_rn(k), U);
+    float b = __fdiv_rn(a, fB);
+    return __fmul_rn(b, T);
+}
+
+// p^alpha; alpha == 1 skips the power (exact).
+__device__ __forceinline__ float pow_alpha(float x, float alpha, bool identity) {
+    return identity ? x : powf(x, alpha);
+}

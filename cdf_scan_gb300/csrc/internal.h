@@ -1,0 +1,69 @@
+// internal.h -- context layout and launcher declarations shared by the
+// library's translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/per.h"
+
+// Device status word bits (recorded by kernels, read by per_check).
+enum : int {
+    ST_TIMEOUT = 1,  // a bounded wait ran out
+    ST_RANGE = 2,    // exact-carry range exceeded
+    ST_VALUE = 4,    // negative / NaN priority, or an index out of range
+    ST_EMPTY = 8,    // total priority 0 when sampling
+};
+
+// Slots of the per-context device counter array.
+enum : int {
+    CTR_SCAN_TICKET = 0,  // next tile id of the running scan
+    CTR_SCAN_DONE = 1,    // tiles finished in the running scan
+    CTR_SCAN_EPOCH = 2,   // tags scan descriptors of the current call (>= 1)
+    CTR_UPD_EPOCH = 3,    // tags winner slots of the current update (>= 1)
+    CTR_UPD_DONE = 4,     // CTAs finished in the running update-apply
+    CTR_ISW_MIN = 5,      // running min of pa (float bits) for IS weights
+    CTR_ISW_BAR_COUNT = 6,
+    CTR_ISW_BAR_GEN = 7,
+    CTR_ISW_DONE = 8,
+    NUM_CTRS = 16
+};
+
+struct per_ctx {
+    int device;
+    int num_sms;
+    int64_t capacity;
+    int64_t alloc_n;      // capacity rounded up (vector loads may touch the pad)
+    int64_t cap_pow2;
+    int log2_cap;
+    int64_t size;
+    float alpha;
+    uint32_t flags;
+
+    float* prio;                      // raw priorities [alloc_n]
+    float* cdf;                       // CDF [alloc_n] (PER_SCAN)
+    float* tree;                      // [2*cap_pow2] (PER_TREE)
+    unsigned long long* scan_desc;    // 4 words per scan tile
+    int64_t scan_desc_tiles;
+    unsigned long long* winner;       // [capacity] epoch-tagged last writer
+    unsigned* ctrs;                   // [NUM_CTRS]
+    int* status;                      // device status word
+};
+
+// Host-side launch accounting (per_launch_count).
+void per_note_launch(int n = 1);
+
+// Launchers (each returns PER_OK or PER_ERR_CUDA after enqueueing).
+per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s);
+per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+                              int32_t* out, cudaStream_t s);
+per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+                              int32_t* out, cudaStream_t s);
+per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta, float* out,
+                             cudaStream_t s);
+per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n, cudaStream_t s);
+per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s);
+per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, uint64_t offset,
+                           const float* u_rows, int32_t* out, float* out_cdf, cudaStream_t s);
+
+inline per_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PER_OK : PER_ERR_CUDA; }

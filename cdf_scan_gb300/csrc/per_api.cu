@@ -1,0 +1,235 @@
+// per_api.cu -- the C ABI declared in include/per.h: context lifetime,
+// argument checking (before any launch) and dispatch to the kernels.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int64_t kMaxCapacity = int64_t(1) << 30;
+constexpr int64_t kPad = 16384;  // buffer padding: vector loads of a ragged tail stay in bounds
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename T>
+cudaError_t alloc_zero(T** p, size_t count, cudaStream_t s) {
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), count * sizeof(T));
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        return e;
+    }
+    return cudaMemsetAsync(*p, 0, count * sizeof(T), s);
+}
+
+void free_ctx(per_ctx* c) {
+    if (!c) return;
+    cudaFree(c->prio);
+    cudaFree(c->cdf);
+    cudaFree(c->tree);
+    cudaFree(c->scan_desc);
+    cudaFree(c->winner);
+    cudaFree(c->ctrs);
+    cudaFree(c->status);
+    std::free(c);
+}
+
+}  // namespace
+
+void per_note_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+extern "C" {
+
+uint64_t per_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* per_status_str(per_status s) {
+    switch (s) {
+        case PER_OK: return "PER_OK";
+        case PER_ERR_ARG: return "PER_ERR_ARG: invalid argument";
+        case PER_ERR_CUDA: return "PER_ERR_CUDA: CUDA call or launch failed";
+        case PER_ERR_OOM: return "PER_ERR_OOM: device allocation failed";
+        case PER_ERR_TIMEOUT: return "PER_ERR_TIMEOUT: a bounded device wait ran out";
+        case PER_ERR_EMPTY: return "PER_ERR_EMPTY: nothing to sample (size or total is zero)";
+        case PER_ERR_STATE: return "PER_ERR_STATE: structure not enabled in this context";
+        case PER_ERR_RANGE: return "PER_ERR_RANGE: a tile sum exceeded the exact-carry range";
+        case PER_ERR_VALUE: return "PER_ERR_VALUE: negative/NaN priority or index out of range";
+    }
+    return "PER_ERR_UNKNOWN";
+}
+
+per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t flags, void* stream) {
+    if (!out) return PER_ERR_ARG;
+    *out = nullptr;
+    if (capacity < 1 || capacity > kMaxCapacity || !(alpha >= 0.f) || alpha > 1e30f) return PER_ERR_ARG;
+    if (flags == 0 || (flags & ~(PER_SCAN | PER_TREE)) != 0) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    per_ctx* c = static_cast<per_ctx*>(std::calloc(1, sizeof(per_ctx)));
+    if (!c) return PER_ERR_OOM;
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+        std::free(c);
+        return PER_ERR_CUDA;
+    }
+    c->capacity = capacity;
+    c->alloc_n = (capacity + kPad - 1) / kPad * kPad + kPad;
+    c->log2_cap = 0;
+    while ((int64_t(1) << c->log2_cap) < capacity) ++c->log2_cap;
+    c->cap_pow2 = int64_t(1) << c->log2_cap;
+    c->size = 0;
+    c->alpha = alpha;
+    c->flags = flags;
+    c->scan_desc_tiles = (c->alloc_n + 1023) / 1024;
+    bool ok = alloc_zero(&c->prio, c->alloc_n, s) == cudaSuccess &&
+              alloc_zero(&c->winner, static_cast<size_t>(capacity), s) == cudaSuccess &&
+              alloc_zero(&c->ctrs, NUM_CTRS, s) == cudaSuccess &&
+              alloc_zero(&c->status, 1, s) == cudaSuccess;
+    if (ok && (flags & PER_SCAN))
+        ok = alloc_zero(&c->cdf, c->alloc_n, s) == cudaSuccess &&
+             alloc_zero(&c->scan_desc, 4 * static_cast<size_t>(c->scan_desc_tiles), s) == cudaSuccess;
+    if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
+    if (ok) {
+        // epochs start at 1 (0 marks "never written"); the IS-weight minimum
+        // starts above every non-negative float.
+        unsigned init[NUM_CTRS] = {0};
+        init[CTR_SCAN_EPOCH] = 1u;
+        init[CTR_UPD_EPOCH] = 1u;
+        init[CTR_ISW_MIN] = 0xffffffffu;
+        ok = cudaMemcpyAsync(c->ctrs, init, sizeof(init), cudaMemcpyHostToDevice, s) == cudaSuccess &&
+             cudaStreamSynchronize(s) == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();
+        free_ctx(c);
+        return PER_ERR_OOM;
+    }
+    *out = c;
+    return PER_OK;
+}
+
+per_status per_destroy(per_ctx* ctx) {
+    if (!ctx) return PER_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    free_ctx(ctx);
+    return cuda_status(e);
+}
+
+per_status per_set_size(per_ctx* ctx, int64_t n) {
+    if (!ctx || n < 0 || n > ctx->capacity) return PER_ERR_ARG;
+    ctx->size = n;
+    return PER_OK;
+}
+
+int64_t per_size(const per_ctx* ctx) { return ctx ? ctx->size : -1; }
+int64_t per_capacity_pow2(const per_ctx* ctx) { return ctx ? ctx->cap_pow2 : -1; }
+const float* per_priorities_ptr(const per_ctx* ctx) { return ctx ? ctx->prio : nullptr; }
+const float* per_cdf_ptr(const per_ctx* ctx) { return ctx ? ctx->cdf : nullptr; }
+const float* per_tree_ptr(const per_ctx* ctx) { return ctx ? ctx->tree : nullptr; }
+
+per_status per_set_priorities(per_ctx* ctx, const float* d_prio, int64_t n, void* stream) {
+    if (!ctx || n < 0 || n > ctx->capacity || (n > 0 && (!d_prio || !aligned16(d_prio)))) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n > 0 && cudaMemcpyAsync(ctx->prio, d_prio, static_cast<size_t>(n) * sizeof(float),
+                                 cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return PER_ERR_CUDA;
+    if (cudaMemsetAsync(ctx->prio + n, 0, static_cast<size_t>(ctx->alloc_n - n) * sizeof(float), s) != cudaSuccess)
+        return PER_ERR_CUDA;
+    ctx->size = n;
+    if (ctx->flags & PER_TREE) return launch_tree_from_prio(ctx, s);
+    return PER_OK;
+}
+
+per_status per_update(per_ctx* ctx, const int32_t* d_idx, const float* d_prio, int32_t n, void* stream) {
+    if (!ctx || n < 0 || (n > 0 && (!d_idx || !d_prio))) return PER_ERR_ARG;
+    if (n == 0) return PER_OK;
+    return launch_update(ctx, d_idx, d_prio, n, static_cast<cudaStream_t>(stream));
+}
+
+per_status per_build_cdf(per_ctx* ctx, void* stream) {
+    if (!ctx) return PER_ERR_ARG;
+    if (!(ctx->flags & PER_SCAN)) return PER_ERR_STATE;
+    if (ctx->size < 1) return PER_ERR_EMPTY;
+    return launch_build_cdf(ctx, static_cast<cudaStream_t>(stream));
+}
+
+per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, int mode, const float* d_u01,
+                      int32_t* d_out_idx, void* stream) {
+    if (!ctx || B < 1 || B > (1 << 24) || !d_out_idx) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mode == static_cast<int>(PER_SCAN)) {
+        if (!(ctx->flags & PER_SCAN)) return PER_ERR_STATE;
+        if (ctx->size < 1) return PER_ERR_EMPTY;
+        return launch_sample_scan(ctx, B, seed, offset, d_u01, d_out_idx, s);
+    }
+    if (mode == static_cast<int>(PER_TREE)) {
+        if (!(ctx->flags & PER_TREE)) return PER_ERR_STATE;
+        return launch_sample_tree(ctx, B, seed, offset, d_u01, d_out_idx, s);
+    }
+    return PER_ERR_ARG;
+}
+
+per_status per_is_weights(per_ctx* ctx, const int32_t* d_idx, int32_t B, float beta, float* d_out_w, void* stream) {
+    if (!ctx || B < 1 || !d_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f) return PER_ERR_ARG;
+    return launch_is_weights(ctx, d_idx, B, beta, d_out_w, static_cast<cudaStream_t>(stream));
+}
+
+per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream) {
+    if (!ctx || !d_out) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float* src = nullptr;
+    if (mode == static_cast<int>(PER_TREE)) {
+        if (!(ctx->flags & PER_TREE)) return PER_ERR_STATE;
+        src = ctx->tree + 1;
+    } else if (mode == static_cast<int>(PER_SCAN)) {
+        if (!(ctx->flags & PER_SCAN)) return PER_ERR_STATE;
+        if (ctx->size < 1) return PER_ERR_EMPTY;
+        src = ctx->cdf + ctx->size - 1;
+    } else {
+        return PER_ERR_ARG;
+    }
+    return cuda_status(cudaMemcpyAsync(d_out, src, sizeof(float), cudaMemcpyDeviceToDevice, s));
+}
+
+per_status per_total_host(per_ctx* ctx, int mode, float* h_out, void* stream) {
+    if (!ctx || !h_out) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float* src = nullptr;
+    if (mode == static_cast<int>(PER_TREE)) {
+        if (!(ctx->flags & PER_TREE)) return PER_ERR_STATE;
+        src = ctx->tree + 1;
+    } else if (mode == static_cast<int>(PER_SCAN)) {
+        if (!(ctx->flags & PER_SCAN)) return PER_ERR_STATE;
+        if (ctx->size < 1) return PER_ERR_EMPTY;
+        src = ctx->cdf + ctx->size - 1;
+    } else {
+        return PER_ERR_ARG;
+    }
+    if (cudaMemcpyAsync(h_out, src, sizeof(float), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PER_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(s));
+}
+
+per_status per_check(per_ctx* ctx, void* stream) {
+    if (!ctx) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = 0;
+    if (cudaMemcpyAsync(&st, ctx->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(ctx->status, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return PER_ERR_CUDA;
+    if (st & ST_TIMEOUT) return PER_ERR_TIMEOUT;
+    if (st & ST_RANGE) return PER_ERR_RANGE;
+    if (st & ST_VALUE) return PER_ERR_VALUE;
+    if (st & ST_EMPTY) return PER_ERR_EMPTY;
+    return PER_OK;
+}
+
+per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t seed, uint64_t offset,
+                        const float* d_u_rows, int32_t* d_out_idx, float* d_out_cdf, void* stream) {
+    if (!d_logw || !d_out_idx || rows < 1 || P < 4 || (P & 3) != 0 || P > (1 << 23)) return PER_ERR_ARG;
+    if (!aligned16(d_logw) || (d_out_cdf && !aligned16(d_out_cdf))) return PER_ERR_ARG;
+    return launch_resample(d_logw, rows, P, seed, offset, d_u_rows, d_out_idx, d_out_cdf,
+                           static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

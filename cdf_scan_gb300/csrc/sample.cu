@@ -1,0 +1,191 @@
+// sample.cu -- stratified inverse-CDF sampling on the scan path.
+//
+// idx_k = first i with cdf[i] >= u_k (searchsorted, right=False; clamp to
+// n-1), with u_k = fl32(fl32(fl32(k + U_k)/B) * T) and T = cdf[n-1]
+// (POPCORNBENCH particle-filter trace: searchsorted + clamp semantics;
+// foxhunt "GPU Segment Tree for PER Sampling" section "Problem": the O(n)
+// path is prefix sum + searchsorted).
+//
+// Stratified thresholds are sorted in k, so the samples of one CTA map to one
+// contiguous window [i_lo, i_hi] of the CDF.  The CTA finds the two window
+// ends with a warp-wide 32-ary search (one gather of 32 probes per round,
+// ~log32(n) rounds), stages the window in shared memory with one bulk copy
+// (cp.async.bulk completing on an mbarrier), and every thread finishes its
+// searches in shared memory.  Windows larger than the staging buffer (very
+// skewed priorities) fall back to a global binary search inside the window.
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kWindowCap = 12288;  // floats staged per CTA (48 KB)
+
+struct SampleParams {
+    const float* __restrict__ cdf;
+    int n;
+    int B;
+    uint64_t seed, offset;
+    const float* __restrict__ u01;
+    int32_t* __restrict__ out;
+    int* status;
+};
+
+__device__ __forceinline__ float draw_u(const SampleParams& P, int k) {
+    return P.u01 ? P.u01[k] : u01_open_closed(P.seed, P.offset + static_cast<uint64_t>(k));
+}
+
+// lower_bound over cdf[0..n) by one warp (all lanes get the answer).
+__device__ int warp_lower_bound(const float* __restrict__ c, int n, float u, int lane) {
+    int lo = 0, hi = n;  // answer in [lo, hi]; hi == n: nothing >= u found yet
+    while (hi - lo > 32) {
+        const int step = (hi - lo + 31) / 32;
+        int pos = lo + (lane + 1) * step - 1;
+        if (pos > hi - 1) pos = hi - 1;
+        const float v = __ldg(c + pos);
+        const unsigned ge = __ballot_sync(PER_FULL_MASK, v >= u);
+        if (ge == 0u) {
+            lo = hi;
+        } else {
+            const int f = __ffs(ge) - 1;
+            const int pf = __shfl_sync(PER_FULL_MASK, pos, f);
+            const int pprev = __shfl_sync(PER_FULL_MASK, pos, f > 0 ? f - 1 : 0);
+            hi = pf;
+            lo = f > 0 ? pprev + 1 : lo;
+        }
+    }
+    const int pos = lo + lane;
+    const bool ge = pos < hi && __ldg(c + pos) >= u;
+    const unsigned m = __ballot_sync(PER_FULL_MASK, ge);
+    const int ans = m ? lo + __ffs(m) - 1 : hi;
+    return ans < n ? ans : n - 1;
+}
+
+template <int THREADS, int SPT>
+__global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
+    extern __shared__ __align__(128) float s_win[];
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ int s_lo, s_hi;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int k0 = blockIdx.x * THREADS * SPT;
+    const int kend = min(P.B, k0 + THREADS * SPT);  // exclusive
+    const float T = __ldg(P.cdf + P.n - 1);
+    if (!(T > 0.f)) {
+        if (threadIdx.x == 0) atomicOr(P.status, ST_EMPTY);
+        for (int s = 0; s < SPT; ++s) {
+            const int k = k0 + threadIdx.x + s * THREADS;
+            if (k < kend) P.out[k] = 0;
+        }
+        return;
+    }
+    const float fB = static_cast<float>(P.B);
+
+    // window ends: first and last threshold of this CTA
+    if (warp == 0) {
+        const float uf = stratified_threshold(k0, draw_u(P, k0), fB, T);
+        const int lo = warp_lower_bound(P.cdf, P.n, uf, lane);
+        if (lane == 0) s_lo = lo;
+    }
+    if (warp == (THREADS > 32 ? 1 : 0)) {
+        const float ul = stratified_threshold(kend - 1, draw_u(P, kend - 1), fB, T);
+        const int hi = warp_lower_bound(P.cdf, P.n, ul, lane);
+        if (lane == 0) s_hi = hi;
+    }
+
+    float u[SPT];
+#pragma unroll
+    for (int s = 0; s < SPT; ++s) {
+        const int k = k0 + threadIdx.x + s * THREADS;
+        u[s] = k < kend ? stratified_threshold(k, draw_u(P, k), fB, T) : 0.f;
+    }
+    __syncthreads();
+    const int ilo = s_lo, ihi = s_hi;
+    const int a0 = ilo & ~3;
+    const int a1 = (ihi + 4) & ~3;  // exclusive; the CDF allocation is padded
+    int res[SPT];
+    if (a1 - a0 <= kWindowCap) {
+        if (threadIdx.x == 0) {
+            mbar_init(&s_bar, 1);
+            const unsigned bytes = static_cast<unsigned>(a1 - a0) * 4u;
+            mbar_arrive_expect_tx(&s_bar, bytes);
+            bulk_copy_g2s(s_win, P.cdf + a0, bytes, &s_bar);
+        }
+        __syncthreads();
+        if (!mbar_wait_bounded(&s_bar, 0)) atomicOr(P.status, ST_TIMEOUT);
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            int lo = ilo - a0, hi = ihi - a0;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (s_win[mid] < u[s]) lo = mid + 1;
+                else hi = mid;
+            }
+            res[s] = a0 + lo;
+        }
+    } else {
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            int lo = ilo, hi = ihi;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(P.cdf + mid) < u[s]) lo = mid + 1;
+                else hi = mid;
+            }
+            res[s] = lo;
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < SPT; ++s) {
+        const int k = k0 + threadIdx.x + s * THREADS;
+        if (k < kend) P.out[k] = res[s];
+    }
+}
+
+template <int THREADS, int SPT>
+per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
+    const int per_cta = THREADS * SPT;
+    const unsigned grid = static_cast<unsigned>((P.B + per_cta - 1) / per_cta);
+    // the staging buffer plus the static barrier words exceed the default
+    // 48 KB dynamic limit: opt in once per instantiation
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(sample_scan_kernel<THREADS, SPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kWindowCap * sizeof(float))) != cudaSuccess)
+            return PER_ERR_CUDA;
+        configured = true;
+    }
+    sample_scan_kernel<THREADS, SPT><<<grid, THREADS, kWindowCap * sizeof(float), s>>>(P);
+    per_note_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+// Samples per CTA: aim the expected window (n/B items per sample, uniform
+// case) at ~2/3 of the staging buffer, and keep at least ~2 CTAs per SM busy
+// when B is small.
+per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+                              int32_t* out, cudaStream_t s) {
+    SampleParams P;
+    P.cdf = ctx->cdf;
+    P.n = static_cast<int>(ctx->size);
+    P.B = B;
+    P.seed = seed;
+    P.offset = offset;
+    P.u01 = u01;
+    P.out = out;
+    P.status = ctx->status;
+    const double ratio = static_cast<double>(P.n) / static_cast<double>(B);
+    int per_cta = 1024;
+    while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
+    while (per_cta > 32 && (B + per_cta - 1) / per_cta < 2 * ctx->num_sms) per_cta >>= 1;
+    switch (per_cta) {
+        case 1024: return launch_cfg<256, 4>(P, s);
+        case 512: return launch_cfg<256, 2>(P, s);
+        case 256: return launch_cfg<256, 1>(P, s);
+        case 128: return launch_cfg<128, 1>(P, s);
+        case 64: return launch_cfg<64, 1>(P, s);
+        default: return launch_cfg<32, 1>(P, s);
+    }
+}

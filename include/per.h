@@ -1,0 +1,208 @@
+/*
+ * per.h -- C ABI of the GB300 (sm_103a) proportional prioritized-experience-
+ * replay sampling library.
+ *
+ * What it computes (sources by page title and section):
+ *   - PufferLib PR #615 "trainer: parallel build_cdf scan + tiled mingru
+ *     backward", section 1 "Parallel build_cdf": the prioritized-replay CDF
+ *     is an inclusive prefix sum of the B priorities, rebuilt once per
+ *     minibatch update, and must stay allocation- and sync-free.
+ *   - foxhunt "GPU Segment Tree for PER Sampling": sections "Tree Layout"
+ *     (flat array, root 1, children 2j/2j+1, leaf of item i at
+ *     capacity_pow2+i, capacity rounded up to a power of two), "Operations"
+ *     (batched update = write leaves then recompute parent sums; sample =
+ *     root-to-leaf descent going left when the threshold is <= the left sum),
+ *     "Integration" (priority^alpha folded into the update; insert_batch;
+ *     update_priorities; total_priority = tree[1]), "Non-Goals" (alpha, beta
+ *     and the IS weights themselves are unchanged PER).
+ *   - POPCORNBENCH Kimi-K2.6 / l2_p48 particle-filter trace: the reference
+ *     forward's resampling -- logsumexp normalisation, exp, cumsum over the
+ *     particle axis, systematic thresholds u_j = (j + U_b)/P with one U_b per
+ *     row, searchsorted(right=False), clamp to P-1.
+ *
+ * Conventions (every call):
+ *   - Device pointers ("d_") are CUDA global-memory addresses on the device
+ *     that was current when the context was created; the caller owns them and
+ *     they must stay valid until the stream work that uses them completes.
+ *     Host pointers are marked "h_".
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call except per_total_host, per_check and per_destroy
+ *     is asynchronous and stream-ordered: it allocates nothing, never
+ *     synchronises the host, and may be captured in a CUDA graph.
+ *   - Argument errors return PER_ERR_ARG (or PER_ERR_STATE / PER_ERR_EMPTY)
+ *     before anything is launched.  A failed launch returns PER_ERR_CUDA.
+ *     Errors found on the device (a bounded wait that ran out, a value out of
+ *     range, a negative or NaN priority) are recorded in the context's status
+ *     word; per_check() reads and clears it.
+ *   - Indices are int32; capacity <= 2^30.  One context must not be used by
+ *     two streams at the same time (calls on one context are not
+ *     thread-safe).
+ *   - Randomness is explicit: a (seed, offset) pair selects Philox4x32-10
+ *     counters offset+k under key seed (Salmon et al., SC'11), or the caller
+ *     passes the uniforms in.  Results are bit-reproducible run to run.
+ */
+#ifndef PER_GB300_H
+#define PER_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct per_ctx per_ctx;
+
+typedef enum {
+    PER_OK = 0,
+    PER_ERR_ARG = 1,      /* bad argument (null, size, alignment, mode) */
+    PER_ERR_CUDA = 2,     /* a CUDA runtime call or launch failed */
+    PER_ERR_OOM = 3,      /* per_create could not allocate device memory */
+    PER_ERR_TIMEOUT = 4,  /* a bounded device-side wait ran out */
+    PER_ERR_EMPTY = 5,    /* nothing to sample: size 0 or total priority 0 */
+    PER_ERR_STATE = 6,    /* structure not enabled in this context */
+    PER_ERR_RANGE = 7,    /* a sum exceeded the exact-carry range */
+    PER_ERR_VALUE = 8     /* a negative or NaN priority was seen */
+} per_status;
+
+/* Structures kept by a context (flags of per_create) and sampling modes. */
+#define PER_SCAN 1u /* raw priorities + CDF built by per_build_cdf (PR #615) */
+#define PER_TREE 2u /* sum segment tree of priority^alpha (foxhunt) */
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* per_status_str(per_status s);
+
+/*
+ * per_create -- allocate a context for `capacity` items (1 <= capacity <=
+ * 2^30) with exponent `alpha` >= 0 (pa_i = p_i^alpha; foxhunt "Integration":
+ * priority^alpha is applied inside the update, not kept as a separate
+ * buffer).  `flags` is PER_SCAN, PER_TREE or both.  All device memory the
+ * context will ever use is allocated here (raw priorities, the CDF, the tree
+ * of 2*capacity_pow2 floats, scan descriptors, update scratch) and
+ * zero-filled on `stream`, which is synchronised before returning.  The size
+ * (number of valid items) starts at 0.  On error *out is NULL.
+ */
+per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t flags, void* stream);
+
+/* per_destroy -- synchronise the device and free everything the context
+ * owns.  NULL is accepted. */
+per_status per_destroy(per_ctx* ctx);
+
+/* per_set_size -- number of valid items n (0 <= n <= capacity): the CDF
+ * covers [0, n) and IS weights use N = n.  Host-side only; nothing launched.
+ * Items >= n keep whatever priority they hold (in the tree they contribute
+ * their leaf value, 0 until written). */
+per_status per_set_size(per_ctx* ctx, int64_t n);
+int64_t per_size(const per_ctx* ctx);
+int64_t per_capacity_pow2(const per_ctx* ctx);
+
+/*
+ * per_set_priorities -- bulk load: raw priorities d_prio[0..n) (float32, n <=
+ * capacity, 16-byte aligned) become items 0..n-1, the size becomes n, and
+ * when PER_TREE is set the tree leaves become p^alpha (zero beyond n) and all
+ * internal sums are rebuilt in the fixed pairwise order of foxhunt "Tree
+ * Layout".  Items >= n are reset to priority 0.
+ */
+per_status per_set_priorities(per_ctx* ctx, const float* d_prio, int64_t n, void* stream);
+
+/*
+ * per_update -- batched priority update (foxhunt "Operations" / Update and
+ * "Integration" / update_priorities_gpu, insert_batch): for k in [0, n),
+ * item d_idx[k] gets raw priority d_prio[k] (>= 0).  When an index occurs
+ * more than once the LAST occurrence in batch order wins.  Updates the raw
+ * priorities (read by the next per_build_cdf) and, with PER_TREE, writes leaf
+ * p^alpha and recomputes every affected internal sum as tree[j] =
+ * tree[2j] + tree[2j+1] -- bit-identical to rebuilding the whole tree.
+ * Indices must lie in [0, capacity); the size is not changed (insert_batch
+ * is per_update followed by per_set_size).  n may be 0.
+ */
+per_status per_update(per_ctx* ctx, const int32_t* d_idx, const float* d_prio, int32_t n,
+                      void* stream);
+
+/*
+ * per_build_cdf -- PR #615 "Parallel build_cdf": cdf[i] = sum_{j<=i} p_j^alpha
+ * over the n valid items, as one single-pass decoupled-lookback scan with
+ * p^alpha fused into the load.  The result is monotone non-decreasing and
+ * bit-reproducible (tile carries are summed exactly in 128-bit fixed point;
+ * each tile's sum of p^alpha must stay below 2^44, else PER_ERR_RANGE is
+ * recorded).  Requires PER_SCAN and n >= 1.  The CDF is read through
+ * per_cdf_ptr(); cdf[n-1] is the total.
+ */
+per_status per_build_cdf(per_ctx* ctx, void* stream);
+
+/*
+ * per_sample -- draw B stratified samples (1 <= B <= 2^24):
+ *   u_k = fl32(fl32(fl32(k + U_k) / B) * T),  U_k in (0, 1],
+ * U_k = ((x >> 8) + 1) * 2^-24 with x the first word of Philox4x32-10 at
+ * counter (offset + k, 0, 0) under key seed, or U_k = d_u01[k] when d_u01 is
+ * not NULL (values in (0,1]).
+ *   mode PER_SCAN: T = cdf[n-1]; idx_k = first i with cdf[i] >= u_k
+ *     (searchsorted(right=False)), clamped to n-1.  Needs per_build_cdf first.
+ *   mode PER_TREE: T = tree[1]; root-to-leaf descent (foxhunt "Operations" /
+ *     Sample): at node j with children L, R: if u > L and R > 0 then
+ *     { u = u - L; go right } else go left.
+ * d_out_idx receives int32[B].  Total 0 records PER_ERR_EMPTY.
+ */
+per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, int mode,
+                      const float* d_u01, int32_t* d_out_idx, void* stream);
+
+/*
+ * per_is_weights -- importance-sampling weights for sampled items d_idx[0..B):
+ *   w_k = (N * P(idx_k))^-beta / max_k (N * P(idx_k))^-beta,
+ * P(i) = pa_i / total, N = size -- computed as (pa_min / pa_{idx_k})^beta
+ * with pa_min the smallest pa in the batch (the max-normalised form; N and the
+ * total cancel).  pa comes from the tree leaves with PER_TREE, else p^alpha of
+ * the raw priorities.  d_out_w receives float32[B]; the largest weight is
+ * exactly 1.  beta >= 0.  A batch containing a zero-priority item yields
+ * non-finite weights.
+ */
+per_status per_is_weights(per_ctx* ctx, const int32_t* d_idx, int32_t B, float beta,
+                          float* d_out_w, void* stream);
+
+/* per_total -- total priority (foxhunt "Integration" / total_priority):
+ * mode PER_TREE reads tree[1], PER_SCAN reads cdf[n-1] (after per_build_cdf).
+ * per_total writes one float to device memory; per_total_host synchronises
+ * `stream` and returns it in *h_out. */
+per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream);
+per_status per_total_host(per_ctx* ctx, int mode, float* h_out, void* stream);
+
+/* Device pointers owned by the context (read-only views, valid until
+ * per_destroy): raw priorities float[capacity], CDF float[capacity] (first
+ * size entries meaningful), tree float[2*capacity_pow2] (NULL without
+ * PER_TREE). */
+const float* per_priorities_ptr(const per_ctx* ctx);
+const float* per_cdf_ptr(const per_ctx* ctx);
+const float* per_tree_ptr(const per_ctx* ctx);
+
+/*
+ * per_check -- synchronise `stream`, read and clear the device status word.
+ * Returns PER_OK, or the first recorded error among PER_ERR_TIMEOUT,
+ * PER_ERR_RANGE, PER_ERR_VALUE, PER_ERR_EMPTY.
+ */
+per_status per_check(per_ctx* ctx, void* stream);
+
+/*
+ * per_resample -- row-batched systematic resampling (POPCORNBENCH particle
+ * filter, reference forward): d_logw is float32[rows][P] row-major (16-byte
+ * aligned, P >= 1, P % 4 == 0, rows >= 1).  Per row b:
+ *   w_i = exp(lw_i - m) / s  (m = row max, s = sum_i exp(lw_i - m)),
+ *   c = cumsum(w),  u_j = fl32(fl32(j + U_b) / P),  U_b in [0, 1)
+ *   idx_j = first i with c_i >= u_j (searchsorted, right=False), clamped P-1
+ * U_b = (x >> 8) * 2^-24 from Philox (offset + b) under key seed, or
+ * d_u_rows[b] when not NULL.  d_out_idx receives int32[rows][P].  If
+ * d_out_cdf is not NULL it receives the float32[rows][P] CDF that was
+ * searched.  Needs no context and no scratch.  A row whose log-weights are
+ * all -inf or contain NaN gives unspecified indices in [0, P).
+ */
+per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t seed,
+                        uint64_t offset, const float* d_u_rows, int32_t* d_out_idx,
+                        float* d_out_cdf, void* stream);
+
+/* Number of this library's kernel launches issued by the calling process so
+ * far (host-side counter; used to report launches per benchmark step). */
+uint64_t per_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PER_GB300_H */
