@@ -38,6 +38,7 @@ SIGNATURES = {
     "per_set_priorities": (ctypes.c_int, [_vp, _vp, _i64, _vp]),
     "per_update": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp]),
     "per_build_cdf": (ctypes.c_int, [_vp, _vp]),
+    "per_build_cdf_noalloc": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp]),
     "per_sample": (ctypes.c_int, [_vp, _i32, _u64, _u64, ctypes.c_int, _vp, _vp, _vp]),
     "per_is_weights": (ctypes.c_int, [_vp, _vp, _i32, _f32, _vp, _vp]),
     "per_total": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp]),
@@ -149,6 +150,17 @@ def per_update(ctx: int, idx: torch.Tensor, prio: torch.Tensor, stream=None) -> 
 
 def per_build_cdf(ctx: int, stream=None) -> None:
     _check("per_build_cdf", lib().per_build_cdf(ctx, _stream(stream)))
+
+
+def per_build_cdf_noalloc(prio: torch.Tensor, alpha: float, out_cdf: torch.Tensor,
+                          status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Context-free build_cdf whose scratch is a fixed array inside the
+    library (for callers that cannot allocate); n <= 2^24."""
+    n = prio.numel()
+    _check("per_build_cdf_noalloc", lib().per_build_cdf_noalloc(
+        _ptr(prio, torch.float32, "prio"), n, alpha, _ptr(out_cdf, torch.float32, "out_cdf", n),
+        _ptr(status, torch.int32, "status", 1), _stream(stream)))
+    return out_cdf
 
 
 def per_sample(ctx: int, B: int, seed: int, offset: int, mode: int, out_idx: torch.Tensor,

@@ -25,6 +25,8 @@
 //    accepts a descriptor only when all four tags match the current call's
 //    epoch, so stale descriptors never need clearing.  The last CTA to finish
 //    resets the ticket counters and advances the epoch.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -338,4 +340,109 @@ per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s) {
     const int64_t big_tiles = (ctx->size + 4095) / 4096;
     if (big_tiles >= 4 * static_cast<int64_t>(ctx->num_sms)) return launch_items<16>(ctx, s);
     return launch_items<4>(ctx, s);
+}
+
+// ====================================================================
+// Allocation-free variant of build_cdf (per_build_cdf_noalloc).
+//
+// Some callers cannot call cudaMalloc: code that runs inside another
+// framework's operator or callback, where the host application owns every
+// byte of device memory through its own pool, or a latency-critical loop in
+// which cudaMalloc's implicit device synchronisation is not acceptable.  This
+// entry point runs the same scan kernel as per_build_cdf, but keeps its
+// lookback descriptors and tile counters in the file-scope array below
+// instead of in a context, so the caller only passes the priorities and the
+// output CDF and nothing is ever allocated.
+//
+// The array is part of the library image: every GPU that loads the library
+// holds it (128 KiB + 128 B) until the process exits.  All calls on a device
+// share it and it keeps the previous call's contents (its counters are left
+// ready for the next call by the kernel itself), so two calls whose kernels
+// overlap on the GPU -- different streams without ordering between them --
+// race on it and give wrong results.  Serialise calls per device.
+// ====================================================================
+
+namespace {
+
+constexpr int64_t kNoAllocMaxN = int64_t(1) << 24;  // 16,777,216 items
+constexpr int64_t kNoAllocMaxTiles = 4096;          // tiles of >= 4096 items at the max size
+constexpr int kNoAllocCtrWords = 8;                 // 16 x u32 counters
+constexpr int kNoAllocMaxDevices = 64;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned long long
+    g_noalloc_scratch[4 * kNoAllocMaxTiles + kNoAllocCtrWords + 8];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+unsigned long long* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+int g_noalloc_sms[kNoAllocMaxDevices] = {};
+
+// Zero the descriptors and counters and start the epoch at 1 (a zero tag
+// means "never written").
+__global__ void noalloc_init_kernel(unsigned long long* scratch) {
+    const int words = 4 * kNoAllocMaxTiles + kNoAllocCtrWords + 8;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) scratch[i] = 0ull;
+}
+
+__global__ void noalloc_epoch_kernel(unsigned* ctrs) { ctrs[CTR_SCAN_EPOCH] = 1u; }
+
+template <int ITEMS>
+per_status noalloc_launch(ScanParams P, cudaStream_t s) {
+    constexpr int TILE = kThreads * ITEMS;
+    const int64_t tiles = (P.n + TILE - 1) / TILE;
+    P.num_tiles = static_cast<unsigned>(tiles);
+    build_cdf_kernel<ITEMS><<<static_cast<unsigned>(tiles), kThreads, 0, s>>>(P);
+    per_note_launch();
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, float* d_cdf,
+                                            int* d_status, void* stream) {
+    if (!d_prio || !d_cdf || n < 1 || n > kNoAllocMaxN || !(alpha >= 0.f) || alpha > 1e30f) return PER_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_prio) & 15u) || (reinterpret_cast<uintptr_t>(d_cdf) & 15u)) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PER_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return PER_ERR_ARG;
+    unsigned long long* scratch = nullptr;
+    {
+        // One-time set-up per device, done by the first call on that device
+        // (with it current): resolve the array's device address -- in host
+        // code the array's name is only a host-side stand-in -- and clear it.
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess) return PER_ERR_CUDA;
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return PER_ERR_CUDA;
+            auto* p = static_cast<unsigned long long*>(addr);
+            noalloc_init_kernel<<<16, 256, 0, s>>>(p);
+            noalloc_epoch_kernel<<<1, 1, 0, s>>>(reinterpret_cast<unsigned*>(p + 4 * kNoAllocMaxTiles));
+            per_note_launch(2);
+            if (cudaGetLastError() != cudaSuccess) return PER_ERR_CUDA;
+            g_noalloc_sms[dev] = sms;
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    ScanParams P;
+    P.p = d_prio;
+    P.cdf = d_cdf;
+    P.n = n;
+    P.alpha = alpha;
+    P.alpha_one = alpha == 1.0f;
+    P.desc = scratch;
+    P.desc_tiles = kNoAllocMaxTiles;
+    P.ctrs = reinterpret_cast<unsigned*>(scratch + 4 * kNoAllocMaxTiles);
+    P.status = d_status ? d_status : reinterpret_cast<int*>(scratch + 4 * kNoAllocMaxTiles + kNoAllocCtrWords);
+    P.num_tiles = 0;
+    // same tile choice as per_build_cdf; at most 4096 tiles for n <= 2^24
+    const int64_t big_tiles = (n + 4095) / 4096;
+    if (big_tiles >= 4 * static_cast<int64_t>(g_noalloc_sms[dev])) return noalloc_launch<16>(P, s);
+    return noalloc_launch<4>(P, s);
 }

@@ -26,9 +26,10 @@
  *     they must stay valid until the stream work that uses them completes.
  *     Host pointers are marked "h_".
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream).  Every call except per_total_host, per_check and per_destroy
- *     is asynchronous and stream-ordered: it allocates nothing, never
- *     synchronises the host, and may be captured in a CUDA graph.
+ *     stream).  Every call except per_total_host, per_check, per_destroy and
+ *     per_build_cdf_noalloc (whose own note below governs it) is asynchronous
+ *     and stream-ordered: it allocates nothing, never synchronises the host,
+ *     and may be captured in a CUDA graph.
  *   - Argument errors return PER_ERR_ARG (or PER_ERR_STATE / PER_ERR_EMPTY)
  *     before anything is launched.  A failed launch returns PER_ERR_CUDA.
  *     Errors found on the device (a bounded wait that ran out, a value out of
@@ -129,6 +130,33 @@ per_status per_update(per_ctx* ctx, const int32_t* d_idx, const float* d_prio, i
  * per_cdf_ptr(); cdf[n-1] is the total.
  */
 per_status per_build_cdf(per_ctx* ctx, void* stream);
+
+/*
+ * per_build_cdf_noalloc -- the build_cdf scan for callers that cannot
+ * allocate device memory.  (The method's sources have no counterpart: it is
+ * an interface addition of this library.)  Some callers cannot call
+ * cudaMalloc -- code running inside another framework's operator or callback
+ * where the host application owns all device memory through its own pool, or
+ * a latency-critical loop where cudaMalloc's implicit device synchronisation
+ * is not acceptable.  This call needs no context: it reads d_prio[0..n)
+ * (float32, >= 0, 16-byte aligned), writes d_cdf[0..n) (16-byte aligned) =
+ * the inclusive prefix sum of d_prio^alpha, with the same kernel and the same
+ * bit-exact result as per_build_cdf, and allocates nothing.
+ *
+ * Its scratch (lookback descriptors and tile counters) is a fixed 128 KiB
+ * array compiled into the library, held by every GPU that loads the library
+ * until the process exits; hence n <= 16,777,216 (2^24), larger n returns
+ * PER_ERR_ARG without launching.  The first call on each device performs a
+ * one-time set-up with that device current (resolves the array's address,
+ * clears it with two small kernels on `stream`); make that first call before
+ * any stream capture.  All calls on a device share the array: calls whose
+ * work overlaps on the GPU (different streams with no ordering between them)
+ * race and give wrong results -- serialise them.  Device-side errors
+ * (negative/NaN priority, range, timeout; the ST_* bits of per_check) are
+ * OR-ed into *d_status when d_status is not NULL.
+ */
+per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, float* d_cdf, int* d_status,
+                                 void* stream);
 
 /*
  * per_sample -- draw B stratified samples (1 <= B <= 2^24):
