@@ -148,54 +148,36 @@ def run_ours(args, rank, world, local_rank):
     ctx = per.PerContext(N, ALPHA, per.PER_SCAN)
     h = ctx.handle
     per.per_set_priorities(h, d_p0)
-    stream = torch.cuda.current_stream()
-    step_counter = [0]
 
-    def one_step(timer=None, e2e=False):
-        s = step_counter[0]
-        step_counter[0] += 1
-        if e2e:
-            d_newp.copy_(h_newp, non_blocking=True)
+    # one step = 32 rounds through the C ABI; captured once as a CUDA graph
+    calls = {
+        "build_cdf": lambda r: per.per_build_cdf(h),
+        "sample": lambda r: per.per_sample(h, B, seed, r * B, per.PER_SCAN, idx[r]),
+        "is_weights": lambda r: per.per_is_weights(h, idx[r], BETA, wts[r]),
+        "update": lambda r: per.per_update(h, idx[r], d_newp[r]),
+    }
+
+    def step_eager():
         for r in range(ROUNDS):
-            off = (s * ROUNDS + r) * B
-            if timer:
-                timer.mark("build_cdf")
-            per.per_build_cdf(h)
-            if timer:
-                timer.mark("sample")
-            per.per_sample(h, B, seed, off, per.PER_SCAN, idx[r])
-            if timer:
-                timer.mark("is_weights")
-            per.per_is_weights(h, idx[r], BETA, wts[r])
-            if timer:
-                timer.mark("update")
-            per.per_update(h, idx[r], d_newp[r])
-        if timer:
-            timer.mark(None)
-        if e2e:
-            h_idx.copy_(idx, non_blocking=True)
-            h_w.copy_(wts, non_blocking=True)
+            for fn in calls.values():
+                fn(r)
 
-    class KernelTimer:
-        """CUDA events between consecutive library calls on the launching stream."""
+    def capture(body):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        before = per.per_launch_count()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        torch.cuda.synchronize()
+        return g, per.per_launch_count() - before
 
-        def __init__(self):
-            self.events = []
-
-        def mark(self, name):
-            ev = torch.cuda.Event(enable_timing=True)
-            ev.record(stream)
-            self.events.append((name, ev))
-
-        def totals(self):
-            out = {}
-            for (name, a), (_, b) in zip(self.events, self.events[1:]):
-                if name is None:
-                    continue
-                t, n = out.get(name, (0.0, 0))
-                out[name] = (t + a.elapsed_time(b), n + 1)
-            self.events = []
-            return out
+    for _ in range(max(args.warmup, 1)):
+        step_eager()  # also configures every kernel before capture
+    torch.cuda.synchronize()
+    step_graph, kernels_per_step = capture(step_eager)
+    kind_graphs = {k: capture(lambda fn=fn: [fn(r) for r in range(ROUNDS)])[0] for k, fn in calls.items()}
+    stream = torch.cuda.current_stream()
 
     def barrier():
         torch.cuda.synchronize()
@@ -203,40 +185,39 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
             torch.cuda.synchronize()
 
-    def timed(steps, e2e=False, timer=None):
-        launches0 = per.per_launch_count()
+    def timed(steps, graph, e2e=False):
         total_ms = 0.0
-        per_kernel = {}
         for _ in range(steps):
             flush.zero_()
             barrier()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            one_step(timer=timer, e2e=e2e)
+            if e2e:
+                d_newp.copy_(h_newp, non_blocking=True)
+            graph.replay()
+            if e2e:
+                h_idx.copy_(idx, non_blocking=True)
+                h_w.copy_(wts, non_blocking=True)
             b.record(stream)
             b.synchronize()
             total_ms += a.elapsed_time(b)
-            if timer:
-                for k, (t, n) in timer.totals().items():
-                    pt, pn = per_kernel.get(k, (0.0, 0))
-                    per_kernel[k] = (pt + t, pn + n)
         barrier()
-        return total_ms, per.per_launch_count() - launches0, per_kernel
+        return total_ms
 
     for _ in range(args.warmup):
-        one_step()
-        one_step(e2e=True)
+        step_graph.replay()
     barrier()
-
     props = torch.cuda.get_device_properties(dev)
-    bus = getattr(props, "pci_bus_id", None)
-    clocks = ClockSampler(bus)
+    clocks = ClockSampler(getattr(props, "pci_bus_id", None))
     clocks.start()
-    timer = KernelTimer()
-    t_ms, launches, per_kernel = timed(args.steps, timer=timer)
+    t_ms = timed(args.steps, step_graph)
     clk = clocks.stop()
-    e2e_ms, _, _ = timed(args.steps, e2e=True)
+    e2e_ms = timed(args.steps, step_graph, e2e=True)
+    # per-kernel durations: each call kind replayed alone (32 launches per
+    # replay, L2 flushed before each replay, as in the step)
+    kreps = max(3, min(args.steps, 50))
+    per_kernel = {k: timed(kreps, g) / (kreps * ROUNDS) for k, g in kind_graphs.items()}
     status = per.per_check(h)
     if status != 0:
         raise RuntimeError(f"device status after timing: {per.per_status_str(status)}")
@@ -254,8 +235,8 @@ def run_ours(args, rank, world, local_rank):
     result = None
     if rank == 0:
         peak, peak_kind = load_peaks()
-        name, (ktot, kn) = max(per_kernel.items(), key=lambda kv: kv[1][0])
-        avg_s = ktot / kn / 1e3
+        name = max(per_kernel, key=per_kernel.get)
+        avg_s = per_kernel[name] / 1e3
         algo = KERNEL_BYTES[name]()
         achieved = algo / avg_s / 1e9
         roofline = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
@@ -270,13 +251,15 @@ def run_ours(args, rank, world, local_rank):
             "e2e": {"value": samples / (e2e_ms / 1e3), "unit": UNIT,
                     "h2d_bytes_per_step": int(ROUNDS * B * 4),
                     "d2h_bytes_per_step": int(ROUNDS * B * 8)},
-            "gpu_launches": int(launches),
+            "gpu_launches": int(kernels_per_step * args.steps),
             "roofline": roofline,
-            "kernel_us_per_step": {k: round(t / args.steps * 1e3, 2) for k, (t, n) in per_kernel.items()},
-            "build_cdf_gbs": round(KERNEL_BYTES["build_cdf"]() / (per_kernel["build_cdf"][0] /
-                                                                 per_kernel["build_cdf"][1] / 1e3) / 1e9, 1),
+            "kernel_us_per_launch": {k: round(v * 1e3, 3) for k, v in per_kernel.items()},
+            "build_cdf_gbs": round(KERNEL_BYTES["build_cdf"]() / (per_kernel["build_cdf"] / 1e3) / 1e9, 1),
+            "us_per_round": round(t_ms / args.steps / ROUNDS * 1e3, 2),
             "clocks": clk,
             "impl": "gb300",
+            "notes": "step = one CUDA-graph replay of 32 rounds through the C ABI; RNG offsets are fixed per "
+                     "captured round while the priority state evolves across steps",
         }
         if not args.no_extras:
             result["extras"] = extras(per, torch, dev, peak)
@@ -429,7 +412,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-extras", action="store_true")

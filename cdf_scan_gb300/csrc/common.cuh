@@ -129,7 +129,49 @@ __device__ __forceinline__ float stratified_threshold(int k, float U, float fB, 
     return __fmul_rn(b, T);
 }
 
+// ---- x^alpha ---------------------------------------------------------------
+// x^alpha = 2^(alpha * log2 x), with x = m * 2^e (m in [1, 2)):
+//   alpha*e is split exactly into p + pe (fma gives the product's rounding
+//   error), n = rint(p), and the small remainder r = (p - n) + (pe + alpha *
+//   log2 m) goes through the hardware base-2 exponential; the result is
+//   2^r * 2^n.  Hardware lg2/ex2 approximations (PTX lg2.approx / ex2.approx)
+//   bound the error to a few ulp for alpha in [0, 1]; zero, subnormal,
+//   infinite, negative and NaN inputs take CUDA's powf (C pow semantics).
+
+__device__ __forceinline__ float hw_lg2(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float hw_ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float pow_fast(float x, float alpha) {
+    const unsigned bits = __float_as_uint(x);
+    if (bits - 0x00800000u >= 0x7f000000u) return powf(x, alpha);  // not a positive normal
+    const float e = static_cast<float>(static_cast<int>(bits >> 23) - 127);
+    const float m = __uint_as_float((bits & 0x007fffffu) | 0x3f800000u);
+    const float f = hw_lg2(m);                // [0, 1)
+    const float p = __fmul_rn(alpha, e);
+    const float pe = __fmaf_rn(alpha, e, -p);  // alpha*e - p exactly
+    const float n = rintf(p);
+    const float r = __fadd_rn(__fsub_rn(p, n), __fmaf_rn(alpha, f, pe));
+    const float y = hw_ex2(r);
+    const int ni = static_cast<int>(n);
+    if (ni > 126 || ni < -126) return ldexpf(y, ni);
+    return __fmul_rn(y, __int_as_float((ni + 127) << 23));
+}
+
 // p^alpha; alpha == 1 skips the power (exact).
 __device__ __forceinline__ float pow_alpha(float x, float alpha, bool identity) {
+    return identity ? x : pow_fast(x, alpha);
+}
+
+// Accurate power (CUDA powf), for quantities with a tight error budget.
+__device__ __forceinline__ float pow_accurate(float x, float alpha, bool identity) {
     return identity ? x : powf(x, alpha);
 }

@@ -23,8 +23,6 @@ enum : int {
     CTR_UPD_EPOCH = 3,    // tags winner slots of the current update (>= 1)
     CTR_UPD_DONE = 4,     // CTAs finished in the running update-apply
     CTR_ISW_MIN = 5,      // running min of pa (float bits) for IS weights
-    CTR_ISW_BAR_COUNT = 6,
-    CTR_ISW_BAR_GEN = 7,
     CTR_ISW_DONE = 8,
     NUM_CTRS = 16
 };
@@ -49,6 +47,14 @@ struct per_ctx {
     unsigned* ctrs;                   // [NUM_CTRS]
     int* status;                      // device status word
 };
+
+// 64-bit words of scan state for up to `tiles` tiles: per tile a 4-word
+// inclusive record and a 1-word aggregate; per group of 32 tiles a 4-word
+// group sum and a 32-bit arrival counter.
+inline int64_t scan_state_words(int64_t tiles) {
+    const int64_t groups = tiles / 32 + 1;
+    return 5 * tiles + 4 * groups + (groups + 1) / 2 + 1;
+}
 
 // Host-side launch accounting (per_launch_count).
 void per_note_launch(int n = 1);

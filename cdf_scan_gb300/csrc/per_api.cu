@@ -88,7 +88,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
               alloc_zero(&c->status, 1, s) == cudaSuccess;
     if (ok && (flags & PER_SCAN))
         ok = alloc_zero(&c->cdf, c->alloc_n, s) == cudaSuccess &&
-             alloc_zero(&c->scan_desc, 4 * static_cast<size_t>(c->scan_desc_tiles), s) == cudaSuccess;
+             alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok) {
         // epochs start at 1 (0 marks "never written"); the IS-weight minimum

@@ -144,7 +144,7 @@ __global__ void leaves_from_prio_kernel(float* __restrict__ tree, const float* _
     if (i < n) {
         const float p = prio[i];
         if (!(p >= 0.f)) atomicOr(status, ST_VALUE);
-        v = pow_alpha(p, alpha, alpha_one);
+        v = pow_accurate(p, alpha, alpha_one);
     }
     tree[cap_pow2 + i] = v;
 }
@@ -177,7 +177,7 @@ __global__ void apply_winners_kernel(const int32_t* __restrict__ idx, const floa
             const float v = p[k];
             if (!(v >= 0.f)) atomicOr(status, ST_VALUE);
             prio[i] = v;
-            if (tree) tree[cap_pow2 + i] = pow_alpha(v, alpha, alpha_one);
+            if (tree) tree[cap_pow2 + i] = pow_accurate(v, alpha, alpha_one);
         }
     }
     // the last CTA advances the epoch for the next update
@@ -192,164 +192,230 @@ __global__ void apply_winners_kernel(const int32_t* __restrict__ idx, const floa
 }
 
 // ====================================================== small-batch update ===
+//
+// One CTA.  (1) Each index is inserted into a shared-memory hash table
+// (index -> largest batch position, via atomicCAS / atomicMax), so the last
+// occurrence of every index wins; the winners write raw priority and leaf.
+// (2) The dirty part of the tree is recomputed in passes of six levels: for
+// every updated leaf, the 64-wide subtree (64 nodes of the pass's bottom
+// level) containing it is recomputed by one warp -- each lane adds one pair,
+// then five shuffle levels -- and all its 63 nodes are written.  Clean nodes
+// of a dirty subtree are rewritten with the value they already hold (every
+// stored node equals the sum of its stored children), so the result is the
+// full pairwise rebuild, bit for bit, and concurrent writers of one node
+// always write the same value.  A per-pass hash set skips subtrees already
+// claimed by another index.
 
-constexpr int kSmallN = 1024;       // one key per thread
-constexpr int kSmallMaxDepth = 20;  // cap_pow2 <= 2^20
-// Entries over all levels: sum_d min(2^d, 1024) for d = 0..20.
-constexpr int kListCap = 1023 + 1024 * 11;
+constexpr int kSmallN = 4096;            // indices per batch on this path
+constexpr int kSmallThreads = 1024;
+constexpr int kHashSlots = 2 * kSmallN;  // power of two
+constexpr unsigned kEmpty = 0xffffffffu;
 
 struct SmallSmem {
-    unsigned long long key[kSmallN];
-    int node[kListCap];
-    float val[kListCap];
-    float sib[kListCap];
-    unsigned short cstart[kListCap];
-    int level_off[kSmallMaxDepth + 2];
-    int level_cnt[kSmallMaxDepth + 2];
-    int warp_cnt[32];
+    unsigned key[kHashSlots];    // index -> slot
+    int pos[kHashSlots];         // largest batch position of the slot's index
+    unsigned claim[kHashSlots];  // subtrees claimed in the current pass
+    int slot_of[kSmallN];        // slot of batch entry k (-1: invalid index)
+    unsigned leaf[kSmallN];      // distinct updated leaves
+    unsigned job[kSmallN];       // distinct subtrees of the current pass
+    int n_leaf, n_job;
 };
 
-// Block-wide exclusive count of `flag` over the 1024 threads; returns the
-// thread's offset and writes the total to *total (all threads).
-__device__ __forceinline__ int block_excl_count(bool flag, int* warp_cnt, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned m = __ballot_sync(PER_FULL_MASK, flag);
-    if (lane == 0) warp_cnt[warp] = __popc(m);
-    __syncthreads();
-    const int c = warp_cnt[lane];
-    int incl = c;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(PER_FULL_MASK, incl, d);
-        if (lane >= d) incl += y;
-    }
-    const int warp_excl = __shfl_sync(PER_FULL_MASK, incl - c, warp);
-    *total = __shfl_sync(PER_FULL_MASK, incl, 31);
-    __syncthreads();  // warp_cnt may be reused
-    return warp_excl + __popc(m & ((1u << lane) - 1u));
+__device__ __forceinline__ unsigned hash_u32(unsigned x) {
+    x ^= x >> 16;
+    x *= 0x7feb352dU;
+    x ^= x >> 15;
+    x *= 0x846ca68bU;
+    x ^= x >> 16;
+    return x;
 }
 
-__global__ void __launch_bounds__(kSmallN) small_update_kernel(const int32_t* __restrict__ idx,
-                                                               const float* __restrict__ p, int n,
-                                                               int64_t capacity, float* __restrict__ prio,
-                                                               float* __restrict__ tree, int log2cap,
-                                                               float alpha, bool alpha_one, int* status) {
+// Insert `key` into a table of kHashSlots slots (at most kSmallN keys, so a
+// free slot always exists); returns its slot and whether this call created it.
+__device__ __forceinline__ int hash_insert(unsigned* keys, unsigned key, bool& inserted) {
+    unsigned h = hash_u32(key) & (kHashSlots - 1);
+    for (int probe = 0; probe < kHashSlots; ++probe) {
+        const unsigned prev = atomicCAS(&keys[h], kEmpty, key);
+        if (prev == kEmpty || prev == key) {
+            inserted = prev == kEmpty;
+            return static_cast<int>(h);
+        }
+        h = (h + 1) & (kHashSlots - 1);
+    }
+    inserted = false;
+    return -1;
+}
+
+// One warp recomputes up to kJobBatch subtrees at once.  Subtree j has bottom
+// nodes [first_j, first_j + width) (width a power of two, 2..64) and is
+// recomputed through log2(width) levels: lane l adds bottom pair l, then
+// shuffles combine neighbours, always left + right.  The batch is processed
+// level by level, so the kJobBatch shuffle chains are independent and their
+// latencies overlap.
+constexpr int kJobBatch = 8;
+
+__device__ __forceinline__ void recompute_subtrees(float* tree, const unsigned* first, int count, int width,
+                                                   int lane) {
+    const int levels = 31 - __clz(width);
+    const bool active = 2 * lane < width;
+    float v[kJobBatch];
+    unsigned node[kJobBatch];
+#pragma unroll
+    for (int j = 0; j < kJobBatch; ++j) {
+        float2 ab = make_float2(0.f, 0.f);
+        const unsigned f = j < count ? first[j] : 0u;
+        if (j < count && active)  // plain loads: written earlier by this CTA or cluster
+            ab = *reinterpret_cast<const float2*>(tree + f + 2 * lane);
+        v[j] = __fadd_rn(ab.x, ab.y);
+        node[j] = (f >> 1) + lane;
+    }
+#pragma unroll
+    for (int j = 0; j < kJobBatch; ++j)
+        if (j < count && active) tree[node[j]] = v[j];
+    for (int l = 1; l < levels; ++l) {
+        const unsigned delta = 1u << (l - 1);
+        const bool writer = active && (lane & ((1 << l) - 1)) == 0;
+        float right[kJobBatch];
+#pragma unroll
+        for (int j = 0; j < kJobBatch; ++j) right[j] = __shfl_down_sync(PER_FULL_MASK, v[j], delta);
+#pragma unroll
+        for (int j = 0; j < kJobBatch; ++j) {
+            node[j] >>= 1;
+            if (writer) {
+                v[j] = __fadd_rn(v[j], right[j]);
+                if (j < count) tree[node[j]] = v[j];
+            }
+        }
+    }
+}
+
+// Append `value` to list[*count] for every lane with `take`, one shared
+// atomic per warp.
+__device__ __forceinline__ void warp_append(bool take, unsigned value, unsigned* list, int* count, int lane) {
+    const unsigned m = __ballot_sync(PER_FULL_MASK, take);
+    if (!m) return;
+    int base = 0;
+    const int leader = __ffs(m) - 1;
+    if (lane == leader) base = atomicAdd(count, __popc(m));
+    base = __shfl_sync(PER_FULL_MASK, base, leader);
+    if (take) list[base + __popc(m & ((1u << lane) - 1u))] = value;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Launched as one cluster of C CTAs (C a power of two, 1..16, C <= cap/64).
+// CTA r owns the leaves under node C + r, i.e. items [r*cap/C, (r+1)*cap/C):
+// every duplicate of an index lands in the same CTA, so the last-writer rule
+// and the subtree recompute are CTA-local and the C subtrees are disjoint.
+// After one cluster barrier CTA 0 recomputes the top log2(C) levels.
+__global__ void __launch_bounds__(kSmallThreads) small_update_kernel(const int32_t* __restrict__ idx,
+                                                                     const float* __restrict__ p, int n,
+                                                                     int64_t capacity, float* __restrict__ prio,
+                                                                     float* tree, int log2cap, float alpha,
+                                                                     bool alpha_one, int* status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SmallSmem& S = *reinterpret_cast<SmallSmem*>(smem_raw);
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarpsPerCta = kSmallThreads / 32;
     const unsigned cap_pow2 = 1u << log2cap;
+    const unsigned C = gridDim.x;               // cluster size == grid size
+    const unsigned rank = cluster_ctarank();
+    const int top = 31 - __clz(C);              // level of the CTA subtree roots
+    const unsigned span = cap_pow2 >> top;      // leaves per CTA
+    const unsigned lo = rank * span;
 
-    // ---- keys: (index << 32) | position; invalid / absent -> all ones -----
-    unsigned long long key = ~0ull;
-    if (tid < n) {
-        const int32_t i = idx[tid];
-        if (i >= 0 && i < capacity) key = (static_cast<unsigned long long>(i) << 32) | static_cast<unsigned>(tid);
-        else atomicOr(status, ST_VALUE);
+    for (int i = tid; i < kHashSlots; i += kSmallThreads) {
+        S.key[i] = kEmpty;
+        S.pos[i] = -1;
+        S.claim[i] = kEmpty;
     }
-    // ---- bitonic sort, ascending (shuffles below stride 32, smem above) ----
-    for (int size = 2; size <= kSmallN; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const bool up = (tid & size) == 0;
-            unsigned long long other;
-            if (stride >= 32) {
-                S.key[tid] = key;
-                __syncthreads();
-                other = S.key[tid ^ stride];
-                __syncthreads();
-            } else {
-                other = __shfl_xor_sync(PER_FULL_MASK, key, stride);
+    if (tid == 0) S.n_leaf = 0;
+    __syncthreads();
+
+    // ---- (1) the last occurrence of each index wins ---------------------------
+    for (int k = tid; k < n; k += kSmallThreads) {
+        const int32_t i = idx[k];
+        int slot = -1;
+        if (i >= 0 && i < capacity) {
+            if (static_cast<unsigned>(i) - lo < span) {
+                bool ins;
+                slot = hash_insert(S.key, static_cast<unsigned>(i), ins);
+                atomicMax(&S.pos[slot], k);
             }
-            const bool lower = (tid & stride) == 0;
-            const bool take_min = (lower == up);
-            key = take_min ? (other < key ? other : key) : (other > key ? other : key);
+        } else if (rank == 0) {
+            atomicOr(status, ST_VALUE);
         }
-    }
-    S.key[tid] = key;
-    __syncthreads();
-
-    // ---- last occurrence of each index wins; write its leaf ----------------
-    const bool valid = key != ~0ull;
-    const unsigned my_index = static_cast<unsigned>(key >> 32);
-    bool winner = false;
-    if (valid) {
-        const unsigned long long next = tid + 1 < kSmallN ? S.key[tid + 1] : ~0ull;
-        winner = next == ~0ull || static_cast<unsigned>(next >> 32) != my_index;
-    }
-    int total;
-    const int e = block_excl_count(winner, S.warp_cnt, &total);
-    if (tid == 0) {
-        S.level_off[log2cap] = 0;
-        S.level_cnt[log2cap] = total;
-    }
-    if (winner) {
-        const float v = p[static_cast<unsigned>(key)];
-        if (!(v >= 0.f)) atomicOr(status, ST_VALUE);
-        const float leaf = pow_alpha(v, alpha, alpha_one);
-        prio[my_index] = v;
-        tree[cap_pow2 + my_index] = leaf;
-        S.node[e] = static_cast<int>(cap_pow2 + my_index);
-        S.val[e] = leaf;
+        S.slot_of[k] = slot;
     }
     __syncthreads();
+    for (int k0 = 0; k0 < n; k0 += kSmallThreads) {  // warp-uniform trip count
+        const int k = k0 + tid;
+        bool win = false;
+        unsigned i = 0;
+        if (k < n) {
+            const int slot = S.slot_of[k];
+            if (slot >= 0 && S.pos[slot] == k) {
+                win = true;
+                i = S.key[slot];
+                const float v = p[k];
+                if (!(v >= 0.f)) atomicOr(status, ST_VALUE);
+                prio[i] = v;
+                tree[cap_pow2 + i] = pow_accurate(v, alpha, alpha_one);
+            }
+        }
+        warp_append(win, i, S.leaf, &S.n_leaf, lane);
+    }
+    __syncthreads();
+    const int n_leaf = S.n_leaf;
 
-    // ---- dirty-node lists, one level at a time (sorted, unique) ------------
-    for (int d = log2cap; d > 0; --d) {
-        const int off = S.level_off[d], cnt = S.level_cnt[d];
-        const int next_off = off + cnt;
-        bool first = false;
-        int parent = 0;
-        if (tid < cnt) {
-            parent = S.node[off + tid] >> 1;
-            first = tid == 0 || (S.node[off + tid - 1] >> 1) != parent;
-        }
-        int pcount;
-        const int pe = block_excl_count(first, S.warp_cnt, &pcount);
-        if (first) {
-            S.node[next_off + pe] = parent;
-            S.cstart[next_off + pe] = static_cast<unsigned short>(off + tid);
-        }
-        if (tid == 0) {
-            S.level_off[d - 1] = next_off;
-            S.level_cnt[d - 1] = pcount;
+    // ---- (2) recompute this CTA's dirty subtrees, six levels per pass ---------
+    for (int bottom = log2cap; bottom > top;) {
+        const int levels = bottom - top < 6 ? bottom - top : 6;
+        const int width = 1 << levels;
+        const int shift = (log2cap - bottom) + levels;  // leaf >> shift = subtree number
+        if (tid == 0) S.n_job = 0;
+        __syncthreads();
+        for (int w0 = 0; w0 < n_leaf; w0 += kSmallThreads) {  // warp-uniform trip count
+            const int w = w0 + tid;
+            const bool has = w < n_leaf;
+            const unsigned sub = has ? S.leaf[w] >> shift : 0xffffffffu;
+            // one claim per distinct subtree of the warp, then one per table
+            const unsigned same = __match_any_sync(PER_FULL_MASK, sub);
+            bool ins = false;
+            if (has && lane == __ffs(same) - 1) hash_insert(S.claim, sub, ins);
+            warp_append(ins, sub, S.job, &S.n_job, lane);
         }
         __syncthreads();
+        const int n_job = S.n_job;
+        for (int j0 = warp * kJobBatch; j0 < n_job; j0 += kWarpsPerCta * kJobBatch) {
+            unsigned first[kJobBatch];
+            const int count = n_job - j0 < kJobBatch ? n_job - j0 : kJobBatch;
+#pragma unroll
+            for (int j = 0; j < kJobBatch; ++j)
+                first[j] = j < count ? (1u << bottom) + S.job[j0 + j] * static_cast<unsigned>(width) : 0u;
+            recompute_subtrees(tree, first, count, width, lane);
+        }
+        for (int i = tid; i < kHashSlots; i += kSmallThreads) S.claim[i] = kEmpty;
+        __syncthreads();  // this pass's nodes written (visible to the CTA) and claims cleared
+        bottom -= levels;
     }
 
-    // ---- one parallel round: fetch every clean sibling of a dirty node -----
-    const int entries = S.level_off[0] + S.level_cnt[0];
-    for (int d = log2cap; d > 0; --d) {
-        const int off = S.level_off[d], cnt = S.level_cnt[d];
-        for (int t = tid; t < cnt; t += kSmallN) {
-            const int j = S.node[off + t];
-            const bool left = (j & 1) == 0;
-            const bool sib_dirty = left ? (t + 1 < cnt && S.node[off + t + 1] == j + 1)
-                                        : (t > 0 && S.node[off + t - 1] == j - 1);
-            S.sib[off + t] = sib_dirty ? 0.f : __ldg(tree + (j ^ 1));
+    // ---- (3) the top levels, from the C subtree roots ---------------------------
+    if (C > 1) {
+        cluster_sync_all();  // every CTA's subtree root is written (release/acquire)
+        if (rank == 0 && warp == 0) {
+            const unsigned first = C;  // nodes [C, 2C) are the subtree roots
+            recompute_subtrees(tree, &first, 1, static_cast<int>(C), lane);
         }
-    }
-    (void)entries;
-    __syncthreads();
-
-    // ---- recompute dirty nodes bottom-up in the fixed left + right order ---
-    for (int d = log2cap - 1; d >= 0; --d) {
-        const int off = S.level_off[d], cnt = S.level_cnt[d];
-        const int coff = S.level_off[d + 1], ccnt = S.level_cnt[d + 1];
-        for (int t = tid; t < cnt; t += kSmallN) {
-            const int j = S.node[off + t];
-            const int c0 = S.cstart[off + t];
-            float left, right;
-            if (S.node[c0] == 2 * j) {
-                left = S.val[c0];
-                right = (c0 + 1 < coff + ccnt && S.node[c0 + 1] == 2 * j + 1) ? S.val[c0 + 1] : S.sib[c0];
-            } else {
-                left = S.sib[c0];
-                right = S.val[c0];
-            }
-            const float v = __fadd_rn(left, right);
-            S.val[off + t] = v;
-            tree[j] = v;
-        }
-        __syncthreads();
     }
 }
 
@@ -389,19 +455,57 @@ per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s) {
 
 per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n, cudaStream_t s) {
     const bool has_tree = (ctx->flags & PER_TREE) != 0;
-    if (has_tree && n <= kSmallN && ctx->log2_cap <= kSmallMaxDepth) {
-        static bool attr_set = false;  // per process; the attribute is per function
+    if (has_tree && n <= kSmallN) {
         const size_t smem = sizeof(SmallSmem);
-        if (!attr_set) {
+        static int max_cluster = 0;  // largest schedulable cluster size (per process)
+        if (max_cluster == 0) {
             if (cudaFuncSetAttribute(small_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)) != cudaSuccess)
                 return PER_ERR_CUDA;
-            attr_set = true;
+            const bool nonportable = cudaFuncSetAttribute(small_update_kernel,
+                                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                                     cudaSuccess;
+            cudaGetLastError();
+            max_cluster = 1;
+            for (int c = nonportable ? 16 : 8; c > 1; c >>= 1) {
+                cudaLaunchConfig_t q = {};
+                q.gridDim = dim3(c);
+                q.blockDim = dim3(kSmallThreads);
+                q.dynamicSmemBytes = smem;
+                cudaLaunchAttribute qa[1];
+                qa[0].id = cudaLaunchAttributeClusterDimension;
+                qa[0].val.clusterDim.x = c;
+                qa[0].val.clusterDim.y = 1;
+                qa[0].val.clusterDim.z = 1;
+                q.attrs = qa;
+                q.numAttrs = 1;
+                int nc = 0;
+                if (cudaOccupancyMaxActiveClusters(&nc, small_update_kernel, &q) == cudaSuccess && nc > 0) {
+                    max_cluster = c;
+                    break;
+                }
+                cudaGetLastError();
+            }
         }
-        small_update_kernel<<<1, kSmallN, smem, s>>>(idx, p, n, ctx->capacity, ctx->prio, ctx->tree,
-                                                     ctx->log2_cap, ctx->alpha, ctx->alpha == 1.0f, ctx->status);
+        int C = max_cluster;
+        while (C > 1 && (ctx->cap_pow2 >> 6) < C) C >>= 1;  // at least 64 leaves per CTA
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(C));
+        cfg.blockDim = dim3(kSmallThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, small_update_kernel, idx, p, n, ctx->capacity, ctx->prio,
+                                                 ctx->tree, ctx->log2_cap, ctx->alpha, ctx->alpha == 1.0f,
+                                                 ctx->status);
         per_note_launch();
-        return cuda_status(cudaGetLastError());
+        return cuda_status(e);
     }
     const unsigned grid = static_cast<unsigned>((n + 255) / 256);
     elect_last_writer_kernel<<<grid, 256, 0, s>>>(idx, n, ctx->capacity, ctx->winner, ctx->ctrs, ctx->status);
