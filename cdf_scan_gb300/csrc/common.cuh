@@ -23,6 +23,12 @@ __device__ __forceinline__ void st_relaxed_v2(unsigned long long* p, unsigned lo
     asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
     unsigned v;
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -150,25 +156,68 @@ __device__ __forceinline__ float hw_ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ float pow_fast(float x, float alpha) {
-    const unsigned bits = __float_as_uint(x);
-    if (bits - 0x00800000u >= 0x7f000000u) return powf(x, alpha);  // not a positive normal
-    const float e = static_cast<float>(static_cast<int>(bits >> 23) - 127);
-    const float m = __uint_as_float((bits & 0x007fffffu) | 0x3f800000u);
-    const float f = hw_lg2(m);                // [0, 1)
-    const float p = __fmul_rn(alpha, e);
-    const float pe = __fmaf_rn(alpha, e, -p);  // alpha*e - p exactly
-    const float n = rintf(p);
-    const float r = __fadd_rn(__fsub_rn(p, n), __fmaf_rn(alpha, f, pe));
-    const float y = hw_ex2(r);
-    const int ni = static_cast<int>(n);
-    if (ni > 126 || ni < -126) return ldexpf(y, ni);
-    return __fmul_rn(y, __int_as_float((ni + 127) << 23));
+// Inputs that are not positive normal floats (zero, subnormal, infinite,
+// negative, NaN) take CUDA's powf; kept out of line so the fast path stays
+// small at every call site.  `bad` is set for negative and NaN inputs.
+static __device__ __noinline__ float pow_special(float x, float alpha, bool* bad) {
+    if (!(x >= 0.f)) *bad = true;
+    return powf(x, alpha);
 }
 
-// p^alpha; alpha == 1 skips the power (exact).
-__device__ __forceinline__ float pow_alpha(float x, float alpha, bool identity) {
-    return identity ? x : pow_fast(x, alpha);
+__device__ __forceinline__ float pow_fast(float x, float alpha, bool& bad) {
+    const unsigned bits = __float_as_uint(x);
+    if (bits - 0x00800000u >= 0x7f000000u) return pow_special(x, alpha, &bad);
+    // e = unbiased exponent as a float, without an int->float conversion:
+    // 2^23 + biased exponent, minus 2^23 + 127
+    const float e = __fsub_rn(__uint_as_float(0x4B000000u | (bits >> 23)), 8388735.0f);
+    const float m = __uint_as_float((bits & 0x007fffffu) | 0x3f800000u);  // [1, 2)
+    const float f = hw_lg2(m);                                             // [0, 1)
+    const float p = __fmul_rn(alpha, e);
+    const float pe = __fmaf_rn(alpha, e, -p);  // alpha*e - p exactly
+    // n = rint(p) by the 1.5*2^23 magic-number addition; its low bits give n
+    const float big = __fadd_rn(p, 12582912.0f);
+    const float n = __fsub_rn(big, 12582912.0f);
+    const int ni = static_cast<int>(__float_as_uint(big) - 0x4B400000u);
+    const float r = __fadd_rn(__fsub_rn(p, n), __fmaf_rn(alpha, f, pe));
+    const float y = hw_ex2(r);
+    if (ni > 126 || ni < -126) return ldexpf(y, ni);
+    return __fmul_rn(y, __uint_as_float(static_cast<unsigned>(ni + 127) << 23));  // y * 2^n
+}
+
+// p^alpha for four values at once (the scan's hot path).  For |log2 x| < 16,
+// i.e. x in (2^-16, 2^16), x^alpha = ex2(alpha * lg2(x)) directly: the
+// hardware lg2 (absolute error ~2^-22.6), the fp32 rounding of L = lg2(x)
+// (<= 2^-21 for |L| < 16), the rounding of alpha*L (<= 2^-21) and the
+// hardware ex2 (~2^-22.5 relative) bound the relative error by ~1e-6.  Any
+// other input -- tiny, huge, zero, subnormal, infinite, negative, NaN (the
+// range test is false for NaN) -- takes pow_fast's exact exponent split.
+// mode: 0 = x^alpha, 1 = alpha == 1 (x), 2 = alpha == 0 (1).
+__device__ __forceinline__ float4 pow4_alpha(float4 q, float alpha, int mode, bool& bad) {
+    if (mode != 0) {
+        const float4 one = make_float4(1.f, 1.f, 1.f, 1.f);
+        if (!(q.x >= 0.f && q.y >= 0.f && q.z >= 0.f && q.w >= 0.f)) bad = true;
+        return mode == 1 ? q : one;
+    }
+    const float l0 = hw_lg2(q.x), l1 = hw_lg2(q.y), l2 = hw_lg2(q.z), l3 = hw_lg2(q.w);
+    const float lmax = fmaxf(fmaxf(fabsf(l0), fabsf(l1)), fmaxf(fabsf(l2), fabsf(l3)));
+    if (lmax < 16.f) {  // false for NaN
+        return make_float4(hw_ex2(__fmul_rn(alpha, l0)), hw_ex2(__fmul_rn(alpha, l1)),
+                           hw_ex2(__fmul_rn(alpha, l2)), hw_ex2(__fmul_rn(alpha, l3)));
+    }
+    return make_float4(fabsf(l0) < 16.f ? hw_ex2(__fmul_rn(alpha, l0)) : pow_fast(q.x, alpha, bad),
+                       fabsf(l1) < 16.f ? hw_ex2(__fmul_rn(alpha, l1)) : pow_fast(q.y, alpha, bad),
+                       fabsf(l2) < 16.f ? hw_ex2(__fmul_rn(alpha, l2)) : pow_fast(q.z, alpha, bad),
+                       fabsf(l3) < 16.f ? hw_ex2(__fmul_rn(alpha, l3)) : pow_fast(q.w, alpha, bad));
+}
+
+// p^alpha; alpha == 1 skips the power (exact).  `bad` is set for negative
+// and NaN inputs.
+__device__ __forceinline__ float pow_alpha(float x, float alpha, bool identity, bool& bad) {
+    if (identity) {
+        bad |= !(x >= 0.f);
+        return x;
+    }
+    return pow_fast(x, alpha, bad);
 }
 
 // Accurate power (CUDA powf), for quantities with a tight error budget.

@@ -48,13 +48,9 @@ struct per_ctx {
     int* status;                      // device status word
 };
 
-// 64-bit words of scan state for up to `tiles` tiles: per tile a 4-word
-// inclusive record and a 1-word aggregate; per group of 32 tiles a 4-word
-// group sum and a 32-bit arrival counter.
-inline int64_t scan_state_words(int64_t tiles) {
-    const int64_t groups = tiles / 32 + 1;
-    return 5 * tiles + 4 * groups + (groups + 1) / 2 + 1;
-}
+// 64-bit words of scan state for up to `tiles` tiles: one tagged aggregate
+// word per tile.
+inline int64_t scan_state_words(int64_t tiles) { return tiles + 1; }
 
 // Host-side launch accounting (per_launch_count).
 void per_note_launch(int n = 1);

@@ -43,6 +43,7 @@ struct ScanParams {
     int64_t n;
     float alpha;
     bool alpha_one;
+    int pow_mode;  // 0: x^alpha, 1: alpha == 1, 2: alpha == 0
     unsigned long long* desc;
     int64_t desc_tiles;
     unsigned* ctrs;
@@ -98,52 +99,20 @@ __device__ __forceinline__ u128 warp_sum_u128(u128 v) {
     return v;
 }
 
-__device__ __forceinline__ void publish(unsigned long long* d, unsigned tag, u128 v) {
-    const unsigned long long t = static_cast<unsigned long long>(tag) << 32;
-    uint64_t lo = static_cast<uint64_t>(v), hi = static_cast<uint64_t>(v >> 64);
-    st_relaxed_v2(d, t | (lo & 0xffffffffull), t | (lo >> 32));
-    st_relaxed_v2(d + 2, t | (hi & 0xffffffffull), t | (hi >> 32));
-}
-
-// Reads descriptor `d`: 0 = not yet published this call, 1 = aggregate,
-// 2 = inclusive prefix.
-__device__ __forceinline__ int read_desc(const unsigned long long* d, unsigned tag_agg, u128& v) {
-    unsigned long long w0, w1, w2, w3;
-    ld_relaxed_v2(d, w0, w1);
-    ld_relaxed_v2(d + 2, w2, w3);
-    unsigned g0 = static_cast<unsigned>(w0 >> 32), g1 = static_cast<unsigned>(w1 >> 32);
-    unsigned g2 = static_cast<unsigned>(w2 >> 32), g3 = static_cast<unsigned>(w3 >> 32);
-    if (g0 != g1 || g1 != g2 || g2 != g3 || (g0 != tag_agg && g0 != tag_agg + 1u)) return 0;
-    uint64_t lo = (w0 & 0xffffffffull) | ((w1 & 0xffffffffull) << 32);
-    uint64_t hi = (w2 & 0xffffffffull) | ((w3 & 0xffffffffull) << 32);
-    v = (static_cast<u128>(hi) << 64) | lo;
-    return g0 == tag_agg ? 1 : 2;
-}
-
 // ---- scan state in global memory ---------------------------------------------
-// For every tile t: aggw[t] = (tag << 32) | fp32 bits of the tile sum, tag
-// 2*epoch (aggregate published) or 2*epoch+1 (inclusive prefix published in
-// inc[t]); inc[t] = 4 tagged words holding the exact 128-bit inclusive prefix.
-// For every full group of 32 tiles: gagg[g] = 4 tagged words holding the
-// group's exact sum, published by the group's last tile to arrive (counted
-// in gcnt[g], which grows by exactly 32 per call, so no reset is needed).
+// One word per tile: aggw[t] = (2*epoch << 32) | fp32 bits of the tile sum,
+// written once per call when the tile has been scanned locally.  A reader
+// accepts it only with the current call's tag, so stale words never need
+// clearing.
 struct ScanState {
     unsigned long long* aggw;
-    unsigned long long* inc;
-    unsigned long long* gagg;
-    unsigned* gcnt;
 };
 
 __device__ __forceinline__ ScanState scan_state(const ScanParams& P) {
     ScanState S;
-    S.inc = P.desc;
-    S.aggw = P.desc + 4 * P.desc_tiles;
-    S.gagg = S.aggw + P.desc_tiles;
-    S.gcnt = reinterpret_cast<unsigned*>(S.gagg + 4 * (P.desc_tiles / 32 + 1));
+    S.aggw = P.desc;
     return S;
 }
-
-constexpr int kGroupQ = 4;  // group rounds per poll: 128 groups (4096 tiles) of reach
 
 __device__ __forceinline__ void spin_pause(unsigned& spins, bool& timed_out, int lane, int* status) {
     if (++spins > kSpinLimit) {
@@ -154,148 +123,45 @@ __device__ __forceinline__ void spin_pause(unsigned& spins, bool& timed_out, int
     if (spins > 8) __nanosleep(spins < 64 ? 64 : 256);
 }
 
-// Inclusive prefix of tile `t` from its record (all lanes; waits until valid).
-__device__ u128 read_inc(const ScanState& S, int64_t t, unsigned tag_inc, int lane, int* status) {
-    unsigned spins = 0;
-    bool timed_out = false;
-    u128 v = 0;
-    for (;;) {
-        const int st = read_desc(S.inc + 4 * t, tag_inc - 1u, v);  // tag_agg = tag_inc - 1
-        if (__all_sync(PER_FULL_MASK, st == 2)) return v;
-        spin_pause(spins, timed_out, lane, status);
-        if (timed_out) return 0;
-    }
-}
+// Exact sum of the published aggregates of tiles [lo, hi), computed by one
+// warp (lane l reads tiles lo + l + 32q); waits until every one of them is
+// published.  All loads of a poll are issued before any is consumed, so a
+// poll costs one round trip.
+constexpr int kLookQ = 16;  // aggregates per lane per poll (512 tiles)
 
-// Exclusive prefix (exact) of tile t, computed by one warp.
-//   1. own group: tiles 32g .. t-1 (lane l reads tile 32g + l): the nearest
-//      one holding an inclusive prefix ends the walk, otherwise all their
-//      aggregates are summed;
-//   2. earlier groups, kGroupQ x 32 per poll: group k is "inclusive" when its
-//      last tile holds an inclusive prefix, else its published group sum is
-//      used; the nearest inclusive group ends the walk.
-// Integer sums are exact, so any mix of tile and group sums gives the same
-// value: the carry is independent of timing.
-__device__ u128 lookback(const ScanState& S, int64_t t, unsigned tag_agg, int lane, int* status) {
-    const unsigned tag_inc = tag_agg + 1u;
-    const int64_t g = t >> 5;
-    const int p = static_cast<int>(t & 31);
+__device__ u128 sum_aggregates(const ScanState& S, int64_t lo, int64_t hi, unsigned tag_agg, int lane,
+                               int* status) {
     unsigned spins = 0;
     bool timed_out = false;
-    u128 part = 0;
-    if (p > 0) {
-        for (;;) {
-            unsigned long long w = 0;
-            if (lane < p) w = *reinterpret_cast<volatile const unsigned long long*>(S.aggw + (g << 5) + lane);
-            const unsigned tag = static_cast<unsigned>(w >> 32);
-            const bool inc = lane < p && tag == tag_inc;
-            const bool valid = lane >= p || tag == tag_agg || tag == tag_inc;
-            const unsigned incm = __ballot_sync(PER_FULL_MASK, inc);
-            const int h = incm ? 31 - __clz(incm) : -1;  // nearest inclusive tile
-            const unsigned need = (lane > h && lane < p) ? 1u : 0u;
-            if (__all_sync(PER_FULL_MASK, valid || !need)) {
+    u128 acc = 0;
+    int64_t j0 = lo;  // first aggregate not yet consumed
+    while (j0 < hi) {
+        unsigned long long w[kLookQ];
+#pragma unroll
+        for (int q = 0; q < kLookQ; ++q) {
+            const int64_t j = j0 + lane + 32 * q;
+            w[q] = j < hi ? ld_relaxed_u64(S.aggw + j) : 0ull;
+        }
+        bool ok = true;
+        u128 a = 0;
+#pragma unroll
+        for (int q = 0; q < kLookQ; ++q) {
+            const int64_t j = j0 + lane + 32 * q;
+            if (j < hi) {
+                if (static_cast<unsigned>(w[q] >> 32) != tag_agg) ok = false;
                 bool err = false;
-                const u128 a = (need && lane < p) ? to_fixed(__uint_as_float(static_cast<unsigned>(w)), err)
-                                                  : static_cast<u128>(0);
-                part = warp_sum_u128(a);
-                if (h >= 0) return part + read_inc(S, (g << 5) + h, tag_inc, lane, status);
-                break;
+                a += to_fixed(__uint_as_float(static_cast<unsigned>(w[q])), err);
             }
-            spin_pause(spins, timed_out, lane, status);
-            if (timed_out) return 0;
         }
-    }
-    // previous groups
-    int64_t k0 = g - 1;  // lane l, round q examines group k0 - l - 32q
-    u128 acc = part;
-    while (k0 >= 0) {
-        int st[kGroupQ];
-        u128 val[kGroupQ];
-        int fq = kGroupQ, fl = 0;
-        for (;;) {
-#pragma unroll
-            for (int q = 0; q < kGroupQ; ++q) {
-                const int64_t k = k0 - lane - 32 * q;
-                val[q] = 0;
-                if (k < 0) {
-                    st[q] = 2;  // before group 0: inclusive prefix 0
-                } else {
-                    const unsigned long long w =
-                        *reinterpret_cast<volatile const unsigned long long*>(S.aggw + (k << 5) + 31);
-                    if (static_cast<unsigned>(w >> 32) == tag_inc) {
-                        st[q] = 3;  // inclusive: value read below
-                    } else {
-                        st[q] = read_desc(S.gagg + 4 * k, tag_agg, val[q]) == 1 ? 1 : 0;
-                    }
-                }
-            }
-            unsigned incm[kGroupQ], invm[kGroupQ];
-#pragma unroll
-            for (int q = 0; q < kGroupQ; ++q) {
-                incm[q] = __ballot_sync(PER_FULL_MASK, st[q] >= 2);
-                invm[q] = __ballot_sync(PER_FULL_MASK, st[q] == 0);
-            }
-            fq = kGroupQ;
-            fl = 0;
-#pragma unroll
-            for (int q = kGroupQ - 1; q >= 0; --q)
-                if (incm[q]) {
-                    fq = q;
-                    fl = __ffs(incm[q]) - 1;
-                }
-            bool ready = true;
-#pragma unroll
-            for (int q = 0; q < kGroupQ; ++q) {
-                if (q < fq && invm[q]) ready = false;
-                if (q == fq && (invm[q] & ((1u << fl) - 1u))) ready = false;
-            }
-            if (ready) break;
-            spin_pause(spins, timed_out, lane, status);
-            if (timed_out) return acc;
+        if (__all_sync(PER_FULL_MASK, ok)) {
+            acc += warp_sum_u128(a);
+            j0 += 32 * kLookQ;
+            continue;
         }
-        u128 c = 0;
-#pragma unroll
-        for (int q = 0; q < kGroupQ; ++q)
-            if (q < fq || (q == fq && lane < fl)) c += val[q];
-        acc += warp_sum_u128(c);
-        if (fq < kGroupQ) {
-            const int64_t k = k0 - fl - 32 * fq;
-            if (k >= 0) acc += read_inc(S, (k << 5) + 31, tag_inc, lane, status);
-            return acc;
-        }
-        k0 -= 32 * kGroupQ;
+        spin_pause(spins, timed_out, lane, status);
+        if (timed_out) return acc;
     }
     return acc;
-}
-
-// After publishing tile t's aggregate: if t completes a full group, the last
-// tile of the group to arrive sums the group's 32 aggregates and publishes
-// the group sum.  One warp; the counter's acquire-release ordering makes the
-// other tiles' aggregates visible.
-__device__ void group_arrive(const ScanState& S, int64_t t, unsigned num_tiles, unsigned tag_agg, int lane,
-                             int* status) {
-    const int64_t g = t >> 5;
-    if ((g << 5) + 31 >= num_tiles) return;  // partial last group: never needed
-    unsigned old = 0;
-    if (lane == 0) {
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(S.gcnt + g) : "memory");
-    }
-    old = __shfl_sync(PER_FULL_MASK, old, 0);
-    if ((old & 31u) != 31u) return;
-    unsigned spins = 0;
-    bool timed_out = false;
-    for (;;) {
-        const unsigned long long w = *reinterpret_cast<volatile const unsigned long long*>(S.aggw + (g << 5) + lane);
-        const unsigned tag = static_cast<unsigned>(w >> 32);
-        if (__all_sync(PER_FULL_MASK, tag == tag_agg || tag == tag_agg + 1u)) {
-            bool err = false;
-            const u128 sum = warp_sum_u128(to_fixed(__uint_as_float(static_cast<unsigned>(w)), err));
-            if (lane == 0) publish(S.gagg + 4 * g, tag_agg, sum);
-            return;
-        }
-        spin_pause(spins, timed_out, lane, status);
-        if (timed_out) return;
-    }
 }
 
 // Issue the bulk copy of tile `t` into stage buffer `buf` (thread 0 only).
@@ -311,59 +177,162 @@ __device__ __forceinline__ void load_tile(const ScanParams& P, unsigned t, float
     if (bytes) bulk_copy_g2s(buf, P.p + base, bytes, bar);
 }
 
-// Persistent scan: each CTA keeps STAGES tiles in flight through a ring of
-// shared-memory buffers filled by bulk copies, takes tile ids in increasing
-// order from the global ticket, and processes them in that order with a lag
-// of one: the local scan of tile k+1 runs before tile k's lookback finishes,
-// so the lookback latency overlaps useful work.  Tile k's local values wait
-// in its stage buffer until its carry is known.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier among the compute warps only (the lookback warp never joins it).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// Persistent, warp-specialised scan over a co-resident grid of G CTAs (the
+// launch is cooperative, so all of them run at once).  CTA c scans tiles
+// c, c + G, c + 2G, ... (round k = its k-th tile), so the CTAs sweep the array
+// one round at a time.  Each CTA runs kThreads compute threads (kWarps warps)
+// plus one lookback warp:
+//   * compute warps: wait for the stage's bulk copy, apply p^alpha, scan the
+//     tile locally, park the tile-local values in the stage buffer, publish
+//     the tile aggregate and signal `parked`; two tiles behind, wait for that
+//     tile's carry, write its CDF values and refill its stage with the tile
+//     STAGES rounds ahead;
+//   * lookback warp: for each of the CTA's tiles in order, wait `parked`, run
+//     the lookback, publish the tile's inclusive prefix, signal `carried`.
+// A lookback waits only on tiles of earlier rounds or earlier tiles of the
+// same round, so the scan always makes progress.
 template <int ITEMS, int STAGES>
-__global__ void __launch_bounds__(kThreads) build_cdf_kernel(ScanParams P) {
-    static_assert(STAGES >= 3, "one buffer scanning, one awaiting its carry, one loading");
+__global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams P) {
+    static_assert(STAGES == 4, "one stage scanning, two awaiting their carry, one loading");
+    constexpr int LAG = 2;
     constexpr int TILE = kThreads * ITEMS;
     constexpr int LANE_ITEMS = 8;             // consecutive items per lane per sub-chunk
     constexpr int SUB = ITEMS / LANE_ITEMS;   // sub-chunks per warp
     constexpr int WCHUNK = 32 * ITEMS;        // items per warp
     extern __shared__ __align__(128) float s_buf[];  // STAGES x TILE
-    __shared__ __align__(8) uint64_t s_bar[STAGES];
-    __shared__ unsigned s_ticket[STAGES];
+    __shared__ __align__(8) uint64_t s_full[STAGES], s_parked[STAGES], s_carried[STAGES];
+    __shared__ float s_agg[STAGES];
+    __shared__ float s_carry[STAGES][4];
+    __shared__ float s_wtot[2][kWarps];
     __shared__ unsigned s_epoch;
-    __shared__ float s_wtot[2][kWarps];  // by iteration parity: reuse is two barriers apart
-    __shared__ float s_agg[2];      // tile sums of the scanned and the pending tile
-    __shared__ float s_carry[4];
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    const int64_t G = gridDim.x;
+    const int64_t c = blockIdx.x;
     const ScanState S = scan_state(P);
     if (threadIdx.x == 0) {
         s_epoch = ld_relaxed_u32(P.ctrs + CTR_SCAN_EPOCH);
         for (int st = 0; st < STAGES; ++st) {
-            mbar_init(&s_bar[st], 1);
-            const unsigned t = atomicAdd(P.ctrs + CTR_SCAN_TICKET, 1u);
-            s_ticket[st] = t;
-            if (t < P.num_tiles) load_tile<TILE>(P, t, s_buf + st * TILE, &s_bar[st]);
+            mbar_init(&s_full[st], 1);
+            mbar_init(&s_parked[st], 1);
+            mbar_init(&s_carried[st], 1);
+            const int64_t t = c + st * G;
+            if (t < P.num_tiles) load_tile<TILE>(P, static_cast<unsigned>(t), s_buf + st * TILE, &s_full[st]);
         }
     }
     __syncthreads();
     const unsigned epoch = s_epoch;
     const unsigned tag_agg = 2u * epoch;
-    int pend_slot = -1;          // stage holding the tile that awaits its carry
-    unsigned pend_t = 0;
 
-    for (int it = 0;; ++it) {
-        const int st = it % STAGES;
-        const unsigned t = s_ticket[st];
-        const bool have = t < P.num_tiles;
-        if (have) {
-            if (!mbar_wait_bounded(&s_bar[st], static_cast<unsigned>(it / STAGES) & 1u))
+    if (warp == kWarps) {
+        // ======================= lookback warp ================================
+        u128 run = 0;  // inclusive prefix of this CTA's previous tile
+        for (int k = 0;; ++k) {
+            const int64_t t = c + k * G;
+            if (t >= P.num_tiles) break;
+            const int st = k % STAGES;
+            if (!mbar_wait_bounded(&s_parked[st], static_cast<unsigned>(k / STAGES) & 1u))
+                if (lane == 0) atomicOr(P.status, ST_TIMEOUT);
+            const float agg = s_agg[st];
+            bool range_err = false;
+            const u128 a_fix = to_fixed(agg, range_err);
+            // exclusive prefix = previous own prefix + the tiles in between
+            const u128 excl = run + sum_aggregates(S, k == 0 ? 0 : t - G + 1, t, tag_agg, lane, P.status);
+            run = excl + a_fix;
+            if (lane == 0) {
+                const double d0 = fixed_to_double(excl);
+                const double d1 = fixed_to_double(excl + a_fix);
+                const float hi = __double2float_rn(d0);
+                s_carry[st][0] = hi;
+                s_carry[st][1] = __double2float_rn(d0 - static_cast<double>(hi));
+                s_carry[st][2] = hi;                     // fl32(E_t)
+                s_carry[st][3] = __double2float_rn(d1);  // fl32(E_{t+1})
+                if (range_err) atomicOr(P.status, ST_RANGE);
+                mbar_arrive(&s_carried[st]);
+            }
+        }
+    } else {
+        // ======================= compute warps ================================
+        // Writes the CDF values of the CTA's k-th tile once its carry is known,
+        // then refills its stage with the tile STAGES rounds ahead.
+        auto emit = [&](int k) {
+            const int ps = k % STAGES;
+            const int64_t pt = c + k * G;
+            if (!mbar_wait_bounded(&s_carried[ps], static_cast<unsigned>(k / STAGES) & 1u))
+                atomicOr(P.status, ST_TIMEOUT);
+            const int64_t tile_base = pt * TILE;
+            const int64_t valid = P.n - tile_base < TILE ? P.n - tile_base : TILE;
+            const bool full = valid == TILE;
+            const float hi = s_carry[ps][0], lo = s_carry[ps][1];
+            const float sig_lo = s_carry[ps][2], sig_hi = s_carry[ps][3];
+            const float* buf = s_buf + ps * TILE;
+            float o[SUB * 2][4];
+#pragma unroll
+            for (int s = 0; s < SUB; ++s) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i0 = warp * WCHUNK + s * 256 + lane * LANE_ITEMS + 4 * h;
+                    const float4 loc = *reinterpret_cast<const float4*>(buf + i0);
+                    o[2 * s + h][0] = hi + (lo + loc.x);
+                    o[2 * s + h][1] = hi + (lo + loc.y);
+                    o[2 * s + h][2] = hi + (lo + loc.z);
+                    o[2 * s + h][3] = hi + (lo + loc.w);
+                }
+            }
+            // values are monotone along the warp's chunk: clamp only if its
+            // first or last value falls outside [fl32(E_t), fl32(E_{t+1})]
+            const float wfirst = __shfl_sync(PER_FULL_MASK, o[0][0], 0);
+            const float wlast = __shfl_sync(PER_FULL_MASK, o[SUB * 2 - 1][3], 31);
+            if (!(wfirst >= sig_lo && wlast <= sig_hi)) {
+#pragma unroll
+                for (int j = 0; j < SUB * 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[j][e] = fminf(fmaxf(o[j][e], sig_lo), sig_hi);
+            }
+#pragma unroll
+            for (int s = 0; s < SUB; ++s) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i0 = warp * WCHUNK + s * 256 + lane * LANE_ITEMS + 4 * h;
+                    const float* oo = o[2 * s + h];
+                    if (full || i0 + 3 < valid) {
+                        st_f4(P.cdf + tile_base + i0, make_float4(oo[0], oo[1], oo[2], oo[3]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (i0 + e < valid) P.cdf[tile_base + i0 + e] = oo[e];
+                    }
+                }
+            }
+            compute_sync();  // the stage was read by everyone
+            if (threadIdx.x == 0) {
+                const int64_t t2 = pt + STAGES * G;
+                if (t2 < P.num_tiles) load_tile<TILE>(P, static_cast<unsigned>(t2), s_buf + ps * TILE, &s_full[ps]);
+            }
+        };
+
+        // the CTA's tiles: k = 0 .. K-1; iteration k scans tile k and emits k - LAG
+        const int K = c < P.num_tiles ? static_cast<int>((P.num_tiles - 1 - c) / G) + 1 : 0;
+        for (int k = 0; k < K + LAG; ++k) {
+          if (k < K) {
+            const int64_t t = c + k * G;
+            const int st = k % STAGES;
+            if (!mbar_wait_bounded(&s_full[st], static_cast<unsigned>(k / STAGES) & 1u))
                 atomicOr(P.status, ST_TIMEOUT);
             float* buf = s_buf + st * TILE;
-            const int64_t tile_base = static_cast<int64_t>(t) * TILE;
+            const int64_t tile_base = t * TILE;
             const int64_t valid = P.n - tile_base < TILE ? P.n - tile_base : TILE;
             const int bulk = static_cast<int>(valid & ~int64_t(3));
             const bool full = valid == TILE;
 
-            // ---- load from shared memory + p^alpha --------------------------
             float v[ITEMS];
             bool bad = false;
 #pragma unroll
@@ -381,9 +350,8 @@ __global__ void __launch_bounds__(kThreads) build_cdf_kernel(ScanParams P) {
                         }
                         q = make_float4(e4[0], e4[1], e4[2], e4[3]);
                     }
-                    bad |= !(q.x >= 0.f) | !(q.y >= 0.f) | !(q.z >= 0.f) | !(q.w >= 0.f);
-                    float a0 = pow_alpha(q.x, P.alpha, P.alpha_one), a1 = pow_alpha(q.y, P.alpha, P.alpha_one);
-                    float a2 = pow_alpha(q.z, P.alpha, P.alpha_one), a3 = pow_alpha(q.w, P.alpha, P.alpha_one);
+                    const float4 pa = pow4_alpha(q, P.alpha, P.pow_mode, bad);
+                    float a0 = pa.x, a1 = pa.y, a2 = pa.z, a3 = pa.w;
                     if (!full) {  // padding beyond n contributes 0 (p^0 would be 1)
                         a0 = i0 < valid ? a0 : 0.f;
                         a1 = i0 + 1 < valid ? a1 : 0.f;
@@ -398,7 +366,6 @@ __global__ void __launch_bounds__(kThreads) build_cdf_kernel(ScanParams P) {
             }
             if (__any_sync(PER_FULL_MASK, bad) && lane == 0) atomicOr(P.status, ST_VALUE);
 
-            // ---- warp-local monotone scan ------------------------------------
             float carry = 0.f;
 #pragma unroll
             for (int s = 0; s < SUB; ++s) {
@@ -429,12 +396,11 @@ __global__ void __launch_bounds__(kThreads) build_cdf_kernel(ScanParams P) {
                 for (int e = 0; e < LANE_ITEMS; ++e) v[s * LANE_ITEMS + e] = fmaxf(r[e], pm);
                 carry = __shfl_sync(PER_FULL_MASK, mx, 31);
             }
-            float* wtot = s_wtot[it & 1];
+            float* wtot = s_wtot[k & 1];
             if (lane == 0) wtot[warp] = carry;
-            __syncthreads();
+            compute_sync();
             float off = 0.f;
             for (int w = 0; w < warp; ++w) off = off + wtot[w];
-            // park the tile-local values in the stage buffer until the carry is known
 #pragma unroll
             for (int s = 0; s < SUB; ++s) {
 #pragma unroll
@@ -445,99 +411,28 @@ __global__ void __launch_bounds__(kThreads) build_cdf_kernel(ScanParams P) {
                                     off + v[s * LANE_ITEMS + 4 * h + 2], off + v[s * LANE_ITEMS + 4 * h + 3]);
                 }
             }
-            if (warp == 0) {
-                float agg = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) agg = agg + wtot[w];
-                if (lane == 0) {
-                    s_agg[it & 1] = agg;
-                    const unsigned long long word = (static_cast<unsigned long long>(tag_agg) << 32) |
-                                                    __float_as_uint(agg);
-                    if (t == 0) {  // tile 0's inclusive prefix is its own sum
-                        bool err = false;
-                        publish(S.inc, tag_agg + 1u, to_fixed(agg, err));
-                    }
-                    *reinterpret_cast<volatile unsigned long long*>(S.aggw + t) =
-                        t == 0 ? (word + (1ull << 32)) : word;
-                }
-                __syncwarp();
-                group_arrive(S, t, P.num_tiles, tag_agg, lane, P.status);
-            }
-        }
-
-        // ---- finish the pending tile: lookback, carry, store, refill --------
-        if (pend_slot >= 0) {
-            const int ps = pend_slot;
-            const int64_t tile_base = static_cast<int64_t>(pend_t) * TILE;
-            const int64_t valid = P.n - tile_base < TILE ? P.n - tile_base : TILE;
-            const bool full = valid == TILE;
-            if (warp == 0) {
-                bool range_err = false;
-                const float agg = s_agg[(it - 1) & 1];
-                const u128 a_fix = to_fixed(agg, range_err);
-                const u128 excl = pend_t == 0 ? static_cast<u128>(0) : lookback(S, pend_t, tag_agg, lane, P.status);
-                if (lane == 0) {
-                    if (pend_t != 0) {
-                        publish(S.inc + 4 * static_cast<int64_t>(pend_t), tag_agg + 1u, excl + a_fix);
-                        const unsigned long long word = (static_cast<unsigned long long>(tag_agg + 1u) << 32) |
-                                                        __float_as_uint(agg);
-                        *reinterpret_cast<volatile unsigned long long*>(S.aggw + pend_t) = word;
-                    }
-                    const double d0 = fixed_to_double(excl);
-                    const double d1 = fixed_to_double(excl + a_fix);
-                    const float hi = __double2float_rn(d0);
-                    s_carry[0] = hi;
-                    s_carry[1] = __double2float_rn(d0 - static_cast<double>(hi));
-                    s_carry[2] = hi;                     // fl32(E_t)
-                    s_carry[3] = __double2float_rn(d1);  // fl32(E_{t+1})
-                    if (range_err) atomicOr(P.status, ST_RANGE);
-                }
-            }
-            __syncthreads();
-            const float hi = s_carry[0], lo = s_carry[1], sig_lo = s_carry[2], sig_hi = s_carry[3];
-            const float* buf = s_buf + ps * TILE;
-#pragma unroll
-            for (int s = 0; s < SUB; ++s) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int i0 = warp * WCHUNK + s * 256 + lane * LANE_ITEMS + 4 * h;
-                    const float4 loc = *reinterpret_cast<const float4*>(buf + i0);
-                    float o[4] = {hi + (lo + loc.x), hi + (lo + loc.y), hi + (lo + loc.z), hi + (lo + loc.w)};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = fminf(fmaxf(o[e], sig_lo), sig_hi);
-                    if (full || i0 + 3 < valid) {
-                        st_f4(P.cdf + tile_base + i0, make_float4(o[0], o[1], o[2], o[3]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (i0 + e < valid) P.cdf[tile_base + i0 + e] = o[e];
-                    }
-                }
-            }
-            __syncthreads();  // pending buffer, s_carry and s_wtot free again
             if (threadIdx.x == 0) {
-                const unsigned t2 = atomicAdd(P.ctrs + CTR_SCAN_TICKET, 1u);
-                s_ticket[ps] = t2;
-                if (t2 < P.num_tiles) load_tile<TILE>(P, t2, s_buf + ps * TILE, &s_bar[ps]);
+                float agg = 0.f;
+                for (int w = 0; w < kWarps; ++w) agg = agg + wtot[w];
+                s_agg[st] = agg;
+                *reinterpret_cast<volatile unsigned long long*>(S.aggw + t) =
+                    (static_cast<unsigned long long>(tag_agg) << 32) | __float_as_uint(agg);
+                mbar_arrive(&s_parked[st]);
             }
-            __syncthreads();
+          }
+          if (k >= LAG) emit(k - LAG);
         }
-        if (!have) break;
-        pend_slot = st;
-        pend_t = t;
     }
+    __syncthreads();
 
-    // ---- the last CTA to finish resets the counters for the next call --------
+    // ---- the last CTA to finish advances the epoch for the next call ---------
     if (threadIdx.x == 0) {
         const unsigned done = atomicAdd(P.ctrs + CTR_SCAN_DONE, 1u);
         if (done == gridDim.x - 1u) {
-            P.ctrs[CTR_SCAN_TICKET] = 0u;
             P.ctrs[CTR_SCAN_DONE] = 0u;
             unsigned next = epoch + 1u;
-            if (next >= (1u << 30)) {  // epoch wrap: clear all scan state once (counters keep
-                // their multiples of 32)
-                const int64_t words = 4 * P.desc_tiles + P.desc_tiles + 4 * (P.desc_tiles / 32 + 1);
-                for (int64_t i = 0; i < words; ++i) P.desc[i] = 0ull;
+            if (next >= (1u << 30)) {  // epoch wrap: clear all scan state once
+                for (int64_t i = 0; i < P.desc_tiles; ++i) P.desc[i] = 0ull;
                 next = 1u;
             }
             P.ctrs[CTR_SCAN_EPOCH] = next;
@@ -610,9 +505,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) build_cdf_cluster_kernel(S
                 q.z = i0 + 2 < valid ? P.p[tile_base + i0 + 2] : 0.f;
                 q.w = i0 + 3 < valid ? P.p[tile_base + i0 + 3] : 0.f;
             }
-            bad |= !(q.x >= 0.f) | !(q.y >= 0.f) | !(q.z >= 0.f) | !(q.w >= 0.f);
-            float a0 = pow_alpha(q.x, P.alpha, P.alpha_one), a1 = pow_alpha(q.y, P.alpha, P.alpha_one);
-            float a2 = pow_alpha(q.z, P.alpha, P.alpha_one), a3 = pow_alpha(q.w, P.alpha, P.alpha_one);
+            const float4 pa = pow4_alpha(q, P.alpha, P.pow_mode, bad);
+            float a0 = pa.x, a1 = pa.y, a2 = pa.z, a3 = pa.w;
             if (!full) {
                 a0 = i0 < valid ? a0 : 0.f;
                 a1 = i0 + 1 < valid ? a1 : 0.f;
@@ -778,8 +672,8 @@ per_status launch_scan(ScanParams P, int num_sms, cudaStream_t s) {
     if (per_sm == 0) {
         if (cudaFuncSetAttribute(build_cdf_kernel<ITEMS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_kernel<ITEMS, STAGES>, kThreads,
-                                                          smem) != cudaSuccess)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_kernel<ITEMS, STAGES>,
+                                                          kThreads + 32, smem) != cudaSuccess)
             return PER_ERR_CUDA;
         if (per_sm < 1) per_sm = 1;
     }
@@ -788,9 +682,21 @@ per_status launch_scan(ScanParams P, int num_sms, cudaStream_t s) {
     P.num_tiles = static_cast<unsigned>(tiles);
     int64_t grid = static_cast<int64_t>(num_sms) * per_sm;
     if (grid > tiles) grid = tiles;
-    build_cdf_kernel<ITEMS, STAGES><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(P);
+    // cooperative: every CTA of the grid is resident at once (the static tile
+    // stride relies on it)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads + 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_kernel<ITEMS, STAGES>, P);
     per_note_launch();
-    return cuda_status(cudaGetLastError());
+    return cuda_status(e);
 }
 
 // Tile size: 4096 items for large inputs (fewer lookback steps per byte);
@@ -801,8 +707,8 @@ per_status scan_dispatch(ScanParams P, int num_sms, cudaStream_t s) {
         if (st != PER_ERR_STATE) return st;
     }
     const int64_t big_tiles = (P.n + 4095) / 4096;
-    if (big_tiles >= 2 * static_cast<int64_t>(num_sms)) return launch_scan<16, 3>(P, num_sms, s);
-    return launch_scan<8, 3>(P, num_sms, s);
+    if (big_tiles >= 2 * static_cast<int64_t>(num_sms)) return launch_scan<16, 4>(P, num_sms, s);
+    return launch_scan<8, 4>(P, num_sms, s);
 }
 
 }  // namespace
@@ -814,6 +720,7 @@ per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s) {
     P.n = ctx->size;
     P.alpha = ctx->alpha;
     P.alpha_one = ctx->alpha == 1.0f;
+    P.pow_mode = ctx->alpha == 1.0f ? 1 : (ctx->alpha == 0.0f ? 2 : 0);
     P.desc = ctx->scan_desc;
     P.desc_tiles = ctx->scan_desc_tiles;
     P.ctrs = ctx->ctrs;
@@ -835,7 +742,7 @@ per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s) {
 // output CDF and nothing is ever allocated.
 //
 // The array is part of the library image: every GPU that loads the library
-// holds it (about 165 KiB) until the process exits.  All calls on a device
+// holds it (about 33 KiB) until the process exits.  All calls on a device
 // share it and it keeps the previous call's contents (its counters are left
 // ready for the next call by the kernel itself), so two calls whose kernels
 // overlap on the GPU -- different streams without ordering between them --
@@ -851,8 +758,7 @@ constexpr int kNoAllocMaxDevices = 64;
 
 }  // namespace
 
-constexpr int64_t kNoAllocStateWords = 5 * kNoAllocMaxTiles + 4 * (kNoAllocMaxTiles / 32 + 1) +
-                                       (kNoAllocMaxTiles / 32 + 2) / 2 + 1;  // == scan_state_words(4096)
+constexpr int64_t kNoAllocStateWords = kNoAllocMaxTiles + 1;  // == scan_state_words(4096)
 static __device__ __align__(256) unsigned long long
     g_noalloc_scratch[kNoAllocStateWords + kNoAllocCtrWords + 8];
 
@@ -908,6 +814,7 @@ extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, floa
     P.n = n;
     P.alpha = alpha;
     P.alpha_one = alpha == 1.0f;
+    P.pow_mode = alpha == 1.0f ? 1 : (alpha == 0.0f ? 2 : 0);
     P.desc = scratch;
     P.desc_tiles = kNoAllocMaxTiles;
     P.ctrs = reinterpret_cast<unsigned*>(scratch + kNoAllocStateWords);
