@@ -357,6 +357,77 @@ def extras(per, torch, dev, peak):
     return out
 
 
+# ------------------------------------------------------ kernel cases --------
+
+KERNEL_CASES = ("scan_stress", "scan_minibatch", "sample_stress", "tree_step", "resample", "is_weights_heavy")
+
+
+def kernel_case(name, reps):
+    """Run one kernel of one workload `reps` times after setup (for ncu
+    captures: -k selects the kernel, -s skips the setup launches).  Prints
+    "ok" after a clean device status; no timing."""
+    import torch
+    import cdf_scan_gb300 as per
+    from cdf_scan_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    ctxs = []
+    if name in ("scan_stress", "sample_stress"):
+        S = workloads.STRESS
+        ctx = per.PerContext(S["N"], S["alpha"], per.PER_SCAN)
+        per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
+        idx = torch.empty(S["B"], dtype=torch.int32, device=dev)
+        if name == "scan_stress":
+            body = lambda: per.per_build_cdf(ctx.handle)  # noqa: E731
+        else:
+            per.per_build_cdf(ctx.handle)
+            body = lambda: per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx)  # noqa: E731
+    elif name == "scan_minibatch":
+        ctx = per.PerContext(N, ALPHA, per.PER_SCAN)
+        per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
+        body = lambda: per.per_build_cdf(ctx.handle)  # noqa: E731
+    elif name == "is_weights_heavy":
+        Hv = workloads.HEAVY
+        ctx = per.PerContext(Hv["N"], Hv["alpha"], per.PER_SCAN)
+        per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.heavy_priorities()).to(dev))
+        per.per_build_cdf(ctx.handle)
+        idx = torch.empty(Hv["B"], dtype=torch.int32, device=dev)
+        w = torch.empty(Hv["B"], dtype=torch.float32, device=dev)
+        per.per_sample(ctx.handle, Hv["B"], 4, 0, per.PER_SCAN, idx)
+        body = lambda: per.per_is_weights(ctx.handle, idx, Hv["betas"][0], w)  # noqa: E731
+    elif name == "tree_step":
+        T = workloads.TREE
+        ctx = per.PerContext(T["capacity"], T["alpha"], per.PER_TREE)
+        p = workloads.lognormal(T["capacity"], workloads.rng(T["seed"], 999))
+        per.per_set_priorities(ctx.handle, torch.from_numpy(p).to(dev))
+        tidx = torch.empty(T["B"], dtype=torch.int32, device=dev)
+        per.per_sample(ctx.handle, T["B"], 3, 0, per.PER_TREE, tidx)
+        ui, up = workloads.tree_update_batch(0, tidx.cpu().numpy())
+        d_ui, d_up = torch.from_numpy(ui).to(dev), torch.from_numpy(up).to(dev)
+
+        def body():
+            per.per_sample(ctx.handle, T["B"], 3, 0, per.PER_TREE, tidx)
+            per.per_update(ctx.handle, d_ui, d_up)
+    elif name == "resample":
+        R = workloads.RESAMPLE
+        logw = torch.from_numpy(workloads.resample_logw()).to(dev)
+        out = torch.empty((R["rows"], R["P"]), dtype=torch.int32, device=dev)
+        ctx = None
+        body = lambda: per.per_resample(logw, 6, 0, out)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown kernel case {name!r}; one of {', '.join(KERNEL_CASES)}")
+    if ctx is not None:
+        ctxs.append(ctx)
+    for _ in range(reps):
+        body()
+    torch.cuda.synchronize()
+    for c in ctxs:
+        if per.per_check(c.handle) != 0:
+            raise SystemExit("device status not clean")
+        c.close()
+    print("ok", flush=True)
+
+
 # -------------------------------------------------------- oracle arms -------
 
 def oracle_step(p, seed, step):
@@ -417,8 +488,14 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--kernel-case", choices=KERNEL_CASES, default=None,
+                    help="run one kernel of one workload a few times (for profiler captures) and exit")
+    ap.add_argument("--reps", type=int, default=5)
     args = ap.parse_args()
     rank, world, local_rank = env_rank()
+    if args.kernel_case:
+        kernel_case(args.kernel_case, args.reps)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
     else:

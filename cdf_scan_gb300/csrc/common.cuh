@@ -7,9 +7,9 @@
 
 #define PER_FULL_MASK 0xffffffffu
 
-// Upper bound on polling iterations of any device-side wait.  Each poll
-// sleeps ~0.25-1 us, so a wait gives up after roughly one to a few seconds
-// and records ST_TIMEOUT instead of hanging.
+// Upper bound on polling iterations of a device-side spin on global memory.
+// Each poll sleeps ~0.25-1 us, so such a wait gives up after roughly one to a
+// few seconds and records ST_TIMEOUT instead of hanging.
 constexpr unsigned kSpinLimit = 1u << 22;
 
 // ---- memory access --------------------------------------------------------
@@ -44,6 +44,13 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 __device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 __device__ __forceinline__ void st_f4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+// 256-bit store of v[0..7] (p 32-byte aligned).
+__device__ __forceinline__ void st_f8(float* p, const float* v) {
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(v[0]), "f"(v[1]),
+                 "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
 
 // ---- mbarrier + bulk copy (global -> shared, completes on an mbarrier) ------
 
@@ -82,15 +89,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
     return ok != 0;
 }
 
-// Bounded wait for phase `parity` of an mbarrier.  A bulk copy from valid
-// global memory always completes, so the limit is a safety net: on expiry
-// the caller's status word records ST_TIMEOUT.
+// try_wait that may suspend the thread in hardware for up to `ns`
+// nanoseconds while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, unsigned parity, unsigned ns) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Every device-side wait gives up after this long and records ST_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait for phase `parity` of an mbarrier: the thread sleeps in
+// hardware between checks.  A bulk copy from valid global memory always
+// completes, so the limit is a safety net: on expiry the caller records
+// ST_TIMEOUT.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
-    for (unsigned i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_for(bar, parity, 20000u)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
-    return false;
 }
 
 // ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) ----------------------
@@ -184,30 +216,66 @@ __device__ __forceinline__ float pow_fast(float x, float alpha, bool& bad) {
     return __fmul_rn(y, __uint_as_float(static_cast<unsigned>(ni + 127) << 23));  // y * 2^n
 }
 
-// p^alpha for four values at once (the scan's hot path).  For |log2 x| < 16,
-// i.e. x in (2^-16, 2^16), x^alpha = ex2(alpha * lg2(x)) directly: the
-// hardware lg2 (absolute error ~2^-22.6), the fp32 rounding of L = lg2(x)
-// (<= 2^-21 for |L| < 16), the rounding of alpha*L (<= 2^-21) and the
-// hardware ex2 (~2^-22.5 relative) bound the relative error by ~1e-6.  Any
-// other input -- tiny, huge, zero, subnormal, infinite, negative, NaN (the
-// range test is false for NaN) -- takes pow_fast's exact exponent split.
+// pow_fast out of line, for the rare inputs outside the direct range below.
+static __device__ __noinline__ float pow_split(float x, float alpha) {
+    bool bad = false;
+    return pow_fast(x, alpha, bad);
+}
+
+// max(|a|, b) that returns NaN when either input is NaN.
+__device__ __forceinline__ float absmax_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(fabsf(a)), "f"(b));
+    return d;
+}
+
+// v[e] <- v[e]^alpha in place (the scan's hot path).  For |log2 x| < 16, i.e.
+// x in (2^-16, 2^16), x^alpha = ex2(alpha * lg2(x)) directly: the hardware
+// lg2 (absolute error ~2^-22.6), the fp32 rounding of L = lg2(x) (<= 2^-21
+// for |L| < 16), the rounding of alpha*L (<= 2^-21) and the hardware ex2
+// (~2^-22.5 relative) bound the relative error by ~1e-6.  One range test
+// covers all N values; any other input -- tiny, huge, zero, subnormal,
+// infinite, negative, NaN (the NaN-propagating max fails the test) -- takes
+// pow_fast's exact exponent split, and negative or NaN inputs set `bad`.
 // mode: 0 = x^alpha, 1 = alpha == 1 (x), 2 = alpha == 0 (1).
-__device__ __forceinline__ float4 pow4_alpha(float4 q, float alpha, int mode, bool& bad) {
+template <int N, class Fetch>
+__device__ __forceinline__ void pow_alpha_n(float (&v)[N], float alpha, int mode, bool& bad, Fetch fetch) {
     if (mode != 0) {
-        const float4 one = make_float4(1.f, 1.f, 1.f, 1.f);
-        if (!(q.x >= 0.f && q.y >= 0.f && q.z >= 0.f && q.w >= 0.f)) bad = true;
-        return mode == 1 ? q : one;
+        bool ok = true;
+#pragma unroll
+        for (int e = 0; e < N; ++e) ok = ok && v[e] >= 0.f;
+        if (!ok) bad = true;
+        if (mode == 2) {
+#pragma unroll
+            for (int e = 0; e < N; ++e) v[e] = 1.f;
+        }
+        return;
     }
-    const float l0 = hw_lg2(q.x), l1 = hw_lg2(q.y), l2 = hw_lg2(q.z), l3 = hw_lg2(q.w);
-    const float lmax = fmaxf(fmaxf(fabsf(l0), fabsf(l1)), fmaxf(fabsf(l2), fabsf(l3)));
-    if (lmax < 16.f) {  // false for NaN
-        return make_float4(hw_ex2(__fmul_rn(alpha, l0)), hw_ex2(__fmul_rn(alpha, l1)),
-                           hw_ex2(__fmul_rn(alpha, l2)), hw_ex2(__fmul_rn(alpha, l3)));
+    // v <- lg2(v) in place; the rare slow path re-reads the inputs via fetch(e)
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = hw_lg2(v[e]);
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < N; ++e) m = absmax_nan(v[e], m);
+    if (m < 16.f) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) v[e] = hw_ex2(__fmul_rn(alpha, v[e]));
+        return;
     }
-    return make_float4(fabsf(l0) < 16.f ? hw_ex2(__fmul_rn(alpha, l0)) : pow_fast(q.x, alpha, bad),
-                       fabsf(l1) < 16.f ? hw_ex2(__fmul_rn(alpha, l1)) : pow_fast(q.y, alpha, bad),
-                       fabsf(l2) < 16.f ? hw_ex2(__fmul_rn(alpha, l2)) : pow_fast(q.z, alpha, bad),
-                       fabsf(l3) < 16.f ? hw_ex2(__fmul_rn(alpha, l3)) : pow_fast(q.w, alpha, bad));
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+        const float x = fetch(e);
+        if (!(x >= 0.f)) bad = true;
+        v[e] = fabsf(v[e]) < 16.f ? hw_ex2(__fmul_rn(alpha, v[e])) : pow_split(x, alpha);
+    }
+}
+
+// Four values at once (same rule as pow_alpha_n).
+__device__ __forceinline__ float4 pow4_alpha(float4 q, float alpha, int mode, bool& bad) {
+    const float x[4] = {q.x, q.y, q.z, q.w};
+    float v[4] = {q.x, q.y, q.z, q.w};
+    pow_alpha_n<4>(v, alpha, mode, bad, [&](int e) { return x[e]; });
+    return make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // p^alpha; alpha == 1 skips the power (exact).  `bad` is set for negative

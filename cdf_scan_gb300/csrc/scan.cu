@@ -4,27 +4,30 @@
 // prefix sum of the priorities rebuilt once per minibatch update, monotone,
 // deterministic, allocation- and sync-free).  The two-level block scan and
 // the serial kernel described there are prior art; this is a single-pass
-// decoupled-lookback scan:
+// scan with an exact, chain-free lookback:
 //
-//  * Tiles of 256 threads x ITEMS floats, taken in order from an atomic
-//    ticket so every tile a CTA waits on is already running.
-//  * p^alpha is applied as the tile is loaded with 128-bit vector loads.
+//  * A co-resident grid of G CTAs (cooperative launch); CTA c scans tiles
+//    c, c+G, c+2G, ... through a 4-stage ring of 1-D bulk copies (TMA)
+//    completing on mbarriers.
+//  * p^alpha is applied as a tile leaves shared memory.
 //  * Inside a tile: each warp scans its contiguous chunk with a thread-serial
-//    pass over 4 values plus warp shuffles, repairs the 1-ulp dips fp32
+//    pass over 8 values plus warp shuffles, repairs the 1-ulp dips fp32
 //    reassociation can leave between lanes with an exact max-scan, and the
 //    warp chunks are chained by a left fold (each warp starts at the previous
 //    warp's last value), so local values are monotone by construction.
 //  * Across tiles the carry is exact: a tile's fp32 sum becomes a 128-bit
-//    fixed-point integer (60 fractional bits) and the lookback adds integers,
-//    so the carry of tile t is the same value whatever order and depth the
-//    lookback takes -- the result is bit-reproducible run to run.
+//    fixed-point integer (60 fractional bits).  A dedicated lookback warp
+//    forms the exclusive prefix of tile t as the CTA's own previous inclusive
+//    prefix plus the exact sum of the G-1 tile sums published in between --
+//    integers, so the carry is the same whatever order they arrive in and the
+//    result is bit-reproducible run to run.
 //  * Each tile turns its exact carry E_t into fp32 hi + lo and writes
 //    clamp(hi + (lo + local), fl32(E_t), fl32(E_{t+1})): the clamp bounds are
 //    monotone in t, so the whole CDF is non-decreasing.
-//  * Descriptors are 4 x 64-bit words (32-bit tag | 32-bit limb); a reader
-//    accepts a descriptor only when all four tags match the current call's
-//    epoch, so stale descriptors never need clearing.  The last CTA to finish
-//    resets the ticket counters and advances the epoch.
+//  * Tile sums are published as one 64-bit word (32-bit epoch tag | fp32
+//    bits); a reader accepts a word only with the current call's tag, so
+//    stale words never need clearing.  The last CTA advances the epoch.
+
 #include <mutex>
 
 #include "common.cuh"
@@ -77,15 +80,31 @@ __device__ __forceinline__ u128 to_fixed(float a, bool& range_err) {
     return static_cast<u128>(m >> (-sh));
 }
 
-// Correctly rounded (monotone) fixed point -> fp64.
-__device__ __forceinline__ double fixed_to_double(u128 x) {
-    if (x == 0) return 0.0;
-    uint64_t hi = static_cast<uint64_t>(x >> 64), lo = static_cast<uint64_t>(x);
-    int lz = hi ? __clzll(static_cast<long long>(hi)) : 64 + __clzll(static_cast<long long>(lo));
-    u128 y = x << lz;
-    uint64_t top = static_cast<uint64_t>(y >> 64);
-    if (static_cast<uint64_t>(y) != 0) top |= 1ull;  // sticky bit
-    return ldexp(__ull2double_rn(top), 64 - lz - kFracBits);
+// Correctly rounded (to nearest, ties to even) fp32 value of the fixed-point
+// number x; monotone in x.  x < 2^104 here (values below 2^44), so the result
+// is a normal float.
+__device__ __forceinline__ float fixed_to_float(u128 x) {
+    if (x == 0) return 0.f;
+    const uint64_t hi = static_cast<uint64_t>(x >> 64), lo = static_cast<uint64_t>(x);
+    const int lz = hi ? __clzll(static_cast<long long>(hi)) : 64 + __clzll(static_cast<long long>(lo));
+    const u128 y = x << lz;  // leading one at bit 127
+    const uint64_t top = static_cast<uint64_t>(y >> 64);
+    const bool rest = static_cast<uint64_t>(y) != 0;
+    uint32_t m = static_cast<uint32_t>(top >> 40);  // 24 bits, leading one included
+    const uint64_t below = top & ((1ull << 40) - 1);
+    const uint64_t half = 1ull << 39;
+    if (below > half || (below == half && (rest || (m & 1u)))) ++m;
+    // value = m * 2^(67 - lz - 23); the leading one of m lands in the exponent
+    // field, and a rounding carry to 2^24 bumps the exponent by one
+    return __uint_as_float((static_cast<uint32_t>(193 - lz) << 23) + m);
+}
+
+// The exact carry E as fp32 hi + lo (hi = fl32(E), lo = fl32(E - hi)).
+__device__ __forceinline__ void fixed_to_float2(u128 E, float& hi, float& lo) {
+    hi = fixed_to_float(E);
+    bool unused = false;
+    const u128 h = to_fixed(hi, unused);
+    lo = E >= h ? fixed_to_float(E - h) : -fixed_to_float(h - E);
 }
 
 __device__ __forceinline__ u128 warp_sum_u128(u128 v) {
@@ -114,54 +133,47 @@ __device__ __forceinline__ ScanState scan_state(const ScanParams& P) {
     return S;
 }
 
-__device__ __forceinline__ void spin_pause(unsigned& spins, bool& timed_out, int lane, int* status) {
-    if (++spins > kSpinLimit) {
-        timed_out = true;
-        if (lane == 0) atomicOr(status, ST_TIMEOUT);
-        return;
-    }
-    if (spins > 8) __nanosleep(spins < 64 ? 64 : 256);
-}
-
 // Exact sum of the published aggregates of tiles [lo, hi), computed by one
-// warp (lane l reads tiles lo + l + 32q); waits until every one of them is
-// published.  All loads of a poll are issued before any is consumed, so a
-// poll costs one round trip.
-constexpr int kLookQ = 16;  // aggregates per lane per poll (512 tiles)
+// warp (lane l takes tiles lo + l + 32q).  A poll issues all of a lane's loads
+// before looking at any; a word is converted and added once, when its tag
+// shows the current call, and later polls only wait for the missing ones.
+// Gives up after kWaitLimitNs (ST_TIMEOUT) and returns what it has.
+constexpr int kLookQ = 16;  // aggregates per lane per chunk (512 tiles)
 
 __device__ u128 sum_aggregates(const ScanState& S, int64_t lo, int64_t hi, unsigned tag_agg, int lane,
                                int* status) {
-    unsigned spins = 0;
-    bool timed_out = false;
     u128 acc = 0;
-    int64_t j0 = lo;  // first aggregate not yet consumed
-    while (j0 < hi) {
-        unsigned long long w[kLookQ];
+    uint64_t t0 = 0;
+    for (int64_t j0 = lo; j0 < hi; j0 += 32 * kLookQ) {
+        unsigned pending = 0;
 #pragma unroll
-        for (int q = 0; q < kLookQ; ++q) {
-            const int64_t j = j0 + lane + 32 * q;
-            w[q] = j < hi ? ld_relaxed_u64(S.aggw + j) : 0ull;
-        }
-        bool ok = true;
-        u128 a = 0;
+        for (int q = 0; q < kLookQ; ++q)
+            if (j0 + lane + 32 * q < hi) pending |= 1u << q;
+        for (;;) {
+            unsigned long long w[kLookQ];
 #pragma unroll
-        for (int q = 0; q < kLookQ; ++q) {
-            const int64_t j = j0 + lane + 32 * q;
-            if (j < hi) {
-                if (static_cast<unsigned>(w[q] >> 32) != tag_agg) ok = false;
-                bool err = false;
-                a += to_fixed(__uint_as_float(static_cast<unsigned>(w[q])), err);
+            for (int q = 0; q < kLookQ; ++q)
+                w[q] = (pending >> q) & 1u ? ld_relaxed_u64(S.aggw + j0 + lane + 32 * q) : 0ull;
+#pragma unroll
+            for (int q = 0; q < kLookQ; ++q) {
+                if (((pending >> q) & 1u) && static_cast<unsigned>(w[q] >> 32) == tag_agg) {
+                    bool err = false;  // range errors are flagged by the tile's owner
+                    acc += to_fixed(__uint_as_float(static_cast<unsigned>(w[q])), err);
+                    pending &= ~(1u << q);
+                }
             }
+            if (!__any_sync(PER_FULL_MASK, pending != 0u)) break;
+            const uint64_t now = global_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                if (lane == 0) atomicOr(status, ST_TIMEOUT);
+                return warp_sum_u128(acc);
+            }
+            __nanosleep(128);
         }
-        if (__all_sync(PER_FULL_MASK, ok)) {
-            acc += warp_sum_u128(a);
-            j0 += 32 * kLookQ;
-            continue;
-        }
-        spin_pause(spins, timed_out, lane, status);
-        if (timed_out) return acc;
     }
-    return acc;
+    return warp_sum_u128(acc);
 }
 
 // Issue the bulk copy of tile `t` into stage buffer `buf` (thread 0 only).
@@ -248,13 +260,12 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
             const u128 excl = run + sum_aggregates(S, k == 0 ? 0 : t - G + 1, t, tag_agg, lane, P.status);
             run = excl + a_fix;
             if (lane == 0) {
-                const double d0 = fixed_to_double(excl);
-                const double d1 = fixed_to_double(excl + a_fix);
-                const float hi = __double2float_rn(d0);
+                float hi, lo;
+                fixed_to_float2(excl, hi, lo);
                 s_carry[st][0] = hi;
-                s_carry[st][1] = __double2float_rn(d0 - static_cast<double>(hi));
-                s_carry[st][2] = hi;                     // fl32(E_t)
-                s_carry[st][3] = __double2float_rn(d1);  // fl32(E_{t+1})
+                s_carry[st][1] = lo;
+                s_carry[st][2] = hi;                             // fl32(E_t)
+                s_carry[st][3] = fixed_to_float(excl + a_fix);   // fl32(E_{t+1})
                 if (range_err) atomicOr(P.status, ST_RANGE);
                 mbar_arrive(&s_carried[st]);
             }
@@ -575,13 +586,12 @@ __global__ void __launch_bounds__(kClusterThreads, 1) build_cdf_cluster_kernel(S
         const u128 excl = warp_sum_u128(mine);
         if (lane == 0) {
         const u128 a_fix = (static_cast<u128>(s_agg[1]) << 64) | s_agg[0];
-        const double d0 = fixed_to_double(excl);
-        const double d1 = fixed_to_double(excl + a_fix);
-        const float hi = __double2float_rn(d0);
+        float hi, lo;
+        fixed_to_float2(excl, hi, lo);
         s_carry[0] = hi;
-        s_carry[1] = __double2float_rn(d0 - static_cast<double>(hi));
+        s_carry[1] = lo;
         s_carry[2] = hi;
-        s_carry[3] = __double2float_rn(d1);
+        s_carry[3] = fixed_to_float(excl + a_fix);
         if (range_err) atomicOr(P.status, ST_RANGE);
         }
     }

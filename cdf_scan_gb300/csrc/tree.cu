@@ -10,11 +10,12 @@
 // equal, bit for bit, to rebuilding the whole tree in the fixed pairwise order
 // tree[j] = tree[2j] + tree[2j+1]:
 //
-//  * small batches (n <= 1024, depth <= 20): one CTA sorts (index, position)
-//    keys, keeps the last occurrence of each index, writes those leaves, builds
-//    the sorted list of dirty nodes of every level, fetches the unchanged
-//    sibling of every dirty node in one parallel round of loads, then
-//    recomputes the dirty nodes level by level in shared memory;
+//  * small batches (n <= 4096): one thread-block cluster of up to 16 CTAs,
+//    CTA r owning the r-th subtree below the top levels, so every duplicate
+//    of an index meets in one CTA: a shared-memory hash table keeps the last
+//    occurrence of each index, the winners write their leaves, and the dirty
+//    64-wide subtrees are recomputed six levels per pass by one warp each;
+//    after one cluster barrier CTA 0 recomputes the few top levels;
 //  * large batches: the last writer of each index is elected with a 64-bit
 //    atomicMax on (epoch << 32 | position), the winners write their leaves,
 //    and the tree is rebuilt bottom-up by a few level-group launches.
