@@ -270,17 +270,23 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def source_sha(files):
+    """sha256 (16 hex digits) over the named files of the CUDA sources."""
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "cdf_scan_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel_name):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[kernel_name]
-        src = os.path.join(ROOT, "cdf_scan_gb300", "csrc", e["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if sha != e["source_sha"]:
+        if source_sha(e["sources"]) != e["source_sha"]:
             return None
         return e["dram_bytes_per_launch"]
     except Exception:
@@ -289,13 +295,23 @@ def traffic_for(kernel_name):
 
 def extras(per, torch, dev, peak):
     """Other headline numbers of the metric, measured in the same run (not
-    the bench value): the 16M scan against HBM, and the tree sample+update
-    step at full fill."""
+    the bench value): the 16M scan against HBM, the 1M-sample sampler, and
+    the tree sample+update step at full fill.  Each is a CUDA graph replayed
+    between CUDA events on the capturing stream."""
     out = {}
-    stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    def time_call(fn, reps, flush_l2=True):
+    def graph_of(body):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        torch.cuda.synchronize()
+        return g
+
+    def time_graph(g, reps, flush_l2=True, per_replay=1):
+        stream = torch.cuda.current_stream()
         ts = []
         for _ in range(reps):
             if flush_l2:
@@ -303,10 +319,10 @@ def extras(per, torch, dev, peak):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            fn()
+            g.replay()
             b.record(stream)
             b.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3)
+            ts.append(a.elapsed_time(b) * 1e3 / per_replay)
         return statistics.median(ts)
 
     S = workloads.STRESS
@@ -315,21 +331,24 @@ def extras(per, torch, dev, peak):
     per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
     for _ in range(3):
         per.per_build_cdf(ctx.handle)
-    us = time_call(lambda: per.per_build_cdf(ctx.handle), 30)
+    us = time_graph(graph_of(lambda: per.per_build_cdf(ctx.handle)), 30)
     gbs = 8 * n / (us * 1e-6) / 1e9
     idx = torch.empty(S["B"], dtype=torch.int32, device=dev)
-    us_s = time_call(lambda: per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx), 20)
+    per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx)
+    us_s = time_graph(graph_of(lambda: per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx)), 20)
     out["stress_build_cdf"] = {"N": n, "us": round(us, 2), "gbs": round(gbs, 1), "frac_of_measured_peak":
                                round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
-                               "l2": "flushed before each rep"}
-    out["stress_sample"] = {"B": S["B"], "us": round(us_s, 2), "samples_per_s": S["B"] / (us_s * 1e-6)}
+                               "l2": "flushed before each rep", "timing": "one-call graph between events"}
+    out["stress_sample"] = {"B": S["B"], "us": round(us_s, 2), "samples_per_s": S["B"] / (us_s * 1e-6),
+                            "l2": "flushed before each rep"}
+    if per.per_check(ctx.handle) != 0:
+        out["stress_build_cdf"]["status"] = "device status not clean"
     ctx.close()
 
     T = workloads.TREE
     cap = T["capacity"]
     ctx = per.PerContext(cap, T["alpha"], per.PER_TREE)
-    p = np.zeros(cap, np.float32)
-    p[:] = workloads.lognormal(cap, workloads.rng(T["seed"], 999))
+    p = workloads.lognormal(cap, workloads.rng(T["seed"], 999))
     per.per_set_priorities(ctx.handle, torch.from_numpy(p).to(dev))
     tidx = torch.empty(T["B"], dtype=torch.int32, device=dev)
     upd_idx = []
@@ -339,21 +358,30 @@ def extras(per, torch, dev, peak):
         i, q = workloads.tree_update_batch(s, tidx.cpu().numpy())
         upd_idx.append(torch.from_numpy(i).to(dev))
         upd_p.append(torch.from_numpy(q).to(dev))
-    k = [0]
 
-    def tree_step():
-        s = k[0] % 8
-        k[0] += 1
-        per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE, tidx)
-        per.per_update(ctx.handle, upd_idx[s], upd_p[s])
-    for _ in range(5):
-        tree_step()
-    us_t = time_call(tree_step, 200, flush_l2=False)
-    out["tree_sample_update_step"] = {"capacity": cap, "B": T["B"], "us": round(us_t, 2),
-                                      "target_us": 20.0, "l2": "warm (tree is 4 MiB, resident across steps)"}
+    def tree_steps():
+        for s in range(8):
+            per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE, tidx)
+            per.per_update(ctx.handle, upd_idx[s], upd_p[s])
+    tree_steps()
+    us_t = time_graph(graph_of(tree_steps), 50, flush_l2=False, per_replay=8)
+    out["tree_sample_update_step"] = {"capacity": cap, "B": T["B"], "us": round(us_t, 2), "target_us": 20.0,
+                                      "l2": "warm (the 4 MiB tree stays resident across steps)",
+                                      "timing": "graph of 8 steps between events, per step"}
     if per.per_check(ctx.handle) != 0:
         out["tree_sample_update_step"]["status"] = "device status not clean"
     ctx.close()
+
+    R = workloads.RESAMPLE
+    logw = torch.from_numpy(workloads.resample_logw()).to(dev)
+    ridx = torch.empty((R["rows"], R["P"]), dtype=torch.int32, device=dev)
+    per.per_resample(logw, 6, 0, ridx)
+    us_r = time_graph(graph_of(lambda: per.per_resample(logw, 6, 0, ridx)), 20)
+    rbytes = 8 * R["rows"] * R["P"]
+    out["resample"] = {"rows": R["rows"], "P": R["P"], "us": round(us_r, 2),
+                       "gbs": round(rbytes / (us_r * 1e-6) / 1e9, 1),
+                       "frac_of_measured_peak": round(rbytes / (us_r * 1e-6) / 1e9 / peak, 4),
+                       "l2": "flushed before each rep"}
     return out
 
 
