@@ -387,7 +387,8 @@ def extras(per, torch, dev, peak):
 
 # ------------------------------------------------------ kernel cases --------
 
-KERNEL_CASES = ("scan_stress", "scan_minibatch", "sample_stress", "tree_step", "resample", "is_weights_heavy")
+KERNEL_CASES = ("scan_stress", "scan_minibatch", "sample_stress", "sample_minibatch", "is_weights_minibatch",
+                "update_minibatch", "tree_step", "resample", "is_weights_heavy")
 
 
 def kernel_case(name, reps):
@@ -410,10 +411,18 @@ def kernel_case(name, reps):
         else:
             per.per_build_cdf(ctx.handle)
             body = lambda: per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx)  # noqa: E731
-    elif name == "scan_minibatch":
+    elif name in ("scan_minibatch", "sample_minibatch", "is_weights_minibatch", "update_minibatch"):
         ctx = per.PerContext(N, ALPHA, per.PER_SCAN)
         per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
-        body = lambda: per.per_build_cdf(ctx.handle)  # noqa: E731
+        per.per_build_cdf(ctx.handle)
+        idx = torch.empty(B, dtype=torch.int32, device=dev)
+        w = torch.empty(B, dtype=torch.float32, device=dev)
+        newp = torch.from_numpy(workloads.minibatch_new_priorities(0)).to(dev)
+        per.per_sample(ctx.handle, B, W["seed"], 0, per.PER_SCAN, idx)
+        body = {"scan_minibatch": lambda: per.per_build_cdf(ctx.handle),
+                "sample_minibatch": lambda: per.per_sample(ctx.handle, B, W["seed"], 0, per.PER_SCAN, idx),
+                "is_weights_minibatch": lambda: per.per_is_weights(ctx.handle, idx, BETA, w),
+                "update_minibatch": lambda: per.per_update(ctx.handle, idx, newp)}[name]
     elif name == "is_weights_heavy":
         Hv = workloads.HEAVY
         ctx = per.PerContext(Hv["N"], Hv["alpha"], per.PER_SCAN)

@@ -41,6 +41,12 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 __device__ __forceinline__ void st_f4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -123,6 +129,41 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
         if (mbar_try_wait_for(bar, parity, 20000u)) return true;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// Barrier across a co-resident grid (cooperative launch).  `ticket` only
+// grows: each use adds gridDim.x, so the arrivals of one barrier hold the
+// tickets [g*G, (g+1)*G) and every CTA waits for the end of its own group.
+// The wait is bounded (kWaitLimitNs; ST_TIMEOUT).  Writes before the barrier
+// are visible to every CTA after it (fence + acquire).  On timeout it sets
+// `timeout_bit` in *status and returns false (the same on every thread of the
+// CTA).
+__device__ __forceinline__ bool grid_barrier(unsigned long long* ticket, int* status, int timeout_bit) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned long long G = gridDim.x;
+        const unsigned long long t = atomicAdd(ticket, 1ull);
+        const unsigned long long target = (t / G + 1ull) * G;
+        int ok = 1;
+        uint64_t t0 = 0;
+        while (ld_acquire_u64(ticket) < target) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
+                atomicOr(status, timeout_bit);
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
 }
 
 // ---- Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11) ----------------------

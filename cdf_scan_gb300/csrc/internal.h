@@ -46,7 +46,18 @@ struct per_ctx {
     unsigned long long* winner;       // [capacity] epoch-tagged last writer
     unsigned* ctrs;                   // [NUM_CTRS]
     int* status;                      // device status word
+    float* coarse;                    // [coarse_n] every 64th CDF value (PER_SCAN)
+    int64_t coarse_n;
+    unsigned long long* tickets;      // [NUM_TICKETS] grid-barrier tickets
+    float* slots;                     // [slot_n] per-CTA partial results
+    int slot_n;
 };
+
+// Grid-barrier ticket words (per_ctx::tickets).
+enum : int { TK_ISW = 0, TK_UPD = 1, NUM_TICKETS = 4 };
+
+// Items per entry of the coarse CDF index: coarse[j] = cdf[min(64j+63, n-1)].
+constexpr int kCoarseStride = 64;
 
 // 64-bit words of scan state for up to `tiles` tiles: one tagged aggregate
 // word per tile.

@@ -34,6 +34,9 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->winner);
     cudaFree(c->ctrs);
     cudaFree(c->status);
+    cudaFree(c->coarse);
+    cudaFree(c->tickets);
+    cudaFree(c->slots);
     std::free(c);
 }
 
@@ -82,12 +85,17 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     c->alpha = alpha;
     c->flags = flags;
     c->scan_desc_tiles = (c->alloc_n + 1023) / 1024;
+    c->coarse_n = c->alloc_n / kCoarseStride + 1;
+    c->slot_n = 16 * c->num_sms;
     bool ok = alloc_zero(&c->prio, c->alloc_n, s) == cudaSuccess &&
               alloc_zero(&c->winner, static_cast<size_t>(capacity), s) == cudaSuccess &&
               alloc_zero(&c->ctrs, NUM_CTRS, s) == cudaSuccess &&
-              alloc_zero(&c->status, 1, s) == cudaSuccess;
+              alloc_zero(&c->status, 1, s) == cudaSuccess &&
+              alloc_zero(&c->tickets, NUM_TICKETS, s) == cudaSuccess &&
+              alloc_zero(&c->slots, static_cast<size_t>(c->slot_n), s) == cudaSuccess;
     if (ok && (flags & PER_SCAN))
         ok = alloc_zero(&c->cdf, c->alloc_n, s) == cudaSuccess &&
+             alloc_zero(&c->coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
              alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok) {
@@ -217,7 +225,14 @@ per_status per_check(per_ctx* ctx, void* stream) {
     if (cudaMemcpyAsync(&st, ctx->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaMemsetAsync(ctx->status, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
         return PER_ERR_CUDA;
-    if (st & ST_TIMEOUT) return PER_ERR_TIMEOUT;
+    if (st & ST_TIMEOUT) {
+        // a grid barrier may have been left short of arrivals: restart the
+        // ticket counts so the next call's barriers line up again
+        if (cudaMemsetAsync(ctx->tickets, 0, NUM_TICKETS * sizeof(unsigned long long), s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return PER_ERR_CUDA;
+        return PER_ERR_TIMEOUT;
+    }
     if (st & ST_RANGE) return PER_ERR_RANGE;
     if (st & ST_VALUE) return PER_ERR_VALUE;
     if (st & ST_EMPTY) return PER_ERR_EMPTY;

@@ -22,6 +22,7 @@ constexpr int kWindowCap = 12288;  // floats staged per CTA (48 KB)
 
 struct SampleParams {
     const float* __restrict__ cdf;
+    const float* __restrict__ coarse;  // coarse[j] = cdf[min(64j + 63, n - 1)], or nullptr
     int n;
     int B;
     uint64_t seed, offset;
@@ -142,6 +143,128 @@ __global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
     }
 }
 
+// ---- with the coarse index -------------------------------------------------
+//
+// build_cdf leaves coarse[j] = cdf[min(64j + 63, n - 1)].  When the whole
+// index fits a CTA's shared memory, one bulk copy stages it; the first block
+// j with coarse[j] >= u holds lower_bound(cdf, u) (coarse is a subsequence of
+// the non-decreasing CDF), so the CTA's window is found without a single
+// dependent global load, then staged with a second bulk copy and searched
+// per thread in shared memory.
+
+constexpr int kCoarseCap = 4096;  // coarse entries staged per CTA (16 KB)
+
+__device__ __forceinline__ int smem_lower_bound(const float* a, int lo, int hi, float u) {
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < u) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <int THREADS, int SPT>
+__global__ void __launch_bounds__(THREADS) sample_coarse_kernel(SampleParams P) {
+    extern __shared__ __align__(128) float s_dyn[];  // kCoarseCap coarse entries, then the window
+    float* s_coarse = s_dyn;
+    float* s_win = s_dyn + kCoarseCap;
+    __shared__ __align__(8) uint64_t s_bar[2];
+    __shared__ int s_lo, s_hi;
+
+    const int k0 = blockIdx.x * THREADS * SPT;
+    const int kend = min(P.B, k0 + THREADS * SPT);  // exclusive
+    const int nc = (P.n + kCoarseStride - 1) / kCoarseStride;
+    if (threadIdx.x == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        // whole 16-byte groups; the coarse allocation is padded past nc
+        const unsigned bytes = (static_cast<unsigned>(nc) * 4u + 15u) & ~15u;
+        mbar_arrive_expect_tx(&s_bar[0], bytes);
+        bulk_copy_g2s(s_coarse, P.coarse, bytes, &s_bar[0]);
+    }
+    const float T = __ldg(P.cdf + P.n - 1);
+    if (!(T > 0.f)) {
+        if (threadIdx.x == 0) {
+            atomicOr(P.status, ST_EMPTY);
+            if (!mbar_wait_bounded(&s_bar[0], 0)) atomicOr(P.status, ST_TIMEOUT);  // no copy left in flight
+        }
+        for (int s = 0; s < SPT; ++s) {
+            const int k = k0 + threadIdx.x + s * THREADS;
+            if (k < kend) P.out[k] = 0;
+        }
+        return;
+    }
+    const float fB = static_cast<float>(P.B);
+    float u[SPT];
+#pragma unroll
+    for (int s = 0; s < SPT; ++s) {
+        const int k = k0 + threadIdx.x + s * THREADS;
+        u[s] = k < kend ? stratified_threshold(k, draw_u(P, k), fB, T) : 0.f;
+    }
+    __syncthreads();  // barrier initialisation visible to every thread
+    if (!mbar_wait_bounded(&s_bar[0], 0)) atomicOr(P.status, ST_TIMEOUT);
+    if (threadIdx.x == 0) {
+        const float uf = stratified_threshold(k0, draw_u(P, k0), fB, T);
+        s_lo = smem_lower_bound(s_coarse, 0, nc, uf);
+    }
+    if (threadIdx.x == (THREADS > 32 ? 32 : 0)) {
+        const float ul = stratified_threshold(kend - 1, draw_u(P, kend - 1), fB, T);
+        s_hi = smem_lower_bound(s_coarse, 0, nc, ul);
+    }
+    __syncthreads();
+    const int jl = min(s_lo, nc - 1), jh = min(s_hi, nc - 1);
+    const int a0 = jl * kCoarseStride;
+    const int a1 = min(jh * kCoarseStride + kCoarseStride, P.n);  // exclusive
+    const int a1r = (a1 + 3) & ~3;                                 // the CDF allocation is padded
+    int res[SPT];
+    if (a1r - a0 <= kWindowCap) {
+        if (threadIdx.x == 0) {
+            const unsigned bytes = static_cast<unsigned>(a1r - a0) * 4u;
+            mbar_arrive_expect_tx(&s_bar[1], bytes);
+            bulk_copy_g2s(s_win, P.cdf + a0, bytes, &s_bar[1]);
+        }
+        if (!mbar_wait_bounded(&s_bar[1], 0)) atomicOr(P.status, ST_TIMEOUT);
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) res[s] = min(a0 + smem_lower_bound(s_win, 0, a1 - a0, u[s]), P.n - 1);
+    } else {
+        // a very skewed window: each thread finds its own 64-item block, then
+        // searches it in global memory
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            const int j = min(smem_lower_bound(s_coarse, jl, jh + 1, u[s]), nc - 1);
+            int lo = j * kCoarseStride, hi = min(lo + kCoarseStride, P.n);
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(P.cdf + mid) < u[s]) lo = mid + 1;
+                else hi = mid;
+            }
+            res[s] = min(lo, P.n - 1);
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < SPT; ++s) {
+        const int k = k0 + threadIdx.x + s * THREADS;
+        if (k < kend) P.out[k] = res[s];
+    }
+}
+
+template <int THREADS, int SPT>
+per_status launch_coarse_cfg(const SampleParams& P, cudaStream_t s) {
+    const int per_cta = THREADS * SPT;
+    const unsigned grid = static_cast<unsigned>((P.B + per_cta - 1) / per_cta);
+    const int smem = (kCoarseCap + kWindowCap) * static_cast<int>(sizeof(float));
+    static bool configured = false;
+    if (!configured) {
+        if (cudaFuncSetAttribute(sample_coarse_kernel<THREADS, SPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem) != cudaSuccess)
+            return PER_ERR_CUDA;
+        configured = true;
+    }
+    sample_coarse_kernel<THREADS, SPT><<<grid, THREADS, smem, s>>>(P);
+    per_note_launch();
+    return cuda_status(cudaGetLastError());
+}
+
 template <int THREADS, int SPT>
 per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
     const int per_cta = THREADS * SPT;
@@ -176,7 +299,22 @@ per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
     P.u01 = u01;
     P.out = out;
     P.status = ctx->status;
+    P.coarse = ctx->coarse;
     const double ratio = static_cast<double>(P.n) / static_cast<double>(B);
+    if (ctx->coarse && (P.n + kCoarseStride - 1) / kCoarseStride <= kCoarseCap) {
+        // latency first: as many samples per CTA as keep the expected window
+        // within ~2/3 of the staging buffer
+        int per_cta = 1024;
+        while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
+        switch (per_cta) {
+            case 1024: return launch_coarse_cfg<256, 4>(P, s);
+            case 512: return launch_coarse_cfg<256, 2>(P, s);
+            case 256: return launch_coarse_cfg<256, 1>(P, s);
+            case 128: return launch_coarse_cfg<128, 1>(P, s);
+            case 64: return launch_coarse_cfg<64, 1>(P, s);
+            default: return launch_coarse_cfg<32, 1>(P, s);
+        }
+    }
     int per_cta = 1024;
     while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
     while (per_cta > 32 && (B + per_cta - 1) / per_cta < 2 * ctx->num_sms) per_cta >>= 1;

@@ -52,6 +52,7 @@ struct ScanParams {
     unsigned* ctrs;
     int* status;
     unsigned num_tiles;
+    float* coarse;  // every kCoarseStride-th CDF value (or nullptr)
 };
 
 // fp32 (>= 0) -> fixed point with kFracBits fractional bits, truncating below
@@ -321,6 +322,14 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
                         for (int e = 0; e < 4; ++e)
                             if (i0 + e < valid) P.cdf[tile_base + i0 + e] = oo[e];
                     }
+                    if (P.coarse) {  // coarse[j] = cdf[min(64j + 63, n - 1)]
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int64_t g = tile_base + i0 + e;
+                            if (g < P.n && ((g & (kCoarseStride - 1)) == kCoarseStride - 1 || g == P.n - 1))
+                                P.coarse[g / kCoarseStride] = oo[e];
+                        }
+                    }
                 }
             }
             compute_sync();  // the stage was read by everyone
@@ -451,222 +460,159 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
     }
 }
 
-// ---- small inputs: one thread-block cluster, DSMEM exchange ----------------
+// ---- one wave of tiles: every tile's CTA resident at once ------------------
 //
-// For n <= kClusterMax * TILE_C the whole array fits one cluster: CTA r of
-// the cluster scans tile r in registers (same per-warp monotone scan as
-// above), publishes its exact tile sum in its own shared memory, and after
-// one cluster barrier reads the sums of CTAs 0..r-1 through distributed
-// shared memory.  The exact 128-bit sum makes the carry independent of order;
-// the clamp bounds fl32(E_r), fl32(E_r + a_r) keep the CDF monotone.  No
-// global scratch, no atomics, no lookback.
+// For inputs that fit one wave of co-resident CTAs (cooperative launch), CTA c
+// scans tile c (THREADS x 8 items) entirely in registers: the same per-warp
+// monotone scan as above (thread-serial over 8 items, warp shuffles, exact
+// max-scan repair, left fold across warps), publishes the tile's fp32 sum as
+// one tagged word, and one warp sums the words of tiles 0..c-1 exactly
+// (128-bit fixed point) while the other warps finish their local values.  No
+// shared-memory ring, no second pass: the data never leaves registers.
 
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ unsigned long long dsmem_ld_u64(const void* local_ptr, unsigned rank) {
-    unsigned remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local_ptr)), "r"(rank));
-    unsigned long long v;
-    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
-    return v;
-}
-
-constexpr int kClusterThreads = 512;
-constexpr int kClusterItems = 32;                       // per thread
-constexpr int kClusterTile = kClusterThreads * kClusterItems;  // 16384
-constexpr int kClusterMax = 16;
-
-__global__ void __launch_bounds__(kClusterThreads, 1) build_cdf_cluster_kernel(ScanParams P) {
-    constexpr int ITEMS = kClusterItems;
-    constexpr int LANE_ITEMS = 8;
-    constexpr int SUB = ITEMS / LANE_ITEMS;
-    constexpr int WCHUNK = 32 * ITEMS;
-    constexpr int WARPS = kClusterThreads / 32;
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) build_cdf_wave_kernel(ScanParams P) {
+    constexpr int ITEMS = 8;
+    constexpr int WARPS = THREADS / 32;
+    constexpr int TILE = THREADS * ITEMS;
     __shared__ float s_wtot[WARPS];
-    __shared__ __align__(16) unsigned long long s_agg[2];
-    __shared__ float s_carry[4];
+    __shared__ float4 s_carry;
+    __shared__ unsigned s_epoch;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned r = cluster_rank();
-    const int64_t tile_base = static_cast<int64_t>(r) * kClusterTile;
-    int64_t valid = P.n - tile_base;
-    valid = valid < 0 ? 0 : (valid > kClusterTile ? kClusterTile : valid);
-    const bool full = valid == kClusterTile;
+    const int64_t c = blockIdx.x;
+    const int64_t base = c * TILE;
+    const int i0 = warp * (32 * ITEMS) + lane * ITEMS;  // this lane's first item in the tile
+    if (threadIdx.x == 0) s_epoch = ld_relaxed_u32(P.ctrs + CTR_SCAN_EPOCH);
 
     float v[ITEMS];
+    if (base + i0 + ITEMS <= P.n) {
+        const float4 a = ld_f4(P.p + base + i0), b = ld_f4(P.p + base + i0 + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < ITEMS; ++e) v[e] = base + i0 + e < P.n ? P.p[base + i0 + e] : 0.f;
+    }
     bool bad = false;
+    pow_alpha_n<ITEMS>(v, P.alpha, P.pow_mode, bad, [&](int e) {
+        return base + i0 + e < P.n ? P.p[base + i0 + e] : 0.f;
+    });
+    if (base + i0 + ITEMS > P.n) {  // padding beyond n contributes 0 (p^0 would be 1)
 #pragma unroll
-    for (int s = 0; s < SUB; ++s) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i0 = warp * WCHUNK + s * 256 + lane * LANE_ITEMS + 4 * h;
-            float4 q;
-            if (full || i0 + 3 < valid) {
-                q = ld_f4(P.p + tile_base + i0);
-            } else {
-                q.x = i0 < valid ? P.p[tile_base + i0] : 0.f;
-                q.y = i0 + 1 < valid ? P.p[tile_base + i0 + 1] : 0.f;
-                q.z = i0 + 2 < valid ? P.p[tile_base + i0 + 2] : 0.f;
-                q.w = i0 + 3 < valid ? P.p[tile_base + i0 + 3] : 0.f;
-            }
-            const float4 pa = pow4_alpha(q, P.alpha, P.pow_mode, bad);
-            float a0 = pa.x, a1 = pa.y, a2 = pa.z, a3 = pa.w;
-            if (!full) {
-                a0 = i0 < valid ? a0 : 0.f;
-                a1 = i0 + 1 < valid ? a1 : 0.f;
-                a2 = i0 + 2 < valid ? a2 : 0.f;
-                a3 = i0 + 3 < valid ? a3 : 0.f;
-            }
-            v[s * LANE_ITEMS + 4 * h + 0] = a0;
-            v[s * LANE_ITEMS + 4 * h + 1] = a1;
-            v[s * LANE_ITEMS + 4 * h + 2] = a2;
-            v[s * LANE_ITEMS + 4 * h + 3] = a3;
-        }
+        for (int e = 0; e < ITEMS; ++e)
+            if (base + i0 + e >= P.n) v[e] = 0.f;
     }
     if (__any_sync(PER_FULL_MASK, bad) && lane == 0) atomicOr(P.status, ST_VALUE);
 
-    float carry = 0.f;
+    // warp-local inclusive scan, monotone across lanes
 #pragma unroll
-    for (int s = 0; s < SUB; ++s) {
-        float rr[LANE_ITEMS];
-        rr[0] = v[s * LANE_ITEMS];
+    for (int e = 1; e < ITEMS; ++e) v[e] = v[e - 1] + v[e];
+    float x = v[ITEMS - 1];
 #pragma unroll
-        for (int e = 1; e < LANE_ITEMS; ++e) rr[e] = rr[e - 1] + v[s * LANE_ITEMS + e];
-        float x = rr[LANE_ITEMS - 1];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const float y = __shfl_up_sync(PER_FULL_MASK, x, d);
-            if (lane >= d) x += y;
-        }
-        float ex = __shfl_up_sync(PER_FULL_MASK, x, 1);
-        if (lane == 0) ex = 0.f;
-        const float base = carry + ex;
-#pragma unroll
-        for (int e = 0; e < LANE_ITEMS; ++e) rr[e] = base + rr[e];
-        float mx = rr[LANE_ITEMS - 1];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const float y = __shfl_up_sync(PER_FULL_MASK, mx, d);
-            if (lane >= d) mx = fmaxf(mx, y);
-        }
-        float pm = __shfl_up_sync(PER_FULL_MASK, mx, 1);
-        if (lane == 0) pm = carry;
-#pragma unroll
-        for (int e = 0; e < LANE_ITEMS; ++e) v[s * LANE_ITEMS + e] = fmaxf(rr[e], pm);
-        carry = __shfl_sync(PER_FULL_MASK, mx, 31);
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(PER_FULL_MASK, x, d);
+        if (lane >= d) x += y;
     }
-    if (lane == 0) s_wtot[warp] = carry;
+    float ex = __shfl_up_sync(PER_FULL_MASK, x, 1);
+    if (lane == 0) ex = 0.f;
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e) v[e] = ex + v[e];
+    float mx = v[ITEMS - 1];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(PER_FULL_MASK, mx, d);
+        if (lane >= d) mx = fmaxf(mx, y);
+    }
+    float pm = __shfl_up_sync(PER_FULL_MASK, mx, 1);
+    if (lane == 0) pm = 0.f;
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e) v[e] = fmaxf(v[e], pm);
+    if (lane == 31) s_wtot[warp] = mx;
     __syncthreads();
+    const unsigned tag_agg = 2u * s_epoch;
+
+    // publish the tile sum, then gather the carry (warp 0) while every warp
+    // applies its left-fold offset
+    float agg = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) agg = agg + s_wtot[w];
+    if (threadIdx.x == 0)
+        *reinterpret_cast<volatile unsigned long long*>(P.desc + c) =
+            (static_cast<unsigned long long>(tag_agg) << 32) | __float_as_uint(agg);
+    if (warp == 0) {
+        const u128 excl = sum_aggregates(scan_state(P), 0, c, tag_agg, lane, P.status);
+        if (lane == 0) {
+            bool range_err = false;
+            const u128 a_fix = to_fixed(agg, range_err);
+            float hi, lo;
+            fixed_to_float2(excl, hi, lo);
+            s_carry = make_float4(hi, lo, hi, fixed_to_float(excl + a_fix));
+            if (range_err) atomicOr(P.status, ST_RANGE);
+        }
+    }
     float off = 0.f;
     for (int w = 0; w < warp; ++w) off = off + s_wtot[w];
-    bool range_err = false;
-    if (threadIdx.x == 0) {
-        float agg = 0.f;
-        for (int w = 0; w < WARPS; ++w) agg = agg + s_wtot[w];
-        const u128 a_fix = to_fixed(agg, range_err);
-        s_agg[0] = static_cast<unsigned long long>(a_fix);
-        s_agg[1] = static_cast<unsigned long long>(a_fix >> 64);
-    }
-    cluster_sync();  // every CTA's tile sum is published in its shared memory
-    if (warp == 0) {
-        // lane q < r reads CTA q's sum: one parallel round of DSMEM loads
-        u128 mine = 0;
-        if (static_cast<unsigned>(lane) < r) {
-            const unsigned long long lo = dsmem_ld_u64(&s_agg[0], lane);
-            const unsigned long long hi = dsmem_ld_u64(&s_agg[1], lane);
-            mine = (static_cast<u128>(hi) << 64) | lo;
-        }
-        const u128 excl = warp_sum_u128(mine);
-        if (lane == 0) {
-        const u128 a_fix = (static_cast<u128>(s_agg[1]) << 64) | s_agg[0];
-        float hi, lo;
-        fixed_to_float2(excl, hi, lo);
-        s_carry[0] = hi;
-        s_carry[1] = lo;
-        s_carry[2] = hi;
-        s_carry[3] = fixed_to_float(excl + a_fix);
-        if (range_err) atomicOr(P.status, ST_RANGE);
-        }
-    }
     __syncthreads();
-    const float hi = s_carry[0], lo = s_carry[1], sig_lo = s_carry[2], sig_hi = s_carry[3];
+    const float4 cy = s_carry;
+    float o[ITEMS];
 #pragma unroll
-    for (int s = 0; s < SUB; ++s) {
+    for (int e = 0; e < ITEMS; ++e) o[e] = fminf(fmaxf(cy.x + (cy.y + (off + v[e])), cy.z), cy.w);
+    if (base + i0 + ITEMS <= P.n) {
+        st_f4(P.cdf + base + i0, make_float4(o[0], o[1], o[2], o[3]));
+        st_f4(P.cdf + base + i0 + 4, make_float4(o[4], o[5], o[6], o[7]));
+    } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i0 = warp * WCHUNK + s * 256 + lane * LANE_ITEMS + 4 * h;
-            float o[4];
+        for (int e = 0; e < ITEMS; ++e)
+            if (base + i0 + e < P.n) P.cdf[base + i0 + e] = o[e];
+    }
+    if (P.coarse) {  // coarse[j] = cdf[min(64j + 63, n - 1)]
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float loc = off + v[s * LANE_ITEMS + 4 * h + e];
-                o[e] = fminf(fmaxf(hi + (lo + loc), sig_lo), sig_hi);
-            }
-            if (full || i0 + 3 < valid) {
-                st_f4(P.cdf + tile_base + i0, make_float4(o[0], o[1], o[2], o[3]));
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (i0 + e < valid) P.cdf[tile_base + i0 + e] = o[e];
-            }
+        for (int e = 0; e < ITEMS; ++e) {
+            const int64_t g = base + i0 + e;
+            if (g < P.n && ((g & (kCoarseStride - 1)) == kCoarseStride - 1 || g == P.n - 1))
+                P.coarse[g / kCoarseStride] = o[e];
         }
     }
-    cluster_sync();  // keep shared memory alive until every CTA has read it
+
+    // ---- the last CTA to finish advances the epoch for the next call ---------
+    if (threadIdx.x == 0) {
+        const unsigned done = atomicAdd(P.ctrs + CTR_SCAN_DONE, 1u);
+        if (done == gridDim.x - 1u) {
+            P.ctrs[CTR_SCAN_DONE] = 0u;
+            unsigned next = s_epoch + 1u;
+            if (next >= (1u << 30)) {  // epoch wrap: clear all scan state once
+                for (int64_t i = 0; i < P.desc_tiles; ++i) P.desc[i] = 0ull;
+                next = 1u;
+            }
+            P.ctrs[CTR_SCAN_EPOCH] = next;
+        }
+    }
 }
 
-// Launches the cluster path when n fits one cluster the GPU can schedule;
+// Launches the one-wave kernel when every tile's CTA can be resident at once;
 // returns PER_ERR_STATE (nothing launched) otherwise.
-per_status launch_scan_cluster(ScanParams P, cudaStream_t s) {
-    const int64_t ctas = (P.n + kClusterTile - 1) / kClusterTile;
-    if (ctas > kClusterMax) return PER_ERR_STATE;
-    static int max_ok = -1;  // largest cluster size verified schedulable
-    if (max_ok < 0) {
-        if (cudaFuncSetAttribute(build_cdf_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            max_ok = 8;
-        } else {
-            max_ok = 1;
-            for (int c = kClusterMax; c >= 1; c >>= 1) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(c);
-                cfg.blockDim = dim3(kClusterThreads);
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = c;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                int nclusters = 0;
-                if (cudaOccupancyMaxActiveClusters(&nclusters, build_cdf_cluster_kernel, &cfg) == cudaSuccess &&
-                    nclusters > 0) {
-                    max_ok = c;
-                    break;
-                }
-                cudaGetLastError();
-            }
-        }
+template <int THREADS>
+per_status launch_scan_wave(ScanParams P, int num_sms, cudaStream_t s) {
+    constexpr int TILE = THREADS * 8;
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_wave_kernel<THREADS>, THREADS, 0) !=
+            cudaSuccess)
+            return PER_ERR_CUDA;
+        if (per_sm < 1) per_sm = 1;
     }
-    if (ctas > max_ok) return PER_ERR_STATE;
+    const int64_t tiles = (P.n + TILE - 1) / TILE;
+    if (tiles > static_cast<int64_t>(num_sms) * per_sm || tiles > P.desc_tiles) return PER_ERR_STATE;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-    cfg.blockDim = dim3(kClusterThreads);
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles));
+    cfg.blockDim = dim3(THREADS);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(ctas);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_cluster_kernel, P);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_wave_kernel<THREADS>, P);
     per_note_launch();
     return cuda_status(e);
 }
@@ -712,8 +658,14 @@ per_status launch_scan(ScanParams P, int num_sms, cudaStream_t s) {
 // Tile size: 4096 items for large inputs (fewer lookback steps per byte);
 // 2048 items when that would leave SMs without a tile.
 per_status scan_dispatch(ScanParams P, int num_sms, cudaStream_t s) {
-    if (P.n <= static_cast<int64_t>(kClusterMax) * kClusterTile) {
-        const per_status st = launch_scan_cluster(P, s);
+    // one wave of 2048-item tiles for small inputs, of 4096-item tiles up to
+    // what the GPU can hold at once, then the persistent ring
+    if (P.n <= int64_t(1) << 19) {
+        const per_status st = launch_scan_wave<256>(P, num_sms, s);
+        if (st != PER_ERR_STATE) return st;
+    }
+    {
+        const per_status st = launch_scan_wave<512>(P, num_sms, s);
         if (st != PER_ERR_STATE) return st;
     }
     const int64_t big_tiles = (P.n + 4095) / 4096;
@@ -736,6 +688,7 @@ per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s) {
     P.ctrs = ctx->ctrs;
     P.status = ctx->status;
     P.num_tiles = 0;
+    P.coarse = ctx->coarse;
     return scan_dispatch(P, ctx->num_sms, s);
 }
 
@@ -830,6 +783,7 @@ extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, floa
     P.ctrs = reinterpret_cast<unsigned*>(scratch + kNoAllocStateWords);
     P.status = d_status ? d_status : reinterpret_cast<int*>(scratch + kNoAllocStateWords + kNoAllocCtrWords);
     P.num_tiles = 0;
+    P.coarse = nullptr;
     // same kernel and tile choice as per_build_cdf; at most 4096 tiles for n <= 2^24
     return scan_dispatch(P, g_noalloc_sms[dev], s);
 }

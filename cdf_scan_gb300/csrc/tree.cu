@@ -192,6 +192,41 @@ __global__ void apply_winners_kernel(const int32_t* __restrict__ idx, const floa
     }
 }
 
+// Scan-only contexts: the last occurrence of every index wins, in one
+// cooperative launch.  (1) Every batch position k writes (epoch << 32 | k)
+// into winner[idx_k] with atomicMax, so the largest position of each index
+// survives; (2) after one grid barrier each position that won writes its
+// priority.  The epoch (read by every CTA before the barrier) is advanced by
+// CTA 0 after it, so winner slots never need clearing.
+__global__ void __launch_bounds__(256) update_scan_kernel(const int32_t* __restrict__ idx,
+                                                          const float* __restrict__ p, int n, int64_t capacity,
+                                                          unsigned long long* winner, float* __restrict__ prio,
+                                                          unsigned* ctrs, unsigned long long* ticket, int* status) {
+    const unsigned epoch = ld_relaxed_u32(ctrs + CTR_UPD_EPOCH);
+    const int stride = gridDim.x * blockDim.x;
+    bool bad = false;
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
+        const int32_t i = idx[k];
+        if (i < 0 || i >= capacity) {
+            bad = true;
+            continue;
+        }
+        atomicMax(winner + i, (static_cast<unsigned long long>(epoch) << 32) | static_cast<unsigned>(k));
+    }
+    grid_barrier(ticket, status, ST_TIMEOUT);
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctrs[CTR_UPD_EPOCH] = epoch + 1u;  // 2^32 updates before a wrap
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
+        const int32_t i = idx[k];
+        if (i < 0 || i >= capacity) continue;
+        if (__ldcg(winner + i) == ((static_cast<unsigned long long>(epoch) << 32) | static_cast<unsigned>(k))) {
+            const float v = p[k];
+            if (!(v >= 0.f)) bad = true;
+            prio[i] = v;
+        }
+    }
+    if (bad) atomicOr(status, ST_VALUE);
+}
+
 // ====================================================== small-batch update ===
 //
 // One CTA.  (1) Each index is inserted into a shared-memory hash table
@@ -505,6 +540,29 @@ per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n
         const cudaError_t e = cudaLaunchKernelEx(&cfg, small_update_kernel, idx, p, n, ctx->capacity, ctx->prio,
                                                  ctx->tree, ctx->log2_cap, ctx->alpha, ctx->alpha == 1.0f,
                                                  ctx->status);
+        per_note_launch();
+        return cuda_status(e);
+    }
+    if (!has_tree) {
+        static int per_sm = 0;
+        if (per_sm == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, update_scan_kernel, 256, 0) != cudaSuccess)
+                return PER_ERR_CUDA;
+            if (per_sm < 1) per_sm = 1;
+        }
+        int ctas = (n + 255) / 256;
+        if (ctas > per_sm * ctx->num_sms) ctas = per_sm * ctx->num_sms;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, update_scan_kernel, idx, p, n, ctx->capacity, ctx->winner,
+                                                 ctx->prio, ctx->ctrs, ctx->tickets + TK_UPD, ctx->status);
         per_note_launch();
         return cuda_status(e);
     }

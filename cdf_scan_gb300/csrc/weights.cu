@@ -6,13 +6,15 @@
 // equivalent max-normalised form w_k = (pa_min / pa_{idx_k})^beta, pa_min the
 // smallest pa in the batch: the weight of the batch minimum is exactly 1.
 //
-// Two launches over many SMs (the powers dominate, so the work is spread):
-//   1. gather pa for every sample (tree leaves, or p^alpha of the raw
-//      priorities) into the output buffer; warp-shuffle + block minimum, then
-//      an order-independent atomicMin on the float's bit pattern (valid for
-//      non-negative floats);
-//   2. w_k = (pa_min / pa_k)^beta in place; the last CTA resets the minimum
-//      word for the next call.
+// One cooperative launch over many SMs (the powers dominate, so the work is
+// spread):
+//   1. every sample's pa (tree leaf, or p^alpha of the raw priority) goes to
+//      the output buffer, and each CTA leaves its minimum in a slot;
+//   2. after one grid barrier every CTA reads all the slots (an
+//      order-independent minimum) and writes w_k = (pa_min / pa_k)^beta in
+//      place.  Nothing needs resetting between calls.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,16 +32,30 @@ struct IswParams {
     float beta;
     int64_t capacity;
     float* out;
-    unsigned* ctrs;
+    float* slots;                 // [gridDim.x] per-CTA minima
+    unsigned long long* ticket;   // grid-barrier ticket
     int* status;
 };
 
-__global__ void __launch_bounds__(kThreads) gather_min_kernel(IswParams P) {
-    __shared__ float s_min[kThreads / 32];
+// Minimum over the CTA of one value per thread (result on every thread).
+__device__ __forceinline__ float block_min(float m, float* s_red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(PER_FULL_MASK, m, o));
+    __syncthreads();  // s_red may still be read from a previous use
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    float b = s_red[0];
+    for (int w = 1; w < kThreads / 32; ++w) b = fminf(b, s_red[w]);
+    return b;
+}
+
+__global__ void __launch_bounds__(kThreads) is_weights_kernel(IswParams P) {
+    __shared__ float s_red[kThreads / 32];
+    const int stride = gridDim.x * kThreads;
     float m = __int_as_float(0x7f800000);  // +inf
     bool bad = false;
-    for (int k = blockIdx.x * kThreads + threadIdx.x; k < P.B; k += gridDim.x * kThreads) {
+    for (int k = blockIdx.x * kThreads + threadIdx.x; k < P.B; k += stride) {
         const int32_t i = P.idx[k];
         float pa;
         if (i < 0 || i >= P.capacity) {
@@ -54,34 +70,25 @@ __global__ void __launch_bounds__(kThreads) gather_min_kernel(IswParams P) {
         m = fminf(m, pa);
     }
     if (bad) atomicOr(P.status, ST_VALUE);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(PER_FULL_MASK, m, o));
-    if (lane == 0) s_min[warp] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float bm = s_min[0];
-        for (int w = 1; w < kThreads / 32; ++w) bm = fminf(bm, s_min[w]);
-        atomicMin(P.ctrs + CTR_ISW_MIN, __float_as_uint(bm));
-    }
-}
-
-__global__ void __launch_bounds__(kThreads) weights_kernel(IswParams P) {
-    const float pa_min = __uint_as_float(ld_relaxed_u32(P.ctrs + CTR_ISW_MIN));
-    for (int k = blockIdx.x * kThreads + threadIdx.x; k < P.B; k += gridDim.x * kThreads)
+    m = block_min(m, s_red);
+    if (threadIdx.x == 0) P.slots[blockIdx.x] = m;
+    grid_barrier(P.ticket, P.status, ST_TIMEOUT);
+    float g = __int_as_float(0x7f800000);
+    for (int j = threadIdx.x; j < static_cast<int>(gridDim.x); j += kThreads) g = fminf(g, __ldcg(P.slots + j));
+    const float pa_min = block_min(g, s_red);
+    for (int k = blockIdx.x * kThreads + threadIdx.x; k < P.B; k += stride)
         P.out[k] = powf(__fdiv_rn(pa_min, P.out[k]), P.beta);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned done = atomicAdd(P.ctrs + CTR_ISW_DONE, 1u);
-        if (done == gridDim.x - 1u) {
-            P.ctrs[CTR_ISW_DONE] = 0u;
-            P.ctrs[CTR_ISW_MIN] = 0xffffffffu;  // above every non-negative float
-        }
-    }
 }
 
 }  // namespace
 
 per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta, float* out, cudaStream_t s) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, is_weights_kernel, kThreads, 0) != cudaSuccess)
+            return PER_ERR_CUDA;
+        if (per_sm < 1) per_sm = 1;
+    }
     IswParams P;
     P.idx = idx;
     P.B = B;
@@ -93,13 +100,23 @@ per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta
     P.beta = beta;
     P.capacity = ctx->capacity;
     P.out = out;
-    P.ctrs = ctx->ctrs;
+    P.slots = ctx->slots;
+    P.ticket = ctx->tickets + TK_ISW;
     P.status = ctx->status;
     int ctas = (B + kThreads - 1) / kThreads;
-    const int max_ctas = 8 * ctx->num_sms;
+    const int max_ctas = std::min(per_sm * ctx->num_sms, ctx->slot_n);
     if (ctas > max_ctas) ctas = max_ctas;
-    gather_min_kernel<<<ctas, kThreads, 0, s>>>(P);
-    weights_kernel<<<ctas, kThreads, 0, s>>>(P);
-    per_note_launch(2);
-    return cuda_status(cudaGetLastError());
+    // cooperative: the grid barrier needs every CTA resident at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, is_weights_kernel, P);
+    per_note_launch();
+    return cuda_status(e);
 }

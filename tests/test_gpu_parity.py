@@ -258,7 +258,7 @@ def test_tree_and_scan_agree_except_in_band():
 # ------------------------------------------------------------ IS weights ----
 
 @pytest.mark.parametrize("flags", [SCAN, TREE])
-@pytest.mark.parametrize("B", [1, 1024, 65536, 1 << 20])
+@pytest.mark.parametrize("B", [1, 1024, 8192, 8193, 65536, 1 << 20])
 def test_is_weights_match_fp64(flags, B):
     N = max(B, 8192)
     p = workloads.heavy_priorities(N=N)

@@ -1,0 +1,213 @@
+"""GPU parity at the workloads' full sizes, in the launch configurations
+bench.py times, against the CPU oracle on the same seeded inputs.
+
+Bars as in test_gpu_parity.py: indices bit-exact when the oracle searches the
+GPU's CDF or tree; CDF within 2e-6 * total (N <= 1M) or 1e-5 * total (16M),
+monotone; priorities after updates bit-exact (last occurrence wins); tree
+nodes bit-exact against the oracle's pairwise rebuild of the GPU leaves; IS
+weights within 1e-6 relative of the fp64 formula.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+per = pytest.importorskip("cdf_scan_gb300")
+SCAN, TREE = per.PER_SCAN, per.PER_TREE
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def new_ctx(p, alpha, flags, capacity=None):
+    ctx = per.PerContext(capacity or p.size, alpha, flags)
+    per.per_set_priorities(ctx.handle, dev(p))
+    return ctx
+
+
+# ------------------------------------------------------------ scan update ---
+
+@pytest.mark.parametrize("n_upd", [1, 7, 8192, 8193, 50000])
+def test_scan_update_last_writer_wins(n_upd):
+    """Scan-only contexts: one-CTA path up to 8192 updates, cooperative beyond;
+    unsorted indices with duplicates."""
+    N = 262144
+    g = workloads.rng(200, n_upd)
+    p0 = workloads.abs_normal(N, g)
+    ctx = new_ctx(p0, 0.6, SCAN)
+    idx = g.integers(0, N, size=n_upd).astype(np.int32)
+    if n_upd > 4:
+        dup = g.choice(n_upd, n_upd // 5, replace=False)
+        idx[dup] = idx[g.integers(0, n_upd, size=dup.size)]
+    newp = workloads.abs_normal(n_upd, g)
+    for _ in range(2):  # the second call runs on the next epoch of the winner slots
+        per.per_update(ctx.handle, dev(idx), dev(newp))
+        want = oracle.apply_updates(p0, idx, newp)
+        assert np.array_equal(host(per.read_priorities(ctx.handle, N)), want)
+        p0 = want
+        newp = workloads.abs_normal(n_upd, g)
+    assert per.per_check(ctx.handle) == 0
+
+
+# ------------------------------------------------------- minibatch loop -----
+
+def test_minibatch_loop_matches_oracle():
+    """The bench step itself: N=262144, 32 rounds of build_cdf, sample 8192,
+    IS weights (beta 0.4), update 8192 at the sampled indices."""
+    W = workloads.MINIBATCH
+    N, B, R, alpha, beta, seed = W["N"], W["B"], W["rounds"], W["alpha"], W["beta"], W["seed"]
+    p = workloads.minibatch_priorities()
+    ctx = new_ctx(p, alpha, SCAN)
+    idx = torch.empty(B, dtype=torch.int32, device="cuda")
+    w = torch.empty(B, dtype=torch.float32, device="cuda")
+    for r in range(R):
+        per.per_build_cdf(ctx.handle)
+        per.per_sample(ctx.handle, B, seed, r * B, SCAN, idx)
+        per.per_is_weights(ctx.handle, idx, beta, w)
+        newp = workloads.minibatch_new_priorities(r)
+        per.per_update(ctx.handle, idx, dev(newp))
+        c = host(per.read_cdf(ctx.handle))[:N]
+        C = oracle.cdf64(p, alpha)
+        assert np.all(np.diff(c) >= 0)
+        assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
+        got = host(idx)
+        want, _ = oracle.sample_cdf_f32(c, B, seed, r * B)
+        assert np.array_equal(got, want), f"round {r}"
+        ww = host(w)
+        assert ww.max() == 1.0
+        assert np.max(np.abs(ww / oracle.is_weights(p, N, alpha, got, beta) - 1.0)) <= 1e-6
+        p = oracle.apply_updates(p, got, newp)
+        assert np.array_equal(host(per.read_priorities(ctx.handle, N)), p), f"round {r}"
+    assert per.per_check(ctx.handle) == 0
+
+
+# ------------------------------------------------------------- stress -------
+
+@pytest.mark.parametrize("alpha", [0.6, 1.0])
+def test_stress_scan_and_sample_full_size(alpha):
+    """N = 16,777,216 uniform(0,1]; B = 1,048,576 stratified samples."""
+    S = workloads.STRESS
+    p = workloads.stress_priorities()
+    ctx = new_ctx(p, alpha, SCAN)
+    per.per_build_cdf(ctx.handle)
+    c = host(per.read_cdf(ctx.handle))[:p.size]
+    assert np.all(np.diff(c) >= 0)
+    C = oracle.cdf64(p, alpha)
+    assert np.max(np.abs(c - C)) <= 1e-5 * C[-1]
+    out = torch.empty(S["B"], dtype=torch.int32, device="cuda")
+    per.per_sample(ctx.handle, S["B"], 1, 0, SCAN, out)
+    want, _ = oracle.sample_cdf_f32(c, S["B"], 1, 0)
+    assert np.array_equal(host(out), want)
+    assert per.per_check(ctx.handle) == 0
+
+
+def test_stress_all_ones_is_exact():
+    """cdf[i] = i + 1 is exact in fp32 up to 2^24 = the stress size."""
+    n = workloads.STRESS["N"]
+    ctx = new_ctx(np.ones(n, np.float32), 0.6, SCAN)
+    per.per_build_cdf(ctx.handle)
+    assert np.array_equal(host(per.read_cdf(ctx.handle))[:n], np.arange(1, n + 1, dtype=np.float32))
+
+
+def test_resample_full_size():
+    """256 rows x 65,536 log-weights N(0, 2^2)."""
+    R = workloads.RESAMPLE
+    lw = workloads.resample_logw()
+    out = torch.empty((R["rows"], R["P"]), dtype=torch.int32, device="cuda")
+    cdf = torch.empty((R["rows"], R["P"]), dtype=torch.float32, device="cuda")
+    per.per_resample(dev(lw), 6, 0, out, out_cdf=cdf)
+    got, c = host(out), host(cdf)
+    for b in range(0, R["rows"], 5):  # every fifth row against the fp64 oracle
+        U = oracle.u01_closed_open(6, 0, b)
+        assert np.array_equal(got[b], oracle.resample_row_on_cdf(c[b], U))
+        _, C, _ = oracle.resample_row(lw[b], U)
+        assert np.max(np.abs(c[b] - C)) <= 2e-6
+    assert np.all(np.diff(got, axis=1) >= 0)
+
+
+# ---------------------------------------------------------------- heavy -----
+
+def test_heavy_workload_scan_and_tree_with_beta_ramp():
+    """N = 1,048,576 lognormal(0, 2) with 1% zeros, alpha 0.7, B = 65,536,
+    beta 0.4 .. 1.0; both sampling paths."""
+    Hv = workloads.HEAVY
+    p = workloads.heavy_priorities()
+    N, B, alpha = p.size, Hv["B"], Hv["alpha"]
+    ctx = new_ctx(p, alpha, SCAN | TREE)
+    per.per_build_cdf(ctx.handle)
+    c = host(per.read_cdf(ctx.handle))[:N]
+    C = oracle.cdf64(p, alpha)
+    assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
+    a = torch.empty(B, dtype=torch.int32, device="cuda")
+    b = torch.empty(B, dtype=torch.int32, device="cuda")
+    per.per_sample(ctx.handle, B, Hv["seed"], 0, SCAN, a)
+    per.per_sample(ctx.handle, B, Hv["seed"], 0, TREE, b)
+    ia, ib = host(a), host(b)
+    assert np.array_equal(ia, oracle.sample_cdf_f32(c, B, Hv["seed"], 0)[0])
+    tree = host(per.read_tree(ctx.handle))
+    assert np.array_equal(ib, oracle.sample_tree(tree, B, Hv["seed"], 0)[0])
+    assert np.all(p[ia] > 0) and np.all(p[ib] > 0)
+    w = torch.empty(B, dtype=torch.float32, device="cuda")
+    for beta in Hv["betas"]:
+        for flags_idx in (a, b):
+            per.per_is_weights(ctx.handle, flags_idx, beta, w)
+            got = host(w)
+            want = oracle.is_weights(p, N, alpha, host(flags_idx), beta)
+            assert got.max() == 1.0
+            assert np.max(np.abs(got / want - 1.0)) <= 1e-6
+    assert per.per_check(ctx.handle) == 0
+
+
+# ----------------------------------------------------------------- tree -----
+
+def test_tree_workload_steps():
+    """Capacity 500,000 (2^19 leaves): initial fill 131,072 lognormal(0,1),
+    then steps of insert 4096 at the ring head, sample 1024, update 1024 with
+    20% duplicate indices.  Every sampled index bit-exact against the oracle's
+    descent of the GPU tree; the whole tree bit-exact against the oracle's
+    pairwise rebuild of the oracle's own leaves at checkpoints."""
+    T = workloads.TREE
+    cap, B, alpha = T["capacity"], T["B"], T["alpha"]
+    prio = np.zeros(cap, np.float32)
+    init = workloads.tree_initial()
+    prio[:init.size] = init
+    ctx = per.PerContext(cap, alpha, TREE)
+    per.per_set_priorities(ctx.handle, dev(prio))
+    size, head = init.size, init.size % cap
+    per.per_set_size(ctx.handle, size)
+    out = torch.empty(B, dtype=torch.int32, device="cuda")
+    steps = 120  # fills the ring (after ~91 steps) and wraps
+    for s in range(steps):
+        ins = workloads.tree_insert(s)
+        ins_idx = ((head + np.arange(ins.size)) % cap).astype(np.int32)
+        per.per_update(ctx.handle, dev(ins_idx), dev(ins))
+        prio = oracle.apply_updates(prio, ins_idx, ins)
+        head = (head + ins.size) % cap
+        size = min(size + ins.size, cap)
+        per.per_set_size(ctx.handle, size)
+        per.per_sample(ctx.handle, B, T["seed"], s * B, TREE, out)
+        got = host(out)
+        tree = host(per.read_tree(ctx.handle))
+        assert np.array_equal(got, oracle.sample_tree(tree, B, T["seed"], s * B)[0]), f"step {s}"
+        assert np.all(got < size)
+        uidx, up = workloads.tree_update_batch(s, got)
+        per.per_update(ctx.handle, dev(uidx), dev(up))
+        prio = oracle.apply_updates(prio, uidx, up)
+        if s % 30 == 29 or s == steps - 1:
+            tree = host(per.read_tree(ctx.handle))
+            leaves = tree[tree.size // 2:]
+            want_leaves = oracle.tree_leaves(prio, alpha, tree.size // 2)
+            d = np.abs(leaves.view(np.int32).astype(np.int64) - want_leaves.view(np.int32).astype(np.int64))
+            assert d.max() <= 4, f"step {s}: leaves differ from pow beyond 4 ulp"
+            assert np.array_equal(tree[1:], oracle.tree_build(leaves)[1:]), f"step {s}"
+    assert per.per_check(ctx.handle) == 0
