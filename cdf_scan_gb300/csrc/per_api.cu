@@ -242,7 +242,7 @@ per_status per_check(per_ctx* ctx, void* stream) {
 per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t seed, uint64_t offset,
                         const float* d_u_rows, int32_t* d_out_idx, float* d_out_cdf, void* stream) {
     if (!d_logw || !d_out_idx || rows < 1 || P < 4 || (P & 3) != 0 || P > (1 << 23)) return PER_ERR_ARG;
-    if (!aligned16(d_logw) || (d_out_cdf && !aligned16(d_out_cdf))) return PER_ERR_ARG;
+    if (!aligned16(d_logw) || !aligned16(d_out_idx) || (d_out_cdf && !aligned16(d_out_cdf))) return PER_ERR_ARG;
     return launch_resample(d_logw, rows, P, seed, offset, d_u_rows, d_out_idx, d_out_cdf,
                            static_cast<cudaStream_t>(stream));
 }

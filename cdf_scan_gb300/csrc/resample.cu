@@ -3,25 +3,39 @@
 // the particle axis, u_j = (j + U_b)/P with one U_b per row, searchsorted
 // (right=False), clamp to P-1).
 //
-// One CTA per row, two passes over the row (the second mostly from L2):
-//   A. online max / sum of exp(lw - max) (fp32, fixed combine order);
-//   B. exp(lw - m) quantised to 40-bit fixed point and scanned with exact
-//      64-bit integer sums (monotone and order-independent), c_i =
-//      fl32(fl32(E_i) * fl32(2^-40 / s)); then, instead of one binary search
-//      per output, every particle i computes n(c) = #{j : u_j <= c} for its
-//      own c_i and its predecessor's c_{i-1} in closed form (a guess from
-//      c*P - U corrected by at most a couple of exact threshold evaluations)
-//      and writes i into outputs [n(c_{i-1}), n(c_i)) -- exactly the outputs
-//      whose lower_bound lands on i.  The last particle's run extends to P,
-//      which is the clamp.
+// One CTA of 512 threads per row (every row of a 256-row batch resident at
+// once), three passes over the row -- the last two served by L2:
+//   1. the row maximum m;
+//   2. the exact total Q of q_i = fix40(exp(lw_i - m)) (40 fractional bits,
+//      64-bit integer sums: order-independent);
+//   3. an exact 64-bit integer scan of the same q_i (8 consecutive particles
+//      per lane, warp shuffles, a block scan per chunk), c_i = f(E_i) *
+//      fl32(1 / Q), f a monotone fp32 rounding of E (u64_to_f32) -- so c is
+//      monotone in the exact prefix E_i -- and then, instead
+//      of one binary search per output, every particle i computes
+//      n(c) = #{j : u_j <= c} for its own c_i in closed form (a guess from
+//      c*P - U corrected by at most a couple of exact threshold evaluations);
+//      particle i owns outputs [n(c_{i-1}), n(c_i)) -- exactly the outputs
+//      whose lower_bound lands on i, the last particle's run extending to P
+//      (the clamp).  Short runs are written by the particle's own lane; long
+//      ones (heavy particles) are queued and written by the whole warp with
+//      16-byte stores.
+// exp is the hardware ex2 of (lw - m) * log2(e): its relative error (~2^-22)
+// stays far inside the CDF tolerance.  For a power-of-two P the threshold
+// division is an exact multiplication by 2^-k.
 #include "common.cuh"
 #include "internal.h"
 
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kChunk = kThreads * 4;
-constexpr float kFix = 1099511627776.0f;  // 2^40
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kLane = 8;                   // consecutive particles per lane per chunk
+constexpr int kBatch = 8;                  // float4 loads in flight per thread in passes 1 and 2
+constexpr int kShortRun = 8;               // runs up to this long are written by their own lane
+constexpr int kQueue = 64;                 // long runs a warp can queue per chunk
+constexpr int kChunk = kThreads * kLane;   // 4096
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct ResampleParams {
     const float* __restrict__ logw;
@@ -32,141 +46,205 @@ struct ResampleParams {
     float* __restrict__ out_cdf;
 };
 
-__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
-    if (m2 == -INFINITY) return;
-    if (m == -INFINITY) {
-        m = m2;
-        s = s2;
-        return;
-    }
-    if (m2 > m) {
-        s = s * expf(m - m2) + s2;
-        m = m2;
-    } else {
-        s = s + s2 * expf(m2 - m);
-    }
-}
-
-__device__ __forceinline__ void lse_add(float& m, float& s, float x) {
-    if (x == -INFINITY) return;
-    if (x > m) {
-        s = (m == -INFINITY) ? 1.f : s * expf(m - x) + 1.f;
-        m = x;
-    } else {
-        s += expf(x - m);
-    }
-}
-
-// Threshold u_j = fl32(fl32(j + U) / P).
-__device__ __forceinline__ float row_threshold(int j, float U, float fP) {
-    return __fdiv_rn(__fadd_rn(__int2float_rn(j), U), fP);
+// Threshold u_j = fl32(fl32(j + U) / P); for a power of two P the division is
+// the exact product with inv_p = 2^-k.
+__device__ __forceinline__ float row_threshold(int j, float U, float fP, float inv_p, bool pow2) {
+    const float a = __fadd_rn(__int2float_rn(j), U);
+    return pow2 ? __fmul_rn(a, inv_p) : __fdiv_rn(a, fP);
 }
 
 // #{ j in [0, P) : u_j <= c }.
-__device__ __forceinline__ int count_le(float c, float U, int P, float fP) {
+__device__ __forceinline__ int count_le(float c, float U, int P, float fP, float inv_p, bool pow2) {
     const float g = __fsub_rn(__fmul_rn(c, fP), U);
     int j;
     if (!(g >= 0.f)) j = -1;
     else if (g >= fP) j = P - 1;
     else j = static_cast<int>(g);
-    while (j + 1 < P && row_threshold(j + 1, U, fP) <= c) ++j;
-    while (j >= 0 && row_threshold(j, U, fP) > c) --j;
+    while (j + 1 < P && row_threshold(j + 1, U, fP, inv_p, pow2) <= c) ++j;
+    while (j >= 0 && row_threshold(j, U, fP, inv_p, pow2) > c) --j;
     return j + 1;
 }
 
-__global__ void __launch_bounds__(kThreads) resample_kernel(ResampleParams R) {
-    __shared__ float s_m[kThreads / 32], s_s[kThreads / 32];
-    __shared__ unsigned long long s_tot[kThreads / 32];
-    __shared__ float s_stats[2];
+// floor(w * 2^40) for w = exp(x - m) in [0, 1], from the float's exponent and
+// mantissa with integer shifts (no 64-bit conversion); -inf weights give 0.
+__device__ __forceinline__ unsigned long long fix40(float x, float m) {
+    const float w = hw_ex2(__fmul_rn(__fsub_rn(x, m), kLog2e));
+    const unsigned bits = __float_as_uint(w);
+    const int sh = static_cast<int>(bits >> 23) - 110;  // w * 2^40 = mant * 2^(e - 150 + 40)
+    const unsigned long long mant = (bits & 0x7fffffu) | 0x800000u;
+    if (sh <= -24) return 0ull;  // below 2^-40, or zero / subnormal
+    return sh >= 0 ? mant << sh : mant >> (-sh);
+}
+
+// Monotone fp32 value of E < 2^56: the high half (below 2^24) is exact in
+// fp32, the low half is rounded once, and one fused multiply-add combines
+// them; a carry into the high half can never make the result decrease.
+__device__ __forceinline__ float u64_to_f32(unsigned long long E) {
+    const float hi = __uint2float_rn(static_cast<unsigned>(E >> 32));
+    const float lo = __uint2float_rn(static_cast<unsigned>(E));
+    return __fmaf_rn(hi, 4294967296.0f, lo);
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long x, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long y = __shfl_up_sync(PER_FULL_MASK, x, d);
+        if (lane >= d) x += y;
+    }
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R) {
+    __shared__ float s_f[kWarps];
+    __shared__ unsigned long long s_u[kWarps];
+    __shared__ unsigned long long s_off[kWarps + 1];
+    __shared__ int s_q[kWarps][3 * kQueue];  // long runs: (particle, first, end) per warp
+    __shared__ int s_qn[kWarps];
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int P = R.P;
     const float* row = R.logw + static_cast<size_t>(b) * P;
     int32_t* orow = R.out + static_cast<size_t>(b) * P;
 
-    // ---- A: max and sum of exp(lw - max) -----------------------------------
-    float m = -INFINITY, s = 0.f;
-    for (int i0 = threadIdx.x * 4; i0 < P; i0 += kChunk) {
-        const float4 q = ld_f4(row + i0);
-        lse_add(m, s, q.x);
-        lse_add(m, s, q.y);
-        lse_add(m, s, q.z);
-        lse_add(m, s, q.w);
+    // ---- 1: row maximum (kBatch loads in flight per thread) -----------------
+    float m = -INFINITY;
+    for (int i0 = threadIdx.x * 4; i0 < P; i0 += kThreads * 4 * kBatch) {
+        float4 q[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kThreads * 4;
+            q[u] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) m = fmaxf(m, fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(PER_FULL_MASK, m, o);
-        const float s2 = __shfl_xor_sync(PER_FULL_MASK, s, o);
-        lse_combine(m, s, m2, s2);
-    }
-    if (lane == 0) {
-        s_m[warp] = m;
-        s_s[warp] = s;
-    }
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(PER_FULL_MASK, m, o));
+    if (lane == 0) s_f[warp] = m;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float bm = s_m[0], bs = s_s[0];
-        for (int w = 1; w < kThreads / 32; ++w) lse_combine(bm, bs, s_m[w], s_s[w]);
-        s_stats[0] = bm;
-        s_stats[1] = bs;
+    float rmax = s_f[0];
+    for (int w = 1; w < kWarps; ++w) rmax = fmaxf(rmax, s_f[w]);
+
+    // ---- 2: exact total -------------------------------------------------------------
+    unsigned long long acc = 0ull;
+    for (int i0 = threadIdx.x * 4; i0 < P; i0 += kThreads * 4 * kBatch) {
+        float4 q[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kThreads * 4;
+            q[u] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            acc += fix40(q[u].x, rmax) + fix40(q[u].y, rmax) + fix40(q[u].z, rmax) + fix40(q[u].w, rmax);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(PER_FULL_MASK, acc, o);
+    if (lane == 0) s_u[warp] = acc;
     __syncthreads();
-    const float rmax = s_stats[0];
-    const float scale = __fdiv_rn(1.0f / kFix, s_stats[1]);
+    unsigned long long Q = 0ull;
+    for (int w = 0; w < kWarps; ++w) Q += s_u[w];
+    // c = fl32(E) * fl32(1 / Q): monotone in E, c(Q) ~= 1
+    const float inv = __fdiv_rn(1.0f, u64_to_f32(Q));
     const float fP = static_cast<float>(P);
+    const bool pow2 = (P & (P - 1)) == 0;
+    const float inv_p = __fdiv_rn(1.0f, fP);
     const float U = R.u_rows ? R.u_rows[b] : u01_closed_open(R.seed, R.offset + static_cast<uint64_t>(b));
 
-    // ---- B: exact fixed-point scan, then scatter each particle's run --------
+    // ---- 3: scan and scatter -----------------------------------------------------
+    // the next chunk's loads are issued before the current chunk is processed
+    float4 nxt[kLane / 4];
+#pragma unroll
+    for (int h = 0; h < kLane / 4; ++h) {
+        const int i = threadIdx.x * kLane + 4 * h;
+        nxt[h] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
     unsigned long long carry = 0ull;
     for (int c0 = 0; c0 < P; c0 += kChunk) {
-        const int i0 = c0 + threadIdx.x * 4;
-        const bool in = i0 < P;
-        float4 q = in ? ld_f4(row + i0) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        const float xs[4] = {q.x, q.y, q.z, q.w};
-        unsigned long long f[4], r[4];
+        const int i0 = c0 + threadIdx.x * kLane;
+        const int nv = min(kLane, P - i0);  // valid particles of this lane (P % 4 == 0)
+        float4 cur[kLane / 4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float w = xs[e] == -INFINITY ? 0.f : expf(xs[e] - rmax);
-            f[e] = __float2ull_rz(__fmul_rn(w, kFix));
+        for (int h = 0; h < kLane / 4; ++h) {
+            cur[h] = nxt[h];
+            const int i = i0 + kChunk + 4 * h;
+            nxt[h] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
-        r[0] = f[0];
-        r[1] = r[0] + f[1];
-        r[2] = r[1] + f[2];
-        r[3] = r[2] + f[3];
-        unsigned long long x = r[3];
+        unsigned long long r[kLane];
+        unsigned long long run = 0ull;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const unsigned long long y = __shfl_up_sync(PER_FULL_MASK, x, d);
-            if (lane >= d) x += y;
+        for (int h = 0; h < kLane / 4; ++h) {
+            run += fix40(cur[h].x, rmax);
+            r[4 * h] = run;
+            run += fix40(cur[h].y, rmax);
+            r[4 * h + 1] = run;
+            run += fix40(cur[h].z, rmax);
+            r[4 * h + 2] = run;
+            run += fix40(cur[h].w, rmax);
+            r[4 * h + 3] = run;
         }
-        if (lane == 31) s_tot[warp] = x;
+        const unsigned long long x = warp_incl_u64(run, lane);
+        if (lane == 31) s_u[warp] = x;
         __syncthreads();
-        const unsigned long long t = s_tot[lane];
-        unsigned long long wi = t;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const unsigned long long y = __shfl_up_sync(PER_FULL_MASK, wi, d);
-            if (lane >= d) wi += y;
+        if (warp == 0) {
+            const unsigned long long t = lane < kWarps ? s_u[lane] : 0ull;
+            const unsigned long long wi = warp_incl_u64(t, lane);
+            if (lane < kWarps) s_off[lane] = wi - t;
+            if (lane == kWarps - 1) s_off[kWarps] = wi;
         }
-        const unsigned long long warp_off = __shfl_sync(PER_FULL_MASK, wi - t, warp);
-        const unsigned long long chunk_total = __shfl_sync(PER_FULL_MASK, wi, 31);
-        const unsigned long long base = carry + warp_off + (x - r[3]);
-        __syncthreads();  // s_tot reused by the next chunk
-        carry += chunk_total;
-        if (!in) continue;
+        __syncthreads();
+        const unsigned long long base = carry + s_off[warp] + (x - run);  // E before this lane's first particle
+        carry += s_off[kWarps];
 
-        float cv[4];
-        int nprev = i0 == 0 ? 0 : count_le(__fmul_rn(__ull2float_rn(base), scale), U, P, fP);
+        // run ends: particle i owns outputs [n(c_{i-1}), n(c_i)); the last
+        // particle's run extends to P (the clamp)
+        int start = 0;  // n(c) of the particle before this lane's first
+        if (i0 >= P) start = P;
+        else if (i0 > 0) start = count_le(__fmul_rn(u64_to_f32(base), inv), U, P, fP, inv_p, pow2);
+        float cv[kLane];
+        int nlast = start;
+        int* q = s_q[warp];
+        if (lane == 0) s_qn[warp] = 0;
+        __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const unsigned long long E = base + r[e];
-            cv[e] = __fmul_rn(__ull2float_rn(E), scale);
+        for (int e = 0; e < kLane; ++e) {
             const int i = i0 + e;
-            const int ncur = (i == P - 1) ? P : count_le(cv[e], U, P, fP);
-            for (int j = nprev; j < ncur; ++j) orow[j] = i;
-            nprev = ncur > nprev ? ncur : nprev;
+            cv[e] = __fmul_rn(u64_to_f32(base + r[e]), inv);
+            int n = nlast;
+            if (e < nv) n = (i == P - 1) ? P : max(count_le(cv[e], U, P, fP, inv_p, pow2), nlast);
+            if (n - nlast <= kShortRun) {
+                for (int j = nlast; j < n; ++j) orow[j] = i;
+            } else {  // a long run: queued for the whole warp
+                const int slot = atomicAdd(&s_qn[warp], 1);
+                if (slot < kQueue) {
+                    q[3 * slot] = i;
+                    q[3 * slot + 1] = nlast;
+                    q[3 * slot + 2] = n;
+                } else {
+                    for (int j = nlast; j < n; ++j) orow[j] = i;
+                }
+            }
+            nlast = n;
         }
-        if (R.out_cdf) st_f4(R.out_cdf + static_cast<size_t>(b) * P + i0, make_float4(cv[0], cv[1], cv[2], cv[3]));
+        if (R.out_cdf && nv > 0) {
+            float* crow = R.out_cdf + static_cast<size_t>(b) * P + i0;
+#pragma unroll
+            for (int h = 0; h < kLane / 4; ++h)
+                if (4 * h < nv) st_f4(crow + 4 * h, make_float4(cv[4 * h], cv[4 * h + 1], cv[4 * h + 2], cv[4 * h + 3]));
+        }
+        __syncwarp();
+        // long runs, one at a time, by all lanes: aligned 16-byte stores for
+        // the body, single stores for the ends
+        const int nq = min(s_qn[warp], kQueue);
+        for (int t = 0; t < nq; ++t) {
+            const int i = q[3 * t], j0 = q[3 * t + 1], j1 = q[3 * t + 2];
+            const int a0 = min((j0 + 3) & ~3, j1), a1 = max(j1 & ~3, a0);
+            if (j0 + lane < a0) orow[j0 + lane] = i;
+            if (a1 + lane < j1) orow[a1 + lane] = i;
+            const int4 v = make_int4(i, i, i, i);
+            for (int j = a0 + 4 * lane; j < a1; j += 128) *reinterpret_cast<int4*>(orow + j) = v;
+        }
+        __syncwarp();  // the queue is reused by the next chunk
     }
 }
 

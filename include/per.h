@@ -212,15 +212,17 @@ per_status per_check(per_ctx* ctx, void* stream);
 /*
  * per_resample -- row-batched systematic resampling (POPCORNBENCH particle
  * filter, reference forward): d_logw is float32[rows][P] row-major (16-byte
- * aligned, P >= 1, P % 4 == 0, rows >= 1).  Per row b:
+ * aligned, 4 <= P <= 2^23, P % 4 == 0, rows >= 1).  Per row b:
  *   w_i = exp(lw_i - m) / s  (m = row max, s = sum_i exp(lw_i - m)),
  *   c = cumsum(w),  u_j = fl32(fl32(j + U_b) / P),  U_b in [0, 1)
  *   idx_j = first i with c_i >= u_j (searchsorted, right=False), clamped P-1
  * U_b = (x >> 8) * 2^-24 from Philox (offset + b) under key seed, or
- * d_u_rows[b] when not NULL.  d_out_idx receives int32[rows][P].  If
- * d_out_cdf is not NULL it receives the float32[rows][P] CDF that was
- * searched.  Needs no context and no scratch.  A row whose log-weights are
- * all -inf or contain NaN gives unspecified indices in [0, P).
+ * d_u_rows[b] when not NULL.  d_out_idx (16-byte aligned) receives
+ * int32[rows][P].  If d_out_cdf (16-byte aligned) is not NULL it receives the
+ * float32[rows][P] CDF that was searched.  Needs no context and no scratch.
+ * A row whose log-weights are all -inf or contain NaN gives unspecified
+ * indices in [0, P).  PER_ERR_ARG: null or misaligned pointers, rows < 1,
+ * P < 4, P % 4 != 0, P > 2^23.
  */
 per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t seed,
                         uint64_t offset, const float* d_u_rows, int32_t* d_out_idx,
