@@ -2,8 +2,9 @@
 
 One step = one PER "train call" of the minibatch workload: N=262144 fp32
 priorities |N(0,1)|+1e-6, alpha=0.6, 32 rounds of
-  build_cdf -> sample 8192 stratified -> IS weights (beta=0.4) ->
-  update the 8192 sampled items with new |N(0,1)|+1e-6 priorities
+  build_cdf -> sample 8192 stratified with their IS weights (beta=0.4;
+  per_sample_weighted) -> update the 8192 sampled items with new
+  |N(0,1)|+1e-6 priorities
 through the library's C ABI.  value = sampled transitions per second over
 all ranks (device-resident inputs); e2e = the same with each step's new
 priorities copied in from pinned host memory and the step's indices and
@@ -42,10 +43,9 @@ L2_FLUSH_BYTES = 512 << 20
 
 # algorithmic bytes per unit: build_cdf reads p and writes cdf
 KERNEL_BYTES = {
-    "build_cdf": lambda: 8 * N,                 # 4 B read + 4 B write per item
-    "sample": lambda: 4 * N + 4 * B,            # every CDF item read once + index write
-    "is_weights": lambda: 12 * B,               # index read + pa gather + weight write
-    "update": lambda: 8 * B + 4 * B + 8 * B,    # idx + p read, priority write, winner slot
+    "build_cdf": lambda: 8 * N,                          # 4 B read + 4 B write per item
+    "sample_is_weights": lambda: 4 * N + 12 * B,         # CDF windows once; index, p gather, weight
+    "update": lambda: 8 * B + 4 * B + 8 * B,             # idx + p read, priority write, winner slot
 }
 
 
@@ -152,8 +152,7 @@ def run_ours(args, rank, world, local_rank):
     # one step = 32 rounds through the C ABI; captured once as a CUDA graph
     calls = {
         "build_cdf": lambda r: per.per_build_cdf(h),
-        "sample": lambda r: per.per_sample(h, B, seed, r * B, per.PER_SCAN, idx[r]),
-        "is_weights": lambda r: per.per_is_weights(h, idx[r], BETA, wts[r]),
+        "sample_is_weights": lambda r: per.per_sample_weighted(h, B, seed, r * B, per.PER_SCAN, BETA, idx[r], wts[r]),
         "update": lambda r: per.per_update(h, idx[r], d_newp[r]),
     }
 

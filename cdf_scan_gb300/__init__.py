@@ -41,6 +41,7 @@ SIGNATURES = {
     "per_build_cdf_noalloc": (ctypes.c_int, [_vp, _i64, _f32, _vp, _vp, _vp]),
     "per_sample": (ctypes.c_int, [_vp, _i32, _u64, _u64, ctypes.c_int, _vp, _vp, _vp]),
     "per_is_weights": (ctypes.c_int, [_vp, _vp, _i32, _f32, _vp, _vp]),
+    "per_sample_weighted": (ctypes.c_int, [_vp, _i32, _u64, _u64, ctypes.c_int, _vp, _f32, _vp, _vp, _vp]),
     "per_total": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp]),
     "per_total_host": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(_f32), _vp]),
     "per_priorities_ptr": (_vp, [_vp]),
@@ -175,6 +176,15 @@ def per_is_weights(ctx: int, idx: torch.Tensor, beta: float, out_w: torch.Tensor
     _check("per_is_weights", lib().per_is_weights(ctx, _ptr(idx, torch.int32, "idx"), B, beta,
                                                   _ptr(out_w, torch.float32, "out_w", B), _stream(stream)))
     return out_w
+
+
+def per_sample_weighted(ctx: int, B: int, seed: int, offset: int, mode: int, beta: float,
+                        out_idx: torch.Tensor, out_w: torch.Tensor, u01: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    _check("per_sample_weighted", lib().per_sample_weighted(
+        ctx, B, seed, offset, mode, _ptr(u01, torch.float32, "u01", B), beta,
+        _ptr(out_idx, torch.int32, "out_idx", B), _ptr(out_w, torch.float32, "out_w", B), _stream(stream)))
+    return out_idx
 
 
 def per_total(ctx: int, mode: int, out: torch.Tensor, stream=None) -> torch.Tensor:

@@ -54,7 +54,7 @@ struct per_ctx {
 };
 
 // Grid-barrier ticket words (per_ctx::tickets).
-enum : int { TK_ISW = 0, TK_UPD = 1, NUM_TICKETS = 4 };
+enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, NUM_TICKETS = 4 };
 
 // Items per entry of the coarse CDF index: coarse[j] = cdf[min(64j+63, n-1)].
 constexpr int kCoarseStride = 64;
@@ -74,6 +74,9 @@ per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
                               int32_t* out, cudaStream_t s);
 per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta, float* out,
                              cudaStream_t s);
+// PER_ERR_STATE (nothing launched) when the fused path does not apply.
+per_status launch_sample_scan_weighted(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+                                       float beta, int32_t* out, float* out_w, cudaStream_t s);
 per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n, cudaStream_t s);
 per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s);
 per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, uint64_t offset,

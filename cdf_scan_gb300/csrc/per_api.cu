@@ -183,6 +183,21 @@ per_status per_is_weights(per_ctx* ctx, const int32_t* d_idx, int32_t B, float b
     return launch_is_weights(ctx, d_idx, B, beta, d_out_w, static_cast<cudaStream_t>(stream));
 }
 
+per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, int mode,
+                               const float* d_u01, float beta, int32_t* d_out_idx, float* d_out_w, void* stream) {
+    if (!ctx || B < 1 || B > (1 << 24) || !d_out_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f)
+        return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mode == static_cast<int>(PER_SCAN) && (ctx->flags & PER_SCAN) && ctx->size >= 1 &&
+        !(ctx->flags & PER_TREE)) {
+        const per_status st = launch_sample_scan_weighted(ctx, B, seed, offset, d_u01, beta, d_out_idx, d_out_w, s);
+        if (st != PER_ERR_STATE) return st;
+    }
+    const per_status st = per_sample(ctx, B, seed, offset, mode, d_u01, d_out_idx, stream);
+    if (st != PER_OK) return st;
+    return per_is_weights(ctx, d_out_idx, B, beta, d_out_w, stream);
+}
+
 per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream) {
     if (!ctx || !d_out) return PER_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -29,6 +29,14 @@ struct SampleParams {
     const float* __restrict__ u01;
     int32_t* __restrict__ out;
     int* status;
+    // fused importance-sampling weights (per_sample_weighted)
+    const float* __restrict__ prio;
+    float alpha;
+    bool alpha_one;
+    float beta;
+    float* __restrict__ out_w;
+    float* slots;                // [gridDim.x] per-CTA minima
+    unsigned long long* ticket;  // grid-barrier ticket
 };
 
 __device__ __forceinline__ float draw_u(const SampleParams& P, int k) {
@@ -154,6 +162,20 @@ __global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
 
 constexpr int kCoarseCap = 4096;  // coarse entries staged per CTA (16 KB)
 
+// Minimum over the CTA of one value per thread (result on every thread).
+template <int THREADS>
+__device__ __forceinline__ float block_min(float m, float* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(PER_FULL_MASK, m, o));
+    __syncthreads();  // s_red may still be read from a previous use
+    if (lane == 0) s_red[warp] = m;
+    __syncthreads();
+    float b = s_red[0];
+    for (int w = 1; w < THREADS / 32; ++w) b = fminf(b, s_red[w]);
+    return b;
+}
+
 __device__ __forceinline__ int smem_lower_bound(const float* a, int lo, int hi, float u) {
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
@@ -163,7 +185,7 @@ __device__ __forceinline__ int smem_lower_bound(const float* a, int lo, int hi, 
     return lo;
 }
 
-template <int THREADS, int SPT>
+template <int THREADS, int SPT, bool WEIGHTS>
 __global__ void __launch_bounds__(THREADS) sample_coarse_kernel(SampleParams P) {
     extern __shared__ __align__(128) float s_dyn[];  // kCoarseCap coarse entries, then the window
     float* s_coarse = s_dyn;
@@ -246,23 +268,71 @@ __global__ void __launch_bounds__(THREADS) sample_coarse_kernel(SampleParams P) 
         const int k = k0 + threadIdx.x + s * THREADS;
         if (k < kend) P.out[k] = res[s];
     }
+    if (WEIGHTS) {
+        // the IS weights of the batch, exactly as per_is_weights computes
+        // them: pa = powf(p, alpha) of every sample, the batch minimum
+        // across CTAs (slots + one grid barrier), w = (pa_min / pa)^beta
+        __shared__ float s_red[THREADS / 32];
+        float pa[SPT];
+        float m = __int_as_float(0x7f800000);  // +inf
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            const int k = k0 + threadIdx.x + s * THREADS;
+            pa[s] = k < kend ? pow_accurate(__ldg(P.prio + res[s]), P.alpha, P.alpha_one) : m;
+            m = fminf(m, pa[s]);
+        }
+        m = block_min<THREADS>(m, s_red);
+        if (threadIdx.x == 0) P.slots[blockIdx.x] = m;
+        grid_barrier(P.ticket, P.status, ST_TIMEOUT);
+        float g = __int_as_float(0x7f800000);
+        for (int j = threadIdx.x; j < static_cast<int>(gridDim.x); j += THREADS) g = fminf(g, __ldcg(P.slots + j));
+        const float pa_min = block_min<THREADS>(g, s_red);
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            const int k = k0 + threadIdx.x + s * THREADS;
+            if (k < kend) P.out_w[k] = powf(__fdiv_rn(pa_min, pa[s]), P.beta);
+        }
+    }
 }
 
-template <int THREADS, int SPT>
+template <int THREADS, int SPT, bool WEIGHTS>
 per_status launch_coarse_cfg(const SampleParams& P, cudaStream_t s) {
     const int per_cta = THREADS * SPT;
     const unsigned grid = static_cast<unsigned>((P.B + per_cta - 1) / per_cta);
     const int smem = (kCoarseCap + kWindowCap) * static_cast<int>(sizeof(float));
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(sample_coarse_kernel<THREADS, SPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        if (cudaFuncSetAttribute(sample_coarse_kernel<THREADS, SPT, WEIGHTS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_coarse_kernel<THREADS, SPT, WEIGHTS>,
+                                                          THREADS, smem) != cudaSuccess)
             return PER_ERR_CUDA;
-        configured = true;
+        if (per_sm < 1) per_sm = 1;
     }
-    sample_coarse_kernel<THREADS, SPT><<<grid, THREADS, smem, s>>>(P);
+    if (!WEIGHTS) {
+        sample_coarse_kernel<THREADS, SPT, WEIGHTS><<<grid, THREADS, smem, s>>>(P);
+        per_note_launch();
+        return cuda_status(cudaGetLastError());
+    }
+    // the grid barrier needs every CTA resident at once: cooperative launch
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        return PER_ERR_CUDA;
+    if (static_cast<int64_t>(grid) > static_cast<int64_t>(per_sm) * sms) return PER_ERR_STATE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, sample_coarse_kernel<THREADS, SPT, WEIGHTS>, P);
     per_note_launch();
-    return cuda_status(cudaGetLastError());
+    return cuda_status(e);
 }
 
 template <int THREADS, int SPT>
@@ -288,9 +358,28 @@ per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
 // Samples per CTA: aim the expected window (n/B items per sample, uniform
 // case) at ~2/3 of the staging buffer, and keep at least ~2 CTAs per SM busy
 // when B is small.
-per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
-                              int32_t* out, cudaStream_t s) {
-    SampleParams P;
+namespace {
+
+// The coarse-index path with or without fused weights; PER_ERR_STATE when it
+// does not apply.
+template <bool WEIGHTS>
+per_status launch_coarse(const SampleParams& P, double ratio, cudaStream_t s) {
+    // latency first: as many samples per CTA as keep the expected window
+    // within ~2/3 of the staging buffer
+    int per_cta = 1024;
+    while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
+    switch (per_cta) {
+        case 1024: return launch_coarse_cfg<256, 4, WEIGHTS>(P, s);
+        case 512: return launch_coarse_cfg<256, 2, WEIGHTS>(P, s);
+        case 256: return launch_coarse_cfg<256, 1, WEIGHTS>(P, s);
+        case 128: return launch_coarse_cfg<128, 1, WEIGHTS>(P, s);
+        case 64: return launch_coarse_cfg<64, 1, WEIGHTS>(P, s);
+        default: return launch_coarse_cfg<32, 1, WEIGHTS>(P, s);
+    }
+}
+
+SampleParams sample_params(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01, int32_t* out) {
+    SampleParams P = {};
     P.cdf = ctx->cdf;
     P.n = static_cast<int>(ctx->size);
     P.B = B;
@@ -300,21 +389,23 @@ per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
     P.out = out;
     P.status = ctx->status;
     P.coarse = ctx->coarse;
+    return P;
+}
+
+bool coarse_fits(const per_ctx* ctx) {
+    return ctx->coarse && (ctx->size + kCoarseStride - 1) / kCoarseStride <= kCoarseCap;
+}
+
+}  // namespace
+
+// Samples per CTA: aim the expected window (n/B items per sample, uniform
+// case) at ~2/3 of the staging buffer, and keep at least ~2 CTAs per SM busy
+// when B is small.
+per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+                              int32_t* out, cudaStream_t s) {
+    SampleParams P = sample_params(ctx, B, seed, offset, u01, out);
     const double ratio = static_cast<double>(P.n) / static_cast<double>(B);
-    if (ctx->coarse && (P.n + kCoarseStride - 1) / kCoarseStride <= kCoarseCap) {
-        // latency first: as many samples per CTA as keep the expected window
-        // within ~2/3 of the staging buffer
-        int per_cta = 1024;
-        while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
-        switch (per_cta) {
-            case 1024: return launch_coarse_cfg<256, 4>(P, s);
-            case 512: return launch_coarse_cfg<256, 2>(P, s);
-            case 256: return launch_coarse_cfg<256, 1>(P, s);
-            case 128: return launch_coarse_cfg<128, 1>(P, s);
-            case 64: return launch_coarse_cfg<64, 1>(P, s);
-            default: return launch_coarse_cfg<32, 1>(P, s);
-        }
-    }
+    if (coarse_fits(ctx)) return launch_coarse<false>(P, ratio, s);
     int per_cta = 1024;
     while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
     while (per_cta > 32 && (B + per_cta - 1) / per_cta < 2 * ctx->num_sms) per_cta >>= 1;
@@ -326,4 +417,24 @@ per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
         case 64: return launch_cfg<64, 1>(P, s);
         default: return launch_cfg<32, 1>(P, s);
     }
+}
+
+// Sampling with the IS weights fused into the same launch (scan path with the
+// coarse index); PER_ERR_STATE when the fused path does not apply.
+per_status launch_sample_scan_weighted(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+                                       float beta, int32_t* out, float* out_w, cudaStream_t s) {
+    if (!coarse_fits(ctx)) return PER_ERR_STATE;
+    SampleParams P = sample_params(ctx, B, seed, offset, u01, out);
+    P.prio = ctx->prio;
+    P.alpha = ctx->alpha;
+    P.alpha_one = ctx->alpha == 1.0f;
+    P.beta = beta;
+    P.out_w = out_w;
+    P.slots = ctx->slots;
+    P.ticket = ctx->tickets + TK_SAMPLE;
+    const double ratio = static_cast<double>(P.n) / static_cast<double>(B);
+    int per_cta = 1024;
+    while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
+    if ((B + per_cta - 1) / per_cta > ctx->slot_n) return PER_ERR_STATE;
+    return launch_coarse<true>(P, ratio, s);
 }

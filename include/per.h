@@ -187,6 +187,18 @@ per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, i
 per_status per_is_weights(per_ctx* ctx, const int32_t* d_idx, int32_t B, float beta,
                           float* d_out_w, void* stream);
 
+/*
+ * per_sample_weighted -- per_sample followed by per_is_weights on the drawn
+ * indices, in one call: the same arguments, checks and results as the two
+ * calls, bit for bit.  On the scan path, when the CDF's coarse index fits a
+ * CTA's shared memory (size <= 262,144 items), both run in one cooperative
+ * launch (sampling, then the batch minimum across CTAs through one grid
+ * barrier, then the weights); otherwise the two launches run in order.
+ */
+per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, int mode,
+                               const float* d_u01, float beta, int32_t* d_out_idx, float* d_out_w,
+                               void* stream);
+
 /* per_total -- total priority (foxhunt "Integration" / total_priority):
  * mode PER_TREE reads tree[1], PER_SCAN reads cdf[n-1] (after per_build_cdf).
  * per_total writes one float to device memory; per_total_host synchronises

@@ -39,8 +39,8 @@ def new_ctx(p, alpha, flags, capacity=None):
 
 @pytest.mark.parametrize("n_upd", [1, 7, 8192, 8193, 50000])
 def test_scan_update_last_writer_wins(n_upd):
-    """Scan-only contexts: one-CTA path up to 8192 updates, cooperative beyond;
-    unsorted indices with duplicates."""
+    """Scan-only contexts (one cooperative launch: last-writer election, grid
+    barrier, apply); unsorted indices with duplicates."""
     N = 262144
     g = workloads.rng(200, n_upd)
     p0 = workloads.abs_normal(N, g)
@@ -62,8 +62,9 @@ def test_scan_update_last_writer_wins(n_upd):
 # ------------------------------------------------------- minibatch loop -----
 
 def test_minibatch_loop_matches_oracle():
-    """The bench step itself: N=262144, 32 rounds of build_cdf, sample 8192,
-    IS weights (beta 0.4), update 8192 at the sampled indices."""
+    """The bench step itself: N=262144, 32 rounds of build_cdf, sample 8192
+    with IS weights (beta 0.4, per_sample_weighted), update 8192 at the
+    sampled indices."""
     W = workloads.MINIBATCH
     N, B, R, alpha, beta, seed = W["N"], W["B"], W["rounds"], W["alpha"], W["beta"], W["seed"]
     p = workloads.minibatch_priorities()
@@ -72,8 +73,7 @@ def test_minibatch_loop_matches_oracle():
     w = torch.empty(B, dtype=torch.float32, device="cuda")
     for r in range(R):
         per.per_build_cdf(ctx.handle)
-        per.per_sample(ctx.handle, B, seed, r * B, SCAN, idx)
-        per.per_is_weights(ctx.handle, idx, beta, w)
+        per.per_sample_weighted(ctx.handle, B, seed, r * B, SCAN, beta, idx, w)
         newp = workloads.minibatch_new_priorities(r)
         per.per_update(ctx.handle, idx, dev(newp))
         c = host(per.read_cdf(ctx.handle))[:N]
@@ -210,4 +210,32 @@ def test_tree_workload_steps():
             d = np.abs(leaves.view(np.int32).astype(np.int64) - want_leaves.view(np.int32).astype(np.int64))
             assert d.max() <= 4, f"step {s}: leaves differ from pow beyond 4 ulp"
             assert np.array_equal(tree[1:], oracle.tree_build(leaves)[1:]), f"step {s}"
+    assert per.per_check(ctx.handle) == 0
+
+
+# ------------------------------------------------ fused sample + weights ----
+
+@pytest.mark.parametrize("N,B,flags", [(262144, 8192, SCAN), (1000, 37, SCAN), (262144, 1, SCAN),
+                                       (1 << 20, 65536, SCAN), (262144, 8192, SCAN | TREE)])
+def test_sample_weighted_equals_the_two_calls(N, B, flags):
+    """per_sample_weighted gives per_sample + per_is_weights bit for bit (one
+    cooperative launch on the scan path when the coarse index fits, else the
+    two launches)."""
+    p = workloads.heavy_priorities(N=N)
+    ctx = new_ctx(p, 0.7, flags)
+    per.per_build_cdf(ctx.handle)
+    i1 = torch.empty(B, dtype=torch.int32, device="cuda")
+    w1 = torch.empty(B, dtype=torch.float32, device="cuda")
+    i2 = torch.empty(B, dtype=torch.int32, device="cuda")
+    w2 = torch.empty(B, dtype=torch.float32, device="cuda")
+    for beta in (0.4, 1.0):
+        per.per_sample(ctx.handle, B, 9, 77, SCAN, i1)
+        per.per_is_weights(ctx.handle, i1, beta, w1)
+        per.per_sample_weighted(ctx.handle, B, 9, 77, SCAN, beta, i2, w2)
+        assert np.array_equal(host(i1), host(i2))
+        assert np.array_equal(host(w1), host(w2))
+        got = host(w2)
+        assert got.max() == 1.0
+        want = oracle.is_weights(p, N, 0.7, host(i2), beta)
+        assert np.max(np.abs(got / want - 1.0)) <= 1e-6
     assert per.per_check(ctx.handle) == 0
