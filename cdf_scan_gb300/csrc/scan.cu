@@ -195,13 +195,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 }
 
 // Barrier among the compute warps only (the lookback warp never joins it).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+template <int N>
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory"); }
 
 // Persistent, warp-specialised scan over a co-resident grid of G CTAs (the
 // launch is cooperative, so all of them run at once).  CTA c scans tiles
 // c, c + G, c + 2G, ... (round k = its k-th tile), so the CTAs sweep the array
-// one round at a time.  Each CTA runs kThreads compute threads (kWarps warps)
-// plus one lookback warp:
+// one round at a time.  Each CTA runs WARPS compute warps plus one lookback
+// warp:
 //   * compute warps: wait for the stage's bulk copy, apply p^alpha, scan the
 //     tile locally, park the tile-local values in the stage buffer, publish
 //     the tile aggregate and signal `parked`; two tiles behind, wait for that
@@ -211,11 +212,12 @@ __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" 
 //     the lookback, publish the tile's inclusive prefix, signal `carried`.
 // A lookback waits only on tiles of earlier rounds or earlier tiles of the
 // same round, so the scan always makes progress.
-template <int ITEMS, int STAGES>
-__global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams P) {
-    static_assert(STAGES == 4, "one stage scanning, two awaiting their carry, one loading");
+template <int ITEMS, int STAGES, int WARPS, int MINB>
+__global__ void __launch_bounds__(WARPS * 32 + 32, MINB) build_cdf_kernel(ScanParams P) {
+    static_assert(STAGES >= 4, "one stage scanning, two awaiting their carry, at least one loading");
+    constexpr int THREADS = WARPS * 32;
     constexpr int LAG = 2;
-    constexpr int TILE = kThreads * ITEMS;
+    constexpr int TILE = THREADS * ITEMS;
     constexpr int LANE_ITEMS = 8;             // consecutive items per lane per sub-chunk
     constexpr int SUB = ITEMS / LANE_ITEMS;   // sub-chunks per warp
     constexpr int WCHUNK = 32 * ITEMS;        // items per warp
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
     __shared__ __align__(8) uint64_t s_full[STAGES], s_parked[STAGES], s_carried[STAGES];
     __shared__ float s_agg[STAGES];
     __shared__ float s_carry[STAGES][4];
-    __shared__ float s_wtot[2][kWarps];
+    __shared__ float s_wtot[2][WARPS];
     __shared__ unsigned s_epoch;
 
     const int lane = threadIdx.x & 31;
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
     const unsigned epoch = s_epoch;
     const unsigned tag_agg = 2u * epoch;
 
-    if (warp == kWarps) {
+    if (warp == WARPS) {
         // ======================= lookback warp ================================
         u128 run = 0;  // inclusive prefix of this CTA's previous tile
         for (int k = 0;; ++k) {
@@ -322,17 +324,27 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
                         for (int e = 0; e < 4; ++e)
                             if (i0 + e < valid) P.cdf[tile_base + i0 + e] = oo[e];
                     }
-                    if (P.coarse) {  // coarse[j] = cdf[min(64j + 63, n - 1)]
+                    // coarse[j] = cdf[min(64j + 63, n - 1)].  In a full tile the
+                    // entries are the items 64j + 63 (n - 1 is one of them when it
+                    // ends the tile): the last item of the second half of every
+                    // eighth lane.  A ragged tile checks each item.
+                    static_assert(LANE_ITEMS == 8 && kCoarseStride == 64, "coarse lane rule");
+                    if (P.coarse) {
+                        if (full) {
+                            if (h == 1 && (lane & 7) == 7)
+                                P.coarse[(tile_base + i0 + 3) / kCoarseStride] = oo[3];
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int64_t g = tile_base + i0 + e;
-                            if (g < P.n && ((g & (kCoarseStride - 1)) == kCoarseStride - 1 || g == P.n - 1))
-                                P.coarse[g / kCoarseStride] = oo[e];
+                            for (int e = 0; e < 4; ++e) {
+                                const int64_t g = tile_base + i0 + e;
+                                if (g < P.n && ((g & (kCoarseStride - 1)) == kCoarseStride - 1 || g == P.n - 1))
+                                    P.coarse[g / kCoarseStride] = oo[e];
+                            }
                         }
                     }
                 }
             }
-            compute_sync();  // the stage was read by everyone
+            compute_sync<THREADS>();  // the stage was read by everyone
             if (threadIdx.x == 0) {
                 const int64_t t2 = pt + STAGES * G;
                 if (t2 < P.num_tiles) load_tile<TILE>(P, static_cast<unsigned>(t2), s_buf + ps * TILE, &s_full[ps]);
@@ -418,7 +430,7 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
             }
             float* wtot = s_wtot[k & 1];
             if (lane == 0) wtot[warp] = carry;
-            compute_sync();
+            compute_sync<THREADS>();
             float off = 0.f;
             for (int w = 0; w < warp; ++w) off = off + wtot[w];
 #pragma unroll
@@ -433,7 +445,7 @@ __global__ void __launch_bounds__(kThreads + 32, 3) build_cdf_kernel(ScanParams 
             }
             if (threadIdx.x == 0) {
                 float agg = 0.f;
-                for (int w = 0; w < kWarps; ++w) agg = agg + wtot[w];
+                for (int w = 0; w < WARPS; ++w) agg = agg + wtot[w];
                 s_agg[st] = agg;
                 *reinterpret_cast<volatile unsigned long long*>(S.aggw + t) =
                     (static_cast<unsigned long long>(tag_agg) << 32) | __float_as_uint(agg);
@@ -566,11 +578,18 @@ __global__ void __launch_bounds__(THREADS) build_cdf_wave_kernel(ScanParams P) {
             if (base + i0 + e < P.n) P.cdf[base + i0 + e] = o[e];
     }
     if (P.coarse) {  // coarse[j] = cdf[min(64j + 63, n - 1)]
+        static_assert(ITEMS == 8 && kCoarseStride == 64, "coarse lane rule assumes 8 items per lane");
+        if (base + i0 + ITEMS < P.n) {
+            // n - 1 lies beyond this lane, so its entries are the items 64j + 63:
+            // only the last item of every eighth lane can be one
+            if ((lane & 7) == 7) P.coarse[(base + i0 + ITEMS - 1) / kCoarseStride] = o[ITEMS - 1];
+        } else {
 #pragma unroll
-        for (int e = 0; e < ITEMS; ++e) {
-            const int64_t g = base + i0 + e;
-            if (g < P.n && ((g & (kCoarseStride - 1)) == kCoarseStride - 1 || g == P.n - 1))
-                P.coarse[g / kCoarseStride] = o[e];
+            for (int e = 0; e < ITEMS; ++e) {
+                const int64_t g = base + i0 + e;
+                if (g < P.n && ((g & (kCoarseStride - 1)) == kCoarseStride - 1 || g == P.n - 1))
+                    P.coarse[g / kCoarseStride] = o[e];
+            }
         }
     }
 
@@ -619,17 +638,17 @@ per_status launch_scan_wave(ScanParams P, int num_sms, cudaStream_t s) {
 
 // Launch: a persistent grid of as many CTAs as can be resident at once
 // (never more CTAs than tiles).
-template <int ITEMS, int STAGES>
+template <int ITEMS, int STAGES, int WARPS, int MINB>
 per_status launch_scan(ScanParams P, int num_sms, cudaStream_t s) {
     static_assert(ITEMS % 8 == 0, "8 consecutive items per lane per sub-chunk");
-    constexpr int TILE = kThreads * ITEMS;
+    constexpr int TILE = WARPS * 32 * ITEMS;
     const size_t smem = static_cast<size_t>(STAGES) * TILE * sizeof(float);
     static int per_sm = 0;
     if (per_sm == 0) {
-        if (cudaFuncSetAttribute(build_cdf_kernel<ITEMS, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(build_cdf_kernel<ITEMS, STAGES, WARPS, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_kernel<ITEMS, STAGES>,
-                                                          kThreads + 32, smem) != cudaSuccess)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_kernel<ITEMS, STAGES, WARPS, MINB>,
+                                                          WARPS * 32 + 32, smem) != cudaSuccess)
             return PER_ERR_CUDA;
         if (per_sm < 1) per_sm = 1;
     }
@@ -642,7 +661,7 @@ per_status launch_scan(ScanParams P, int num_sms, cudaStream_t s) {
     // stride relies on it)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads + 32);
+    cfg.blockDim = dim3(WARPS * 32 + 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -650,7 +669,7 @@ per_status launch_scan(ScanParams P, int num_sms, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_kernel<ITEMS, STAGES>, P);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_kernel<ITEMS, STAGES, WARPS, MINB>, P);
     per_note_launch();
     return cuda_status(e);
 }
@@ -669,8 +688,8 @@ per_status scan_dispatch(ScanParams P, int num_sms, cudaStream_t s) {
         if (st != PER_ERR_STATE) return st;
     }
     const int64_t big_tiles = (P.n + 4095) / 4096;
-    if (big_tiles >= 2 * static_cast<int64_t>(num_sms)) return launch_scan<16, 4>(P, num_sms, s);
-    return launch_scan<8, 4>(P, num_sms, s);
+    if (big_tiles >= 2 * static_cast<int64_t>(num_sms)) return launch_scan<16, 4, 8, 3>(P, num_sms, s);
+    return launch_scan<8, 4, 8, 3>(P, num_sms, s);
 }
 
 }  // namespace
