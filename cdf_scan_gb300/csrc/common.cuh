@@ -229,6 +229,21 @@ __device__ __forceinline__ float hw_ex2(float x) {
     return y;
 }
 
+// Flush-to-zero forms: a subnormal input of lg2 reads as 0 (result -inf) and
+// a subnormal result of ex2 becomes 0.  Callers keep both out of their
+// domain (pow_alpha_n below).
+__device__ __forceinline__ float hw_lg2_ftz(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float hw_ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Inputs that are not positive normal floats (zero, subnormal, infinite,
 // negative, NaN) take CUDA's powf; kept out of line so the fast path stays
 // small at every call site.  `bad` is set for negative and NaN inputs.
@@ -270,17 +285,20 @@ __device__ __forceinline__ float absmax_nan(float a, float b) {
     return d;
 }
 
-// v[e] <- v[e]^alpha in place (the scan's hot path).  For |log2 x| < 16, i.e.
-// x in (2^-16, 2^16), x^alpha = ex2(alpha * lg2(x)) directly: the hardware
-// lg2 (absolute error ~2^-22.6), the fp32 rounding of L = lg2(x) (<= 2^-21
-// for |L| < 16), the rounding of alpha*L (<= 2^-21) and the hardware ex2
-// (~2^-22.5 relative) bound the relative error by ~1e-6.  One range test
-// covers all N values; any other input -- tiny, huge, zero, subnormal,
-// infinite, negative, NaN (the NaN-propagating max fails the test) -- takes
-// pow_fast's exact exponent split, and negative or NaN inputs set `bad`.
-// mode: 0 = x^alpha, 1 = alpha == 1 (x), 2 = alpha == 0 (1).
+// v[e] <- v[e]^alpha in place (the scan's hot path).  For |log2 x| < lim,
+// x^alpha = ex2(alpha * lg2(x)) directly: the hardware lg2 (absolute error
+// ~2^-22.6), the fp32 rounding of L = lg2(x) (<= 2^-21 for |L| < 16), the
+// rounding of alpha*L (<= 2^-21) and the hardware ex2 (~2^-22.5 relative)
+// bound the relative error by ~1e-6.  `lim` = min(16, 120/alpha) (pow_limit)
+// keeps x and the result normal floats, so the flush-to-zero forms of lg2
+// and ex2 are exact stand-ins for the full ones there.  One range test covers
+// all N values; any other input -- tiny, huge, zero, subnormal (lg2 reads it
+// as 0), infinite, negative, NaN (the NaN-propagating max fails the test) --
+// takes pow_fast's exact exponent split, and negative or NaN inputs set
+// `bad`.  mode: 0 = x^alpha, 1 = alpha == 1 (x), 2 = alpha == 0 (1).
 template <int N, class Fetch>
-__device__ __forceinline__ void pow_alpha_n(float (&v)[N], float alpha, int mode, bool& bad, Fetch fetch) {
+__device__ __forceinline__ void pow_alpha_n(float (&v)[N], float alpha, float lim, int mode, bool& bad,
+                                            Fetch fetch) {
     if (mode != 0) {
         bool ok = true;
 #pragma unroll
@@ -294,29 +312,101 @@ __device__ __forceinline__ void pow_alpha_n(float (&v)[N], float alpha, int mode
     }
     // v <- lg2(v) in place; the rare slow path re-reads the inputs via fetch(e)
 #pragma unroll
-    for (int e = 0; e < N; ++e) v[e] = hw_lg2(v[e]);
+    for (int e = 0; e < N; ++e) v[e] = hw_lg2_ftz(v[e]);
     float m = 0.f;
 #pragma unroll
     for (int e = 0; e < N; ++e) m = absmax_nan(v[e], m);
-    if (m < 16.f) {
+    if (m < lim) {
 #pragma unroll
-        for (int e = 0; e < N; ++e) v[e] = hw_ex2(__fmul_rn(alpha, v[e]));
+        for (int e = 0; e < N; ++e) v[e] = hw_ex2_ftz(__fmul_rn(alpha, v[e]));
         return;
     }
 #pragma unroll
     for (int e = 0; e < N; ++e) {
         const float x = fetch(e);
         if (!(x >= 0.f)) bad = true;
-        v[e] = fabsf(v[e]) < 16.f ? hw_ex2(__fmul_rn(alpha, v[e])) : pow_split(x, alpha);
+        v[e] = fabsf(v[e]) < lim ? hw_ex2_ftz(__fmul_rn(alpha, v[e])) : pow_split(x, alpha);
     }
 }
 
-// Four values at once (same rule as pow_alpha_n).
-__device__ __forceinline__ float4 pow4_alpha(float4 q, float alpha, int mode, bool& bad) {
-    const float x[4] = {q.x, q.y, q.z, q.w};
-    float v[4] = {q.x, q.y, q.z, q.w};
-    pow_alpha_n<4>(v, alpha, mode, bad, [&](int e) { return x[e]; });
-    return make_float4(v[0], v[1], v[2], v[3]);
+// Range bound of pow_alpha_n's direct path for exponent alpha > 0: with
+// |lg2 x| < lim, |alpha * lg2 x| < 120, so x^alpha stays a normal float.
+inline __host__ __device__ float pow_limit(float alpha) {
+    return alpha > 7.5f ? 120.f / alpha : 16.f;
+}
+
+// ---- packed fp32 pairs (sm_100+ f32x2 arithmetic; per-lane IEEE rounding,
+// the same results as two scalar operations) ---------------------------------
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// v[e] <- k + v[e] for an even count of values
+template <int N>
+__device__ __forceinline__ void add_each(float k, float* v) {
+    const unsigned long long k2 = f2_pack(k, k);
+#pragma unroll
+    for (int e = 0; e < N; e += 2) f2_unpack(f2_add(k2, f2_pack(v[e], v[e + 1])), v[e], v[e + 1]);
+}
+
+// max / min of three (max propagates NaN)
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// pow_alpha_n's rule (mode 0) for the N values a lane holds, with one range
+// test for the whole warp: when every lane's lg2 values lie in (-lim, lim)
+// the direct path runs without a divergent branch; otherwise each value
+// takes pow_alpha_n's per-value decision (fetch(e) re-reads input e).  All
+// 32 lanes must call it together.  N even.
+template <int N, class Fetch>
+__device__ __forceinline__ void pow_alpha_warp(float (&v)[N], float alpha, float lim, bool& bad, Fetch fetch) {
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = hw_lg2_ftz(v[e]);
+    float mx = max3_nan(v[0], v[1], v[1]), mn = min3(v[0], v[1], v[1]);
+#pragma unroll
+    for (int e = 2; e + 1 < N; e += 2) {
+        mx = max3_nan(mx, v[e], v[e + 1]);
+        mn = min3(mn, v[e], v[e + 1]);
+    }
+    if (__all_sync(PER_FULL_MASK, mx < lim && mn > -lim)) {
+        const unsigned long long a2 = f2_pack(alpha, alpha);
+#pragma unroll
+        for (int e = 0; e < N; e += 2) {
+            float p0, p1;
+            f2_unpack(f2_mul(a2, f2_pack(v[e], v[e + 1])), p0, p1);
+            v[e] = hw_ex2_ftz(p0);
+            v[e + 1] = hw_ex2_ftz(p1);
+        }
+        return;
+    }
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+        const float x = fetch(e);
+        if (!(x >= 0.f)) bad = true;
+        v[e] = fabsf(v[e]) < lim ? hw_ex2_ftz(__fmul_rn(alpha, v[e])) : pow_split(x, alpha);
+    }
 }
 
 // p^alpha; alpha == 1 skips the power (exact).  `bad` is set for negative

@@ -51,13 +51,19 @@ struct per_ctx {
     unsigned long long* tickets;      // [NUM_TICKETS] grid-barrier tickets
     float* slots;                     // [slot_n] per-CTA partial results
     int slot_n;
+    unsigned long long* scan_xsum;    // [kScanXsumWords] chunk sums of the two-pass scan
 };
 
 // Grid-barrier ticket words (per_ctx::tickets).
-enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, NUM_TICKETS = 4 };
+enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_SCAN = 3, NUM_TICKETS = 4 };
 
 // Items per entry of the coarse CDF index: coarse[j] = cdf[min(64j+63, n-1)].
 constexpr int kCoarseStride = 64;
+
+// Exchange words of the two-pass scan: 2 parities x kScanMaxGrid CTAs x one
+// 128-bit exact sum, 2 parities x a 128-bit total, a ready word, padding.
+constexpr int kScanMaxGrid = 1024;
+constexpr int64_t kScanXsumWords = 4 * kScanMaxGrid + 8;
 
 // 64-bit words of scan state for up to `tiles` tiles: one tagged aggregate
 // word per tile.

@@ -37,6 +37,7 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->coarse);
     cudaFree(c->tickets);
     cudaFree(c->slots);
+    cudaFree(c->scan_xsum);
     std::free(c);
 }
 
@@ -96,7 +97,8 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     if (ok && (flags & PER_SCAN))
         ok = alloc_zero(&c->cdf, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
-             alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess;
+             alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
+             alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok) {
         // epochs start at 1 (0 marks "never written"); the IS-weight minimum
