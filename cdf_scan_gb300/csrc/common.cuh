@@ -131,33 +131,40 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     }
 }
 
-// Barrier across a co-resident grid (cooperative launch).  `ticket` only
-// grows: each use adds gridDim.x, so the arrivals of one barrier hold the
-// tickets [g*G, (g+1)*G) and every CTA waits for the end of its own group.
-// The wait is bounded (kWaitLimitNs; ST_TIMEOUT).  Writes before the barrier
-// are visible to every CTA after it (fence + acquire).  On timeout it sets
-// `timeout_bit` in *status and returns false (the same on every thread of the
-// CTA).
+// Barrier across a co-resident grid (cooperative launch).  `ticket` holds
+// (generation << 32) | arrivals.  Each CTA adds one arrival; the CTA whose
+// arrival completes the grid moves the word to (generation + 1, 0) with one
+// more atomic, and the others wait for the generation to change.  The count
+// is back at 0 after every barrier, so launches of any grid size can share
+// the word.  The wait is bounded (kWaitLimitNs; ST_TIMEOUT).  Writes before
+// the barrier are visible to every CTA after it (fence + acquire).  On
+// timeout it sets `timeout_bit` in *status and returns false (the same on
+// every thread of the CTA); the word is then left mid-barrier and must be
+// cleared before the next launch (per_check does).
 __device__ __forceinline__ bool grid_barrier(unsigned long long* ticket, int* status, int timeout_bit) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         const unsigned long long G = gridDim.x;
-        const unsigned long long t = atomicAdd(ticket, 1ull);
-        const unsigned long long target = (t / G + 1ull) * G;
+        const unsigned long long old = atomicAdd(ticket, 1ull);
         int ok = 1;
-        uint64_t t0 = 0;
-        while (ld_acquire_u64(ticket) < target) {
-            const uint64_t now = global_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
-                atomicOr(status, timeout_bit);
-                ok = 0;
-                break;
+        if ((old & 0xffffffffull) == G - 1ull) {
+            atomicAdd(ticket, (1ull << 32) - G);  // arrivals G -> 0, generation + 1
+        } else {
+            const unsigned gen = static_cast<unsigned>(old >> 32);
+            uint64_t t0 = 0;
+            while (static_cast<unsigned>(ld_acquire_u64(ticket) >> 32) == gen) {
+                const uint64_t now = global_ns();
+                if (t0 == 0) {
+                    t0 = now;
+                } else if (now - t0 > kWaitLimitNs) {
+                    atomicOr(status, timeout_bit);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
             }
-            __nanosleep(64);
         }
         __threadfence();
         s_ok = ok;

@@ -239,3 +239,36 @@ def test_sample_weighted_equals_the_two_calls(N, B, flags):
         want = oracle.is_weights(p, N, 0.7, host(i2), beta)
         assert np.max(np.abs(got / want - 1.0)) <= 1e-6
     assert per.per_check(ctx.handle) == 0
+
+
+# ------------------------------------------- grid barriers across grid sizes ---
+
+def test_grid_barriers_across_varying_batch_sizes():
+    """One context, batches whose grid sizes change from call to call: the
+    grid-barrier word is shared by launches of different grid sizes and must
+    come back ready after each (no timeout, results still exact)."""
+    N = 262144
+    g = workloads.rng(404, N)
+    p = workloads.abs_normal(N, g)
+    ctx = new_ctx(p, 0.6, SCAN)
+    for n_upd in (8192, 1000, 8192, 300, 50000, 8193):
+        idx = g.integers(0, N, size=n_upd).astype(np.int32)
+        newp = workloads.abs_normal(n_upd, g)
+        per.per_update(ctx.handle, dev(idx), dev(newp))
+        p = oracle.apply_updates(p, idx, newp)
+        assert per.per_check(ctx.handle) == 0, f"update n={n_upd}"
+        assert np.array_equal(host(per.read_priorities(ctx.handle, N)), p)
+    per.per_build_cdf(ctx.handle)
+    c = host(per.read_cdf(ctx.handle))[:N]
+    for B in (8192, 1000, 8192, 37, 65536, 8192):
+        i1 = torch.empty(B, dtype=torch.int32, device="cuda")
+        w1 = torch.empty(B, dtype=torch.float32, device="cuda")
+        w2 = torch.empty(B, dtype=torch.float32, device="cuda")
+        per.per_sample_weighted(ctx.handle, B, 5, B, SCAN, 0.4, i1, w1)
+        assert per.per_check(ctx.handle) == 0, f"sample_weighted B={B}"
+        per.per_is_weights(ctx.handle, i1, 0.4, w2)
+        assert per.per_check(ctx.handle) == 0, f"is_weights B={B}"
+        want, _ = oracle.sample_cdf_f32(c, B, 5, B)
+        assert np.array_equal(host(i1), want)
+        assert np.array_equal(host(w1), host(w2))
+        assert np.max(np.abs(host(w2) / oracle.is_weights(p, N, 0.6, want, 0.4) - 1.0)) <= 1e-6
