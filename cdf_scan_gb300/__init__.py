@@ -42,6 +42,7 @@ SIGNATURES = {
     "per_sample": (ctypes.c_int, [_vp, _i32, _u64, _u64, ctypes.c_int, _vp, _vp, _vp]),
     "per_is_weights": (ctypes.c_int, [_vp, _vp, _i32, _f32, _vp, _vp]),
     "per_sample_weighted": (ctypes.c_int, [_vp, _i32, _u64, _u64, ctypes.c_int, _vp, _f32, _vp, _vp, _vp]),
+    "per_step": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _u64, _u64, ctypes.c_int, _vp, _f32, _vp, _vp, _vp]),
     "per_total": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp]),
     "per_total_host": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(_f32), _vp]),
     "per_priorities_ptr": (_vp, [_vp]),
@@ -184,6 +185,17 @@ def per_sample_weighted(ctx: int, B: int, seed: int, offset: int, mode: int, bet
     _check("per_sample_weighted", lib().per_sample_weighted(
         ctx, B, seed, offset, mode, _ptr(u01, torch.float32, "u01", B), beta,
         _ptr(out_idx, torch.int32, "out_idx", B), _ptr(out_w, torch.float32, "out_w", B), _stream(stream)))
+    return out_idx
+
+
+def per_step(ctx: int, upd_idx: torch.Tensor | None, upd_prio: torch.Tensor | None, B: int, seed: int,
+             offset: int, mode: int, beta: float, out_idx: torch.Tensor, out_w: torch.Tensor,
+             u01: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    n = 0 if upd_idx is None else upd_idx.numel()
+    _check("per_step", lib().per_step(
+        ctx, _ptr(upd_idx, torch.int32, "upd_idx"), _ptr(upd_prio, torch.float32, "upd_prio", n), n, B, seed,
+        offset, mode, _ptr(u01, torch.float32, "u01", B), beta, _ptr(out_idx, torch.int32, "out_idx", B),
+        _ptr(out_w, torch.float32, "out_w", B), _stream(stream)))
     return out_idx
 
 

@@ -51,11 +51,13 @@ struct per_ctx {
     unsigned long long* tickets;      // [NUM_TICKETS] grid-barrier tickets
     float* slots;                     // [slot_n] per-CTA partial results
     int slot_n;
+    unsigned* step_min;               // [3] per_step: call counter, then the batch minimum of p^alpha
+                                      // (float bits) of even and odd calls
     unsigned long long* scan_xsum;    // [kScanXsumWords] chunk sums of the two-pass scan
 };
 
 // Grid-barrier ticket words (per_ctx::tickets).
-enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_SCAN = 3, NUM_TICKETS = 4 };
+enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_SCAN = 3, TK_STEP = 4, NUM_TICKETS = 8 };
 
 // Items per entry of the coarse CDF index: coarse[j] = cdf[min(64j+63, n-1)].
 constexpr int kCoarseStride = 64;
@@ -66,8 +68,13 @@ constexpr int kScanMaxGrid = 1024;
 constexpr int64_t kScanXsumWords = 4 * kScanMaxGrid + 8;
 
 // 64-bit words of scan state for up to `tiles` tiles: one tagged aggregate
-// word per tile.
-inline int64_t scan_state_words(int64_t tiles) { return tiles + 1; }
+// word per tile, each alone in a 128-byte line (kDescStride words apart) so
+// that the lookbacks of a whole wave of CTAs polling them spread over L2
+// instead of queueing on a few lines.  Only the one-wave kernels use them,
+// so at most kMaxWaveTiles tiles.
+constexpr int kDescStride = 16;
+constexpr int64_t kMaxWaveTiles = 1024;
+inline int64_t scan_state_words(int64_t tiles) { return tiles * kDescStride + 1; }
 
 // Host-side launch accounting (per_launch_count).
 void per_note_launch(int n = 1);
@@ -83,6 +90,8 @@ per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta
 // PER_ERR_STATE (nothing launched) when the fused path does not apply.
 per_status launch_sample_scan_weighted(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
                                        float beta, int32_t* out, float* out_w, cudaStream_t s);
+per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p, int n_upd, int B, uint64_t seed,
+                       uint64_t offset, const float* u01, float beta, int32_t* out, float* out_w, cudaStream_t s);
 per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n, cudaStream_t s);
 per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s);
 per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, uint64_t offset,

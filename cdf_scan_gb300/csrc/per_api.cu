@@ -1,5 +1,6 @@
 // per_api.cu -- the C ABI declared in include/per.h: context lifetime,
 // argument checking (before any launch) and dispatch to the kernels.
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -38,6 +39,7 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->tickets);
     cudaFree(c->slots);
     cudaFree(c->scan_xsum);
+    cudaFree(c->step_min);
     std::free(c);
 }
 
@@ -85,7 +87,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     c->size = 0;
     c->alpha = alpha;
     c->flags = flags;
-    c->scan_desc_tiles = (c->alloc_n + 1023) / 1024;
+    c->scan_desc_tiles = std::min<int64_t>((c->alloc_n + 1023) / 1024, kMaxWaveTiles);
     c->coarse_n = c->alloc_n / kCoarseStride + 1;
     c->slot_n = 16 * c->num_sms;
     bool ok = alloc_zero(&c->prio, c->alloc_n, s) == cudaSuccess &&
@@ -98,7 +100,8 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
         ok = alloc_zero(&c->cdf, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
              alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
-             alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess;
+             alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess &&
+             alloc_zero(&c->step_min, 3, s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok) {
         // epochs start at 1 (0 marks "never written"); the IS-weight minimum
@@ -107,7 +110,10 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
         init[CTR_SCAN_EPOCH] = 1u;
         init[CTR_UPD_EPOCH] = 1u;
         init[CTR_ISW_MIN] = 0xffffffffu;
+        const unsigned step_init[3] = {0u, 0x7f800000u, 0x7f800000u};  // call 0; +inf, +inf
         ok = cudaMemcpyAsync(c->ctrs, init, sizeof(init), cudaMemcpyHostToDevice, s) == cudaSuccess &&
+             (!c->step_min ||
+              cudaMemcpyAsync(c->step_min, step_init, sizeof(step_init), cudaMemcpyHostToDevice, s) == cudaSuccess) &&
              cudaStreamSynchronize(s) == cudaSuccess;
     }
     if (!ok) {
@@ -198,6 +204,27 @@ per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t 
     const per_status st = per_sample(ctx, B, seed, offset, mode, d_u01, d_out_idx, stream);
     if (st != PER_OK) return st;
     return per_is_weights(ctx, d_out_idx, B, beta, d_out_w, stream);
+}
+
+per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
+                    uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta, int32_t* d_out_idx,
+                    float* d_out_w, void* stream) {
+    if (!ctx || n_upd < 0 || (n_upd > 0 && (!d_upd_idx || !d_upd_prio))) return PER_ERR_ARG;
+    if (B < 1 || B > (1 << 24) || !d_out_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f) return PER_ERR_ARG;
+    if (mode != static_cast<int>(PER_SCAN) && mode != static_cast<int>(PER_TREE)) return PER_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mode == static_cast<int>(PER_SCAN) && ctx->flags == PER_SCAN && ctx->size >= 1) {
+        const per_status st =
+            launch_step(ctx, d_upd_idx, d_upd_prio, n_upd, B, seed, offset, d_u01, beta, d_out_idx, d_out_w, s);
+        if (st != PER_ERR_STATE) return st;
+    }
+    per_status st = per_update(ctx, d_upd_idx, d_upd_prio, n_upd, stream);
+    if (st != PER_OK) return st;
+    if (ctx->flags & PER_SCAN) {
+        st = per_build_cdf(ctx, stream);
+        if (st != PER_OK) return st;
+    }
+    return per_sample_weighted(ctx, B, seed, offset, mode, d_u01, beta, d_out_idx, d_out_w, stream);
 }
 
 per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream) {

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "update_core.cuh"
 
 namespace {
 
@@ -193,37 +194,19 @@ __global__ void apply_winners_kernel(const int32_t* __restrict__ idx, const floa
 }
 
 // Scan-only contexts: the last occurrence of every index wins, in one
-// cooperative launch.  (1) Every batch position k writes (epoch << 32 | k)
-// into winner[idx_k] with atomicMax, so the largest position of each index
-// survives; (2) after one grid barrier each position that won writes its
-// priority.  The epoch (read by every CTA before the barrier) is advanced by
-// CTA 0 after it, so winner slots never need clearing.
+// cooperative launch (update_core.cuh: elect, grid barrier, apply); CTA 0
+// advances the winner epoch after the barrier.
 __global__ void __launch_bounds__(256) update_scan_kernel(const int32_t* __restrict__ idx,
                                                           const float* __restrict__ p, int n, int64_t capacity,
                                                           unsigned long long* winner, float* __restrict__ prio,
                                                           unsigned* ctrs, unsigned long long* ticket, int* status) {
     const unsigned epoch = ld_relaxed_u32(ctrs + CTR_UPD_EPOCH);
-    const int stride = gridDim.x * blockDim.x;
+    const int first = blockIdx.x * blockDim.x + threadIdx.x, stride = gridDim.x * blockDim.x;
     bool bad = false;
-    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
-        const int32_t i = idx[k];
-        if (i < 0 || i >= capacity) {
-            bad = true;
-            continue;
-        }
-        atomicMax(winner + i, (static_cast<unsigned long long>(epoch) << 32) | static_cast<unsigned>(k));
-    }
+    update_elect(idx, n, capacity, winner, epoch, first, stride, bad);
     grid_barrier(ticket, status, ST_TIMEOUT);
     if (blockIdx.x == 0 && threadIdx.x == 0) ctrs[CTR_UPD_EPOCH] = epoch + 1u;  // 2^32 updates before a wrap
-    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < n; k += stride) {
-        const int32_t i = idx[k];
-        if (i < 0 || i >= capacity) continue;
-        if (__ldcg(winner + i) == ((static_cast<unsigned long long>(epoch) << 32) | static_cast<unsigned>(k))) {
-            const float v = p[k];
-            if (!(v >= 0.f)) bad = true;
-            prio[i] = v;
-        }
-    }
+    update_apply(idx, p, n, capacity, winner, prio, epoch, first, stride, bad);
     if (bad) atomicOr(status, ST_VALUE);
 }
 

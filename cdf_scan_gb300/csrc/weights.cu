@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kThreads) is_weights_kernel(IswParams P) {
         m = fminf(m, pa);
     }
     if (bad) atomicOr(P.status, ST_VALUE);
-    m = block_min(m, s_red);
+    m = block_min(m, s_red) + 0.f;  // a -0 minimum becomes +0, as in the fused sampler
     if (threadIdx.x == 0) P.slots[blockIdx.x] = m;
     grid_barrier(P.ticket, P.status, ST_TIMEOUT);
     float g = __int_as_float(0x7f800000);

@@ -199,6 +199,23 @@ per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t 
                                const float* d_u01, float beta, int32_t* d_out_idx, float* d_out_w,
                                void* stream);
 
+/*
+ * per_step -- one minibatch step of proportional PER (PufferLib PR #615: the
+ * prefix sum is rebuilt once per minibatch update; foxhunt "Integration":
+ * update, then sample with IS weights): per_update(d_upd_idx, d_upd_prio,
+ * n_upd) when n_upd > 0, then per_build_cdf, then per_sample_weighted(B,
+ * seed, offset, mode, d_u01, beta, d_out_idx, d_out_w) -- the same
+ * arguments, checks and results as those calls, bit for bit.  For scan-only
+ * contexts (PER_SCAN without PER_TREE, mode PER_SCAN) of size <= 262,144
+ * and B <= 1024 per 2048 items, the three run in one cooperative launch with
+ * grid barriers between them; otherwise as the separate calls, in order.
+ * n_upd >= 0; the update buffers may be NULL when n_upd == 0.  Errors as the
+ * separate calls (PER_ERR_ARG before any launch).
+ */
+per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
+                    uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta, int32_t* d_out_idx,
+                    float* d_out_w, void* stream);
+
 /* per_total -- total priority (foxhunt "Integration" / total_priority):
  * mode PER_TREE reads tree[1], PER_SCAN reads cdf[n-1] (after per_build_cdf).
  * per_total writes one float to device memory; per_total_host synchronises

@@ -272,3 +272,72 @@ def test_grid_barriers_across_varying_batch_sizes():
         assert np.array_equal(host(i1), want)
         assert np.array_equal(host(w1), host(w2))
         assert np.max(np.abs(host(w2) / oracle.is_weights(p, N, 0.6, want, 0.4) - 1.0)) <= 1e-6
+
+
+# ------------------------------------------------------------- fused step ---
+
+@pytest.mark.parametrize("N,B,n_upd,flags", [(262144, 8192, 8192, SCAN), (262144, 8192, 0, SCAN),
+                                             (262144, 1, 5, SCAN), (1000, 37, 300, SCAN), (8192, 1024, 1024, SCAN),
+                                             (262144, 65536, 8192, SCAN), (1 << 20, 8192, 4096, SCAN),
+                                             (262144, 8192, 8192, SCAN | TREE)])
+def test_per_step_equals_the_separate_calls(N, B, n_upd, flags):
+    """per_step (one cooperative launch when it applies, else the separate
+    calls) gives per_update + per_build_cdf + per_sample_weighted bit for
+    bit: indices, weights, priorities and CDF, over several rounds."""
+    g = workloads.rng(505, N + B + n_upd)
+    p = workloads.abs_normal(N, g)
+    a, b = new_ctx(p, 0.6, flags), new_ctx(p, 0.6, flags)
+    ia = torch.empty(B, dtype=torch.int32, device="cuda")
+    wa = torch.empty(B, dtype=torch.float32, device="cuda")
+    ib = torch.empty(B, dtype=torch.int32, device="cuda")
+    wb = torch.empty(B, dtype=torch.float32, device="cuda")
+    for r in range(3):
+        if n_upd:
+            idx = g.integers(0, N, size=n_upd).astype(np.int32)
+            if n_upd > 4:
+                dup = g.choice(n_upd, n_upd // 5, replace=False)
+                idx[dup] = idx[g.integers(0, n_upd, size=dup.size)]
+            ui, up = dev(idx), dev(workloads.abs_normal(n_upd, g))
+        else:
+            ui = up = None
+        u01 = dev(workloads.uniform_open_closed(B, g)) if r == 2 else None
+        per.per_step(a.handle, ui, up, B, 11, r * B, SCAN, 0.4, ia, wa, u01=u01)
+        if n_upd:
+            per.per_update(b.handle, ui, up)
+        per.per_build_cdf(b.handle)
+        per.per_sample_weighted(b.handle, B, 11, r * B, SCAN, 0.4, ib, wb, u01=u01)
+        assert np.array_equal(host(ia), host(ib)), f"round {r}"
+        assert np.array_equal(host(wa), host(wb)), f"round {r}"
+        assert np.array_equal(host(per.read_priorities(a.handle, N)), host(per.read_priorities(b.handle, N)))
+        assert np.array_equal(host(per.read_cdf(a.handle))[:N], host(per.read_cdf(b.handle))[:N])
+    assert per.per_check(a.handle) == 0
+    assert per.per_check(b.handle) == 0
+
+
+def test_minibatch_loop_with_per_step_matches_oracle():
+    """The minibatch workload through per_step: round r applies round r-1's
+    updates, rebuilds and samples; checked against the oracle every round."""
+    W = workloads.MINIBATCH
+    N, B, R, alpha, beta, seed = W["N"], W["B"], W["rounds"], W["alpha"], W["beta"], W["seed"]
+    p = workloads.minibatch_priorities()
+    ctx = new_ctx(p, alpha, SCAN)
+    idx = [torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(2)]
+    w = torch.empty(B, dtype=torch.float32, device="cuda")
+    newp = None
+    for r in range(R):
+        prev = idx[(r + 1) % 2] if r else None
+        per.per_step(ctx.handle, prev, newp, B, seed, r * B, SCAN, beta, idx[r % 2], w)
+        if r:
+            p = oracle.apply_updates(p, host(prev), host(newp))
+        c = host(per.read_cdf(ctx.handle))[:N]
+        C = oracle.cdf64(p, alpha)
+        assert np.all(np.diff(c) >= 0)
+        assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
+        got = host(idx[r % 2])
+        want, _ = oracle.sample_cdf_f32(c, B, seed, r * B)
+        assert np.array_equal(got, want), f"round {r}"
+        ww = host(w)
+        assert ww.max() == 1.0
+        assert np.max(np.abs(ww / oracle.is_weights(p, N, alpha, got, beta) - 1.0)) <= 1e-6
+        newp = dev(workloads.minibatch_new_priorities(r))
+    assert per.per_check(ctx.handle) == 0
