@@ -592,7 +592,8 @@ per_status launch_scan_2p(ScanParams P, int num_sms, cudaStream_t s) {
 // ---- one wave of tiles (wave_scan_tile) ---------------------------------------
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) build_cdf_wave_kernel(ScanParams P) {
-    const unsigned epoch = wave_scan_tile<THREADS>(P, blockIdx.x);
+    const unsigned epoch = wave_scan_tile<THREADS>(P, blockIdx.x, P.p + static_cast<int64_t>(blockIdx.x) * THREADS * 8,
+                                                   nullptr);
     // the last CTA to finish advances the epoch for the next call
     if (threadIdx.x == 0) {
         const unsigned done = atomicAdd(P.ctrs + CTR_SCAN_DONE, 1u);

@@ -182,11 +182,15 @@ __device__ __forceinline__ void advance_scan_epoch(const ScanParams& P, unsigned
 // finish their local values.  Each tile writes
 // clamp(hi + (lo + local), fl32(E_c), fl32(E_{c+1})) with E_c its exact carry
 // as fp32 hi + lo; the clamp bounds are monotone in c, so the CDF is
-// non-decreasing.  Returns the epoch the tile was tagged with; the caller
-// advances it once every tile is done (advance_scan_epoch).
+// non-decreasing.  `src` points at the tile's first priority (global memory,
+// or a shared-memory copy); when `s_out` is not null the tile's CDF values
+// are also left there (shared memory, TILE floats).  Returns the epoch the
+// tile was tagged with; the caller advances it once every tile is done
+// (advance_scan_epoch).
 
 template <int THREADS>
-__device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t c) {
+__device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t c, const float* src,
+                                                   float* s_out) {
     constexpr int ITEMS = 8;
     constexpr int WARPS = THREADS / 32;
     constexpr int TILE = THREADS * ITEMS;
@@ -200,17 +204,16 @@ __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t 
 
     float v[ITEMS];
     if (base + i0 + ITEMS <= P.n) {
-        const float4 a = ld_f4(P.p + base + i0), b = ld_f4(P.p + base + i0 + 4);
+        const float4 a = ld_f4(src + i0), b = ld_f4(src + i0 + 4);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
 #pragma unroll
-        for (int e = 0; e < ITEMS; ++e) v[e] = base + i0 + e < P.n ? P.p[base + i0 + e] : 0.f;
+        for (int e = 0; e < ITEMS; ++e) v[e] = base + i0 + e < P.n ? src[i0 + e] : 0.f;
     }
     bool bad = false;
-    pow_alpha_n<ITEMS>(v, P.alpha, P.pow_lim, P.pow_mode, bad, [&](int e) {
-        return base + i0 + e < P.n ? P.p[base + i0 + e] : 0.f;
-    });
+    pow_alpha_n<ITEMS>(v, P.alpha, P.pow_lim, P.pow_mode, bad,
+                       [&](int e) { return base + i0 + e < P.n ? src[i0 + e] : 0.f; });
     if (base + i0 + ITEMS > P.n) {  // padding beyond n contributes 0 (p^0 would be 1)
 #pragma unroll
         for (int e = 0; e < ITEMS; ++e)
@@ -271,6 +274,10 @@ __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t 
     float o[ITEMS];
 #pragma unroll
     for (int e = 0; e < ITEMS; ++e) o[e] = fminf(fmaxf(cy.x + (cy.y + (off + v[e])), cy.z), cy.w);
+    if (s_out) {  // the tile's CDF values for the caller (shared memory)
+        *reinterpret_cast<float4*>(s_out + i0) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(s_out + i0 + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
     if (base + i0 + ITEMS <= P.n) {
         st_f4(P.cdf + base + i0, make_float4(o[0], o[1], o[2], o[3]));
         st_f4(P.cdf + base + i0 + 4, make_float4(o[4], o[5], o[6], o[7]));

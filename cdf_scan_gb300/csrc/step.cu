@@ -18,43 +18,100 @@
 
 namespace {
 
-constexpr int kStepThreads = 256;  // the one-wave scan's tile: 256 x 8 items
+constexpr int kStepThreads = 256;               // the one-wave scan's tile: 256 x 8 items
+constexpr int kStepTile = kStepThreads * 8;
 
 struct StepParams {
     ScanParams scan;
-    SampleParams sample;
+    // sampling and weights
+    int B;
+    uint64_t seed, offset;
+    float alpha, beta;
+    bool alpha_one;
+    int32_t* __restrict__ out;
+    float* __restrict__ out_w;
+    // updates
     const int32_t* __restrict__ upd_idx;
     const float* __restrict__ upd_p;
     int n_upd;
     int64_t capacity;
-    float* prio;
-    unsigned long long* ticket;  // grid-barrier word of every phase
+    float* prio;                 // the buffer the updates write (== scan.p)
+    unsigned long long* ticket;  // grid-barrier word
+    unsigned long long* last;    // [tile * kDescStride]: tagged last CDF value of each tile
     unsigned* step_min;          // call counter, then the batch-minimum word of even and odd calls
-    int* status;
-    int per_cta;  // samples per CTA
 };
 
-// CTA c owns scan tile c (the grid is exactly the tiles) and samples
-// [c * per_cta, (c + 1) * per_cta).
-template <int SPT>
-__global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
-    extern __shared__ __align__(128) float s_dyn[];  // the sampler's coarse index and window
-    constexpr int THREADS = kStepThreads;
+// Bounded wait for a tagged word (tag << 32 | float bits) of this call.
+__device__ __forceinline__ float wait_tagged(const unsigned long long* w, unsigned tag, int* status) {
+    uint64_t t0 = 0;
+    for (;;) {
+        const unsigned long long x = ld_relaxed_u64(w);
+        if (static_cast<unsigned>(x >> 32) == tag) return __uint_as_float(static_cast<unsigned>(x));
+        const uint64_t now = global_ns();
+        if (t0 == 0) {
+            t0 = now;
+        } else if (now - t0 > kWaitLimitNs) {
+            atomicOr(status, ST_TIMEOUT);
+            return __int_as_float(0x7fc00000);
+        }
+        __nanosleep(32);
+    }
+}
 
-    // ---- 1. priority updates of this CTA's tile ----------------------------
-    // The CTA owns items [c * TILE, (c + 1) * TILE) (the launcher guarantees
-    // capacity <= gridDim.x * TILE): it reads the whole batch, keeps in
-    // shared memory the last batch position of each of its items, writes
-    // the winners' priorities, and scans them below -- no other CTA reads
-    // or writes these items, so no grid barrier is needed.
-    if (S.n_upd > 0) {
-        constexpr int TILE = THREADS * 8;
-        __shared__ int s_win[TILE];
-        const int64_t lo = static_cast<int64_t>(blockIdx.x) * TILE;
+// CTA c owns items [c * TILE, (c + 1) * TILE) (the grid is exactly the
+// tiles; capacity <= tiles * TILE when there are updates):
+//   0. one bulk copy brings the tile's priorities into shared memory while
+//      the update batch is read;
+//   1. the last batch position of each of the CTA's items is elected in
+//      shared memory (atomicMax), and the winners' priorities are written
+//      to the buffer and to the shared copy -- no other CTA touches these
+//      items, so no grid barrier;
+//   2. the tile is scanned from the shared copy (wave_scan_tile); its CDF
+//      values stay in shared memory and its last one is published as a
+//      tagged word;
+//   3. with T = the last tile's last value and the previous tile's last
+//      value, the CTA takes exactly the strata k whose threshold u_k falls
+//      in (previous last, own last] -- their lower_bound lies in this tile
+//      -- searches them in shared memory and computes p^alpha of the hits;
+//   4. the batch minimum of p^alpha goes through one atomicMin word and one
+//      grid barrier, then the weights.
+// Thresholds are Philox draws (U in (0, 1]), so u_k lies within a rounding
+// margin of stratum k's interval (k T/B, (k+1) T/B]; the CTA evaluates the
+// strata whose interval meets its range widened by that margin.
+__global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
+    constexpr int THREADS = kStepThreads, TILE = kStepTile;
+    __shared__ __align__(16) float s_p[TILE];    // the tile's priorities (after the updates)
+    __shared__ __align__(16) float s_cdf[TILE];  // the tile's CDF values
+    __shared__ int s_win[TILE];                  // last batch position updating each item
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ unsigned s_parity;
+    __shared__ float s_red[THREADS / 32];
+    __shared__ float s_bound[3];  // previous tile's last value, own last value, T
+    __shared__ float s_min;
+
+    const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
+    const int n = static_cast<int>(S.scan.n);
+    const int lo = c * TILE;
+    const int valid = min(TILE, n - lo);  // >= 1
+    const int bulk = valid & ~3;
+    int* status = S.scan.status;
+
+    // ---- 0. the tile's priorities ------------------------------------------
+    if (threadIdx.x == 0) {
+        s_parity = ld_relaxed_u32(S.step_min) & 1u;
+        mbar_init(&s_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(&s_bar, static_cast<unsigned>(bulk) * 4u);
+        if (bulk) bulk_copy_g2s(s_p, S.scan.p + lo, static_cast<unsigned>(bulk) * 4u, &s_bar);
+    }
+    if (S.n_upd > 0)
         for (int j = threadIdx.x; j < TILE; j += THREADS) s_win[j] = -1;
-        __syncthreads();
-        bool bad = false;
-        constexpr int kU = 8;  // batch positions per thread per round, loads issued first
+    __syncthreads();
+
+    // ---- 1. the updates of this tile ----------------------------------------
+    bool bad = false;
+    if (S.n_upd > 0) {
+        constexpr int kU = 16;  // batch positions per thread per round, loads issued first
         for (int k0 = 0; k0 < S.n_upd; k0 += THREADS * kU) {
             int32_t iv[kU];
 #pragma unroll
@@ -74,94 +131,125 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
                 if (i >= lo && i < lo + TILE) atomicMax(&s_win[i - lo], k);
             }
         }
-        __syncthreads();
+    }
+    if (!mbar_wait_bounded(&s_bar, 0)) atomicOr(status, ST_TIMEOUT);
+    for (int j = bulk + threadIdx.x; j < valid; j += THREADS) s_p[j] = S.scan.p[lo + j];  // 0-3 tail items
+    __syncthreads();
+    if (S.n_upd > 0) {
         for (int j = threadIdx.x; j < TILE; j += THREADS) {
             const int k = s_win[j];
             if (k >= 0) {
                 const float v = __ldg(S.upd_p + k);
                 if (!(v >= 0.f)) bad = true;
                 S.prio[lo + j] = v;
+                if (j < valid) s_p[j] = v;
             }
         }
-        if (bad) atomicOr(S.status, ST_VALUE);
-        __syncthreads();  // this CTA's new priorities before its scan reads them
+        __syncthreads();
     }
+    if (bad) atomicOr(status, ST_VALUE);
 
-    // ---- 2. build_cdf: tile blockIdx.x ------------------------------------
-    // (this call's parity picks the batch-minimum word: step_min[0] counts
-    // the calls, every CTA reads it before the grid barrier below, CTA 0
-    // advances it after the weights' barrier and resets the next call's word)
-    __shared__ unsigned s_parity;
-    if (threadIdx.x == 0) s_parity = ld_relaxed_u32(S.step_min) & 1u;
-    const unsigned scan_epoch = wave_scan_tile<THREADS>(S.scan, blockIdx.x);
-    grid_barrier(S.ticket, S.status, ST_TIMEOUT);  // CDF and coarse index complete
+    // ---- 2. the scan of this tile ---------------------------------------------
+    const unsigned epoch = wave_scan_tile<THREADS>(S.scan, c, s_p, s_cdf);
+    __syncthreads();  // s_cdf complete
+    const unsigned tag = 2u * epoch + 1u;
     if (threadIdx.x == 0) {
-        if (blockIdx.x == 0) {
-            advance_scan_epoch(S.scan, scan_epoch);
-            S.step_min[1 + (s_parity ^ 1u)] = 0x7f800000u;  // +inf for the next call
-        }
-        // the sampler's bulk copies (async proxy) read what this launch wrote
-        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const float own = s_cdf[valid - 1];
+        *reinterpret_cast<volatile unsigned long long*>(S.last + static_cast<int64_t>(c) * kDescStride) =
+            (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(own);
+        s_bound[0] = c == 0 ? -__int_as_float(0x7f800000)
+                            : wait_tagged(S.last + static_cast<int64_t>(c - 1) * kDescStride, tag, status);
+        s_bound[1] = own;
+        s_bound[2] = c == G - 1 ? own : wait_tagged(S.last + static_cast<int64_t>(G - 1) * kDescStride, tag, status);
     }
     __syncthreads();
-
-    // ---- 3. samples and IS weights ----------------------------------------
-    SampleParams sp = S.sample;
-    sp.min_word = S.step_min + 1 + s_parity;
-    const int k0 = static_cast<int>(blockIdx.x) * S.per_cta;
-    const int kend = min(sp.B, k0 + S.per_cta);
-    coarse_sample<THREADS, SPT, true>(sp, k0 < kend ? k0 : kend, kend, s_dyn);
-    if (blockIdx.x == 0 && threadIdx.x == 0) S.step_min[0] = S.step_min[0] + 1u;  // every CTA has read it
-}
-
-template <int SPT>
-per_status launch_step_cfg(const StepParams& S, unsigned grid, cudaStream_t s) {
-    const int smem = (kCoarseCap + kWindowCap) * static_cast<int>(sizeof(float));
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        if (cudaFuncSetAttribute(per_step_kernel<SPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-                cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, per_step_kernel<SPT>, kStepThreads, smem) !=
-                cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
+    const float prev = s_bound[0], own = s_bound[1], T = s_bound[2];
+    const int B = S.B;
+    // every tile's scan is done once T is known (the last tile's carry needed
+    // all of them), so the epoch and the call counter may move on
+    auto finish = [&]() {
+        if (c == 0 && threadIdx.x == 0) {
+            advance_scan_epoch(S.scan, epoch);
+            if (epoch + 1u >= (1u << 30))  // the epoch wrapped: clear the tagged words once
+                for (int64_t i = 0; i < kMaxWaveTiles; ++i) S.last[i * kDescStride] = 0ull;
+            S.step_min[1 + (s_parity ^ 1u)] = 0x7f800000u;  // +inf for the next call
+            S.step_min[0] = S.step_min[0] + 1u;
+        }
+    };
+    if (!(T > 0.f)) {  // nothing to sample: every CTA sees the same T
+        if (c == 0 && threadIdx.x == 0) atomicOr(status, ST_EMPTY);
+        const int per = (B + G - 1) / G;
+        for (int k = c * per + threadIdx.x; k < min(B, (c + 1) * per); k += THREADS) S.out[k] = 0;
+        finish();
+        return;
     }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess)
-        return PER_ERR_CUDA;
-    if (static_cast<int64_t>(grid) > static_cast<int64_t>(per_sm) * sms) return PER_ERR_STATE;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kStepThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, per_step_kernel<SPT>, S);
-    per_note_launch();
-    return cuda_status(e);
+
+    // ---- 3. the strata of this tile -------------------------------------------
+    const float fB = static_cast<float>(B);
+    const double scale = static_cast<double>(B) / static_cast<double>(T);
+    const int margin = 2 + (B >> 20);
+    const int k_lo = c == 0 ? 0 : max(0, static_cast<int>(floor(static_cast<double>(prev) * scale)) - margin);
+    const int k_hi = c == G - 1 ? B : min(B, static_cast<int>(ceil(static_cast<double>(own) * scale)) + margin + 1);
+    auto mine = [&](float u) { return (c == 0 || u > prev) && (c == G - 1 || u <= own); };
+    float m = __int_as_float(0x7f800000);  // +inf
+    int k_first = -1;                      // this thread's hit in the first round (weights from registers)
+    float pa_first = 0.f;
+    for (int k0 = k_lo; k0 < k_hi; k0 += THREADS) {
+        const int k = k0 + threadIdx.x;
+        if (k >= k_hi) continue;
+        const float u = stratified_threshold(k, u01_open_closed(S.seed, S.offset + static_cast<uint64_t>(k)), fB, T);
+        if (!mine(u)) continue;
+        const int idx = min(lo + smem_lower_bound(s_cdf, 0, valid, u), n - 1);
+        S.out[k] = idx;
+        const float pa = pow_accurate(s_p[idx - lo], S.alpha, S.alpha_one);
+        m = fminf(m, pa);
+        if (k0 == k_lo) {
+            k_first = k;
+            pa_first = pa;
+        } else {
+            S.out_w[k] = pa;  // staged until the minimum is known
+        }
+    }
+
+    // ---- 4. the batch minimum, then the weights --------------------------------
+    m = block_min<THREADS>(m, s_red) + 0.f;  // a -0 minimum becomes +0
+    unsigned* min_word = S.step_min + 1 + s_parity;
+    if (threadIdx.x == 0) atomicMin(min_word, __float_as_uint(m));
+    grid_barrier(S.ticket, status, ST_TIMEOUT);
+    if (threadIdx.x == 0) s_min = __uint_as_float(ld_relaxed_u32(min_word));
+    __syncthreads();
+    finish();
+    const float pa_min = s_min;
+    if (k_first >= 0) S.out_w[k_first] = powf(__fdiv_rn(pa_min, pa_first), S.beta);
+    for (int k0 = k_lo + THREADS; k0 < k_hi; k0 += THREADS) {
+        const int k = k0 + threadIdx.x;
+        if (k >= k_hi) continue;
+        const float u = stratified_threshold(k, u01_open_closed(S.seed, S.offset + static_cast<uint64_t>(k)), fB, T);
+        if (mine(u)) S.out_w[k] = powf(__fdiv_rn(pa_min, __ldcg(S.out_w + k)), S.beta);
+    }
 }
 
 }  // namespace
 
 // The fused step for scan-only contexts whose CDF fits one wave of
-// 2048-item tiles and whose coarse index fits the sampler's staging buffer;
-// PER_ERR_STATE (nothing launched) when it does not apply.
+// 2048-item tiles, with Philox thresholds; PER_ERR_STATE (nothing launched)
+// when it does not apply.
 per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p, int n_upd, int B, uint64_t seed,
                        uint64_t offset, const float* u01, float beta, int32_t* out, float* out_w, cudaStream_t s) {
-    constexpr int TILE = kStepThreads * 8;
+    constexpr int TILE = kStepTile;
     const int64_t n = ctx->size;
-    if (ctx->flags != PER_SCAN || !ctx->coarse || n < 1 || n > (int64_t(1) << 19)) return PER_ERR_STATE;
-    if ((n + kCoarseStride - 1) / kCoarseStride > kCoarseCap) return PER_ERR_STATE;
+    if (ctx->flags != PER_SCAN || u01 || !ctx->step_last || n < 1 || n > (int64_t(1) << 19)) return PER_ERR_STATE;
     const int64_t tiles = (n + TILE - 1) / TILE;
+    if (tiles > ctx->scan_desc_tiles) return PER_ERR_STATE;
     // every index an update may name lies in some CTA's tile
     if (n_upd > 0 && ctx->capacity > tiles * TILE) return PER_ERR_STATE;
-    if (tiles > ctx->scan_desc_tiles || tiles > ctx->slot_n) return PER_ERR_STATE;
-    const int64_t per_cta = (B + tiles - 1) / tiles;
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, per_step_kernel, kStepThreads, 0) != cudaSuccess)
+            return PER_ERR_CUDA;
+        if (per_sm < 1) per_sm = 1;
+    }
+    if (tiles > static_cast<int64_t>(per_sm) * ctx->num_sms) return PER_ERR_STATE;
     StepParams S = {};
     S.scan.p = ctx->prio;
     S.scan.cdf = ctx->cdf;
@@ -177,34 +265,32 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
     S.scan.status = ctx->status;
     S.scan.num_tiles = static_cast<unsigned>(tiles);
     S.scan.coarse = ctx->coarse;
-    S.sample.cdf = ctx->cdf;
-    S.sample.coarse = ctx->coarse;
-    S.sample.n = static_cast<int>(n);
-    S.sample.B = B;
-    S.sample.seed = seed;
-    S.sample.offset = offset;
-    S.sample.u01 = u01;
-    S.sample.out = out;
-    S.sample.status = ctx->status;
-    S.sample.prio = ctx->prio;
-    S.sample.alpha = ctx->alpha;
-    S.sample.alpha_one = ctx->alpha == 1.0f;
-    S.sample.beta = beta;
-    S.sample.out_w = out_w;
-    S.sample.slots = ctx->slots;
-    S.sample.ticket = ctx->tickets + TK_STEP;
+    S.B = B;
+    S.seed = seed;
+    S.offset = offset;
+    S.alpha = ctx->alpha;
+    S.beta = beta;
+    S.alpha_one = ctx->alpha == 1.0f;
+    S.out = out;
+    S.out_w = out_w;
     S.upd_idx = upd_idx;
     S.upd_p = upd_p;
     S.n_upd = n_upd;
     S.capacity = ctx->capacity;
     S.prio = ctx->prio;
     S.ticket = ctx->tickets + TK_STEP;
+    S.last = ctx->step_last;
     S.step_min = ctx->step_min;
-    S.status = ctx->status;
-    S.per_cta = static_cast<int>(per_cta);
-    const unsigned grid = static_cast<unsigned>(tiles);
-    if (per_cta <= kStepThreads) return launch_step_cfg<1>(S, grid, s);
-    if (per_cta <= 2 * kStepThreads) return launch_step_cfg<2>(S, grid, s);
-    if (per_cta <= 4 * kStepThreads) return launch_step_cfg<4>(S, grid, s);
-    return PER_ERR_STATE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles));
+    cfg.blockDim = dim3(kStepThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, per_step_kernel, S);
+    per_note_launch();
+    return cuda_status(e);
 }
