@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
     __shared__ unsigned s_parity;
     __shared__ float s_red[THREADS / 32];
     __shared__ float s_bound[3];  // previous tile's last value, own last value, T
+    __shared__ int s_krange[2];   // strata [k_lo, k_hi) this CTA evaluates
     __shared__ float s_min;
 
     const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
     // ---- 1. the updates of this tile ----------------------------------------
     bool bad = false;
     if (S.n_upd > 0) {
-        constexpr int kU = 16;  // batch positions per thread per round, loads issued first
+        constexpr int kU = 32;  // batch positions per thread per round, loads issued first
         for (int k0 = 0; k0 < S.n_upd; k0 += THREADS * kU) {
             int32_t iv[kU];
 #pragma unroll
@@ -160,7 +161,15 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
         s_bound[0] = c == 0 ? -__int_as_float(0x7f800000)
                             : wait_tagged(S.last + static_cast<int64_t>(c - 1) * kDescStride, tag, status);
         s_bound[1] = own;
-        s_bound[2] = c == G - 1 ? own : wait_tagged(S.last + static_cast<int64_t>(G - 1) * kDescStride, tag, status);
+        const float T = c == G - 1 ? own : wait_tagged(S.last + static_cast<int64_t>(G - 1) * kDescStride, tag, status);
+        s_bound[2] = T;
+        // strata whose interval (k T/B, (k+1) T/B], widened by the rounding
+        // margin of the threshold, meets (prev, own] (once, in fp64)
+        const int B = S.B;
+        const int margin = 2 + (B >> 20);
+        const double scale = static_cast<double>(B) / static_cast<double>(T);
+        s_krange[0] = c == 0 ? 0 : max(0, static_cast<int>(floor(static_cast<double>(s_bound[0]) * scale)) - margin);
+        s_krange[1] = c == G - 1 ? B : min(B, static_cast<int>(ceil(static_cast<double>(own) * scale)) + margin + 1);
     }
     __syncthreads();
     const float prev = s_bound[0], own = s_bound[1], T = s_bound[2];
@@ -186,10 +195,7 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
 
     // ---- 3. the strata of this tile -------------------------------------------
     const float fB = static_cast<float>(B);
-    const double scale = static_cast<double>(B) / static_cast<double>(T);
-    const int margin = 2 + (B >> 20);
-    const int k_lo = c == 0 ? 0 : max(0, static_cast<int>(floor(static_cast<double>(prev) * scale)) - margin);
-    const int k_hi = c == G - 1 ? B : min(B, static_cast<int>(ceil(static_cast<double>(own) * scale)) + margin + 1);
+    const int k_lo = s_krange[0], k_hi = s_krange[1];
     auto mine = [&](float u) { return (c == 0 || u > prev) && (c == G - 1 || u <= own); };
     float m = __int_as_float(0x7f800000);  // +inf
     int k_first = -1;                      // this thread's hit in the first round (weights from registers)
