@@ -9,17 +9,17 @@
 //   2. the exact total Q of q_i = fix40(exp(lw_i - m)) (40 fractional bits,
 //      64-bit integer sums: order-independent);
 //   3. an exact 64-bit integer scan of the same q_i (8 consecutive particles
-//      per lane, warp shuffles, a block scan per chunk), c_i = f(E_i) *
-//      fl32(1 / Q), f a monotone fp32 rounding of E (u64_to_f32) -- so c is
-//      monotone in the exact prefix E_i -- and then, instead
-//      of one binary search per output, every particle i computes
-//      n(c) = #{j : u_j <= c} for its own c_i in closed form (a guess from
-//      c*P - U corrected by at most a couple of exact threshold evaluations);
-//      particle i owns outputs [n(c_{i-1}), n(c_i)) -- exactly the outputs
-//      whose lower_bound lands on i, the last particle's run extending to P
-//      (the clamp).  Short runs are written by the particle's own lane; long
-//      ones (heavy particles) are queued and written by the whole warp with
-//      16-byte stores.
+//      per lane, warp shuffles, a block scan per chunk of 4096 particles),
+//      c_i = f(E_i) * fl32(1 / Q), f a monotone fp32 rounding of E
+//      (u64_to_f32) -- so c is monotone in the exact prefix E_i.  Every
+//      particle i computes n(c_i) = #{j : u_j <= c_i} in closed form (a guess
+//      from c*P - U corrected by a couple of exact threshold evaluations) and
+//      owns outputs [n(c_{i-1}), n(c_i)) -- exactly the outputs whose
+//      lower_bound lands on i, the last particle's run extending to P (the
+//      clamp).  The outputs are written in blocks of 4096 aligned to output
+//      positions: each non-empty run puts its particle at its first output in
+//      shared memory, and a block-wide prefix max fills every output with the
+//      particle whose run covers it (16-byte stores; no per-output search).
 // exp is the hardware ex2 of (lw - m) * log2(e): its relative error (~2^-22)
 // stays far inside the CDF tolerance.  For a power-of-two P the threshold
 // division is an exact multiplication by 2^-k.
@@ -32,8 +32,6 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kLane = 8;                   // consecutive particles per lane per chunk
 constexpr int kBatch = 8;                  // float4 loads in flight per thread in passes 1 and 2
-constexpr int kShortRun = 8;               // runs up to this long are written by their own lane
-constexpr int kQueue = 64;                 // long runs a warp can queue per chunk
 constexpr int kChunk = kThreads * kLane;   // 4096
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -62,6 +60,28 @@ __device__ __forceinline__ int count_le(float c, float U, int P, float fP, float
     else j = static_cast<int>(g);
     while (j + 1 < P && row_threshold(j + 1, U, fP, inv_p, pow2) <= c) ++j;
     while (j >= 0 && row_threshold(j, U, fP, inv_p, pow2) > c) --j;
+    return j + 1;
+}
+
+// count_le for a power-of-two P without loops.  u_j <= c exactly when
+// fl32(j + U) <= C = c * P (both products by a power of two are exact), and
+// fl32(j + U) is non-decreasing in j with fl32(j + U) <= C for j + U <= C - 1
+// and > C for j + U >= C + 1 (C < 2^24), so the last such j lies within one of
+// floor(C - U); the fp32 rounding of C - U moves the guess by at most one more:
+// two exact checks each way settle it.
+__device__ __forceinline__ int count_le_pow2(float c, float U, int P, float fP) {
+    const float C = __fmul_rn(c, fP);
+    const float g = __fsub_rn(C, U);
+    int j;
+    if (!(g >= 0.f)) j = -1;
+    else if (g >= fP) j = P - 1;
+    else j = static_cast<int>(g);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        if (j + 1 < P && __fadd_rn(__int2float_rn(j + 1), U) <= C) ++j;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        if (j >= 0 && __fadd_rn(__int2float_rn(j), U) > C) --j;
     return j + 1;
 }
 
@@ -98,8 +118,9 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     __shared__ float s_f[kWarps];
     __shared__ unsigned long long s_u[kWarps];
     __shared__ unsigned long long s_off[kWarps + 1];
-    __shared__ int s_q[kWarps][3 * kQueue];  // long runs: (particle, first, end) per warp
-    __shared__ int s_qn[kWarps];
+    __shared__ __align__(16) int s_stage[kChunk];  // one block of outputs: run starts, then filled
+    __shared__ int s_wmax[kWarps];
+    __shared__ int s_range[2];                      // the chunk's outputs [j_lo, j_hi)
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int P = R.P;
@@ -151,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     const float inv_p = __fdiv_rn(1.0f, fP);
     const float U = R.u_rows ? R.u_rows[b] : u01_closed_open(R.seed, R.offset + static_cast<uint64_t>(b));
 
-    // ---- 3: scan and scatter -----------------------------------------------------
+    // ---- 3: scan, then the outputs of each chunk ----------------------------------
     // the next chunk's loads are issued before the current chunk is processed
     float4 nxt[kLane / 4];
 #pragma unroll
@@ -162,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     unsigned long long carry = 0ull;
     for (int c0 = 0; c0 < P; c0 += kChunk) {
         const int i0 = c0 + threadIdx.x * kLane;
-        const int nv = min(kLane, P - i0);  // valid particles of this lane (P % 4 == 0)
+        const int valid = min(kChunk, P - c0);  // particles of this chunk (P % 4 == 0)
         float4 cur[kLane / 4];
 #pragma unroll
         for (int h = 0; h < kLane / 4; ++h) {
@@ -195,56 +216,88 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
         __syncthreads();
         const unsigned long long base = carry + s_off[warp] + (x - run);  // E before this lane's first particle
         carry += s_off[kWarps];
-
-        // run ends: particle i owns outputs [n(c_{i-1}), n(c_i)); the last
-        // particle's run extends to P (the clamp)
+        float cv[kLane];
+#pragma unroll
+        for (int e = 0; e < kLane; ++e) cv[e] = __fmul_rn(u64_to_f32(base + r[e]), inv);
+        if (R.out_cdf && i0 < P) {
+            float* crow = R.out_cdf + static_cast<size_t>(b) * P + i0;
+            st_f4(crow, make_float4(cv[0], cv[1], cv[2], cv[3]));
+            if (i0 + 4 < P) st_f4(crow + 4, make_float4(cv[4], cv[5], cv[6], cv[7]));
+        }
+        // run ends: particle i owns outputs [n(c_{i-1}), n(c_i)), the last
+        // particle's run extending to P (the clamp)
+        auto n_of = [&](float c) { return pow2 ? count_le_pow2(c, U, P, fP) : count_le(c, U, P, fP, inv_p, pow2); };
         int start = 0;  // n(c) of the particle before this lane's first
         if (i0 >= P) start = P;
-        else if (i0 > 0) start = count_le(__fmul_rn(u64_to_f32(base), inv), U, P, fP, inv_p, pow2);
-        float cv[kLane];
-        int nlast = start;
-        int* q = s_q[warp];
-        if (lane == 0) s_qn[warp] = 0;
-        __syncwarp();
+        else if (i0 > 0) start = n_of(__fmul_rn(u64_to_f32(base), inv));
+        int nend[kLane];
+        int prev = start;
 #pragma unroll
         for (int e = 0; e < kLane; ++e) {
             const int i = i0 + e;
-            cv[e] = __fmul_rn(u64_to_f32(base + r[e]), inv);
-            int n = nlast;
-            if (e < nv) n = (i == P - 1) ? P : max(count_le(cv[e], U, P, fP, inv_p, pow2), nlast);
-            if (n - nlast <= kShortRun) {
-                for (int j = nlast; j < n; ++j) orow[j] = i;
-            } else {  // a long run: queued for the whole warp
-                const int slot = atomicAdd(&s_qn[warp], 1);
-                if (slot < kQueue) {
-                    q[3 * slot] = i;
-                    q[3 * slot + 1] = nlast;
-                    q[3 * slot + 2] = n;
-                } else {
-                    for (int j = nlast; j < n; ++j) orow[j] = i;
-                }
-            }
-            nlast = n;
+            int n = prev;
+            if (i < P) n = (i == P - 1) ? P : max(n_of(cv[e]), prev);
+            nend[e] = n;
+            prev = n;
         }
-        if (R.out_cdf && nv > 0) {
-            float* crow = R.out_cdf + static_cast<size_t>(b) * P + i0;
+        // the chunk's outputs [j_lo, j_hi): from its first particle's run start
+        // to its last particle's run end
+        if (threadIdx.x == 0) s_range[0] = start;
+        if (threadIdx.x == kThreads - 1) s_range[1] = c0 + kChunk >= P ? P : nend[kLane - 1];
+        __syncthreads();
+        const int j_lo = s_range[0], j_hi = s_range[1];
+        // outputs in blocks of kChunk aligned to absolute output positions:
+        // each non-empty run writes its particle at its first output, and a
+        // prefix max fills every output with the particle whose run covers it
+        int started = -1;  // the last particle started in earlier blocks
+        for (int b0 = j_lo & ~(kChunk - 1); b0 < j_hi; b0 += kChunk) {
+            const int t0 = threadIdx.x * kLane;  // this thread's outputs in the block: b0 + t0 .. + 7
+            *reinterpret_cast<int4*>(s_stage + t0) = make_int4(-1, -1, -1, -1);
+            *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(-1, -1, -1, -1);
+            __syncthreads();
+            int a = start;
 #pragma unroll
-            for (int h = 0; h < kLane / 4; ++h)
-                if (4 * h < nv) st_f4(crow + 4 * h, make_float4(cv[4 * h], cv[4 * h + 1], cv[4 * h + 2], cv[4 * h + 3]));
+            for (int e = 0; e < kLane; ++e) {
+                if (nend[e] > a && a >= b0 && a < b0 + kChunk) s_stage[a - b0] = i0 + e;
+                a = nend[e];
+            }
+            __syncthreads();
+            const int4 v0 = *reinterpret_cast<const int4*>(s_stage + t0);
+            const int4 v1 = *reinterpret_cast<const int4*>(s_stage + t0 + 4);
+            int v[kLane] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int e = 1; e < kLane; ++e) v[e] = max(v[e], v[e - 1]);
+            int x = v[kLane - 1];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(PER_FULL_MASK, x, d);
+                if (lane >= d) x = max(x, y);
+            }
+            if (lane == 31) s_wmax[warp] = x;
+            int before = __shfl_up_sync(PER_FULL_MASK, x, 1);
+            if (lane == 0) before = -1;
+            __syncthreads();
+            int wb = started, all = started;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                if (w < warp) wb = max(wb, s_wmax[w]);
+                all = max(all, s_wmax[w]);
+            }
+            before = max(before, wb);
+#pragma unroll
+            for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
+            const int j0 = b0 + t0;
+            if (j0 >= j_lo && j0 + kLane <= j_hi) {
+                *reinterpret_cast<int4*>(orow + j0) = make_int4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<int4*>(orow + j0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kLane; ++e)
+                    if (j0 + e >= j_lo && j0 + e < j_hi) orow[j0 + e] = v[e];
+            }
+            started = all;
+            __syncthreads();  // s_stage and s_wmax are reused by the next block
         }
-        __syncwarp();
-        // long runs, one at a time, by all lanes: aligned 16-byte stores for
-        // the body, single stores for the ends
-        const int nq = min(s_qn[warp], kQueue);
-        for (int t = 0; t < nq; ++t) {
-            const int i = q[3 * t], j0 = q[3 * t + 1], j1 = q[3 * t + 2];
-            const int a0 = min((j0 + 3) & ~3, j1), a1 = max(j1 & ~3, a0);
-            if (j0 + lane < a0) orow[j0 + lane] = i;
-            if (a1 + lane < j1) orow[a1 + lane] = i;
-            const int4 v = make_int4(i, i, i, i);
-            for (int j = a0 + 4 * lane; j < a1; j += 128) *reinterpret_cast<int4*>(orow + j) = v;
-        }
-        __syncwarp();  // the queue is reused by the next chunk
     }
 }
 

@@ -308,6 +308,30 @@ def test_resample_matches_oracle(rows, P):
         assert np.all(np.diff(got[b]) >= 0)
 
 
+@pytest.mark.parametrize("P", [4096, 4100, 65536])
+def test_resample_skewed_rows(P):
+    """Rows whose mass sits on one or two particles: most chunks own no
+    output, one chunk owns nearly all (long galloping searches), and the
+    heavy particle may sit in the ragged last chunk."""
+    rows = 6
+    lw = np.full((rows, P), -np.inf, np.float32)
+    lw[0, 0] = 0.0                         # one-hot at the start
+    lw[1, P - 1] = 0.0                     # one-hot at the end (ragged tail when P % 4096)
+    lw[2, P // 3] = 0.0                    # one-hot in the middle
+    lw[3, 5], lw[3, P - 7] = 0.0, -1.0     # two heavy particles far apart
+    lw[4] = workloads.resample_logw(rows=1, P=P, seed=7)[0] * 4.0  # very skewed N(0, 8^2)
+    lw[5, ::97] = 0.0                      # sparse equal weights
+    out = torch.empty((rows, P), dtype=torch.int32, device="cuda")
+    cdf = torch.empty((rows, P), dtype=torch.float32, device="cuda")
+    per.per_resample(dev(lw), 3, 7, out, out_cdf=cdf)
+    got, c = host(out), host(cdf)
+    for b in range(rows):
+        U = oracle.u01_closed_open(3, 7, b)
+        assert np.array_equal(got[b], oracle.resample_row_on_cdf(c[b], U)), f"row {b}"
+        assert np.all(np.diff(got[b]) >= 0)
+        assert got[b].min() >= 0 and got[b].max() < P
+
+
 def test_resample_equal_weights_identity_and_u_override():
     rows, P = 2, 4096
     lw = np.zeros((rows, P), np.float32)
