@@ -77,7 +77,8 @@ def _load():
         "oracle_tree_leaves": (None, [_f32p, _i64, ctypes.c_double, _i64, _f32p]),
         "oracle_tree_build": (None, [_f32p, _i64, _f32p]),
         "oracle_tree_descend": (_i64, [_f32p, _i64, ctypes.c_float]),
-        "oracle_sample_tree": (None, [_f32p, _i64, _i64, _u64, _u64, _vp, _i32p, _f32p]),
+        "oracle_sample_tree": (None, [_f32p, _i64, _i64, _u64, _u64, _vp, ctypes.c_int, _i32p, _f32p]),
+        "oracle_thresholds_iid": (None, [_i64, _u64, _u64, _vp, ctypes.c_float, _f32p]),
         "oracle_is_weights": (None, [_f32p, _i64, ctypes.c_double, _i32p, _i64, ctypes.c_double, _f64p]),
         "oracle_resample_row": (None, [_f32p, _i64, ctypes.c_float, _vp, _i32p, _vp]),
         "oracle_resample_row_on_cdf": (None, [_f32p, _i64, ctypes.c_float, _i32p]),
@@ -153,6 +154,14 @@ def thresholds(B: int, seed: int, offset: int, T: float, u01=None) -> np.ndarray
     return out
 
 
+def thresholds_iid(B: int, seed: int, offset: int, T: float, u01=None) -> np.ndarray:
+    """i.i.d. thresholds u_k = fl32(U_k * T) (foxhunt "CUDA Kernels")."""
+    keep, ptr = _opt_f32(u01)
+    out = np.empty(B, np.float32)
+    _load().oracle_thresholds_iid(B, seed, offset, ptr, np.float32(T), out)
+    return out
+
+
 def lower_bound_f32(c, u: float) -> int:
     c = _f32(c)
     return int(_load().oracle_lower_bound_f32(c, c.size, np.float32(u)))
@@ -213,12 +222,12 @@ def tree_descend(tree, u: float) -> int:
     return int(_load().oracle_tree_descend(tree, tree.size // 2, np.float32(u)))
 
 
-def sample_tree(tree, B: int, seed: int, offset: int, u01=None):
+def sample_tree(tree, B: int, seed: int, offset: int, u01=None, iid: bool = False):
     tree = _f32(tree)
     keep, ptr = _opt_f32(u01)
     idx = np.empty(B, np.int32)
     u = np.empty(B, np.float32)
-    _load().oracle_sample_tree(tree, tree.size // 2, B, seed, offset, ptr, idx, u)
+    _load().oracle_sample_tree(tree, tree.size // 2, B, seed, offset, ptr, int(iid), idx, u)
     return idx, u
 
 

@@ -114,6 +114,17 @@ void oracle_thresholds(int64_t B, uint64_t seed, uint64_t offset, const float* u
     }
 }
 
+/* i.i.d. thresholds (foxhunt "CUDA Kernels": each sampling thread draws its
+ * own threshold in [0, total)): u_k = fl32(U_k * T), U_k from the same Philox
+ * stream as the stratified thresholds (or u01). */
+void oracle_thresholds_iid(int64_t B, uint64_t seed, uint64_t offset, const float* u01,
+                           float T, float* u_out) {
+    for (int64_t k = 0; k < B; ++k) {
+        float U = u01 ? u01[k] : oracle_u01_open_closed(seed, offset, (uint64_t)k);
+        u_out[k] = U * T;           /* fl32(U * T) */
+    }
+}
+
 int64_t oracle_lower_bound_f32(const float* c, int64_t n, float u) {
     int64_t lo = 0, hi = n; /* first i in [lo,hi) with c[i] >= u */
     while (lo < hi) {
@@ -193,10 +204,11 @@ int64_t oracle_tree_descend(const float* tree, int64_t cap_pow2, float u) {
 }
 
 void oracle_sample_tree(const float* tree, int64_t cap_pow2, int64_t B, uint64_t seed,
-                        uint64_t offset, const float* u01, int32_t* idx, float* u_out) {
+                        uint64_t offset, const float* u01, int iid, int32_t* idx, float* u_out) {
     float T = tree[1];
     float* u = (float*)malloc((size_t)B * sizeof(float));
-    oracle_thresholds(B, seed, offset, u01, T, u);
+    if (iid) oracle_thresholds_iid(B, seed, offset, u01, T, u);
+    else oracle_thresholds(B, seed, offset, u01, T, u);
     for (int64_t k = 0; k < B; ++k) {
         idx[k] = (int32_t)oracle_tree_descend(tree, cap_pow2, u[k]);
         if (u_out) u_out[k] = u[k];

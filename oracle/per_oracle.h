@@ -56,6 +56,10 @@ void oracle_cdf64(const float* p, int64_t n, double alpha, double* C);
  * (0,1] from Philox (or u01[k] when u01 != NULL).  fp32 throughout. */
 void oracle_thresholds(int64_t B, uint64_t seed, uint64_t offset, const float* u01,
                        float T, float* u_out);
+/* i.i.d. thresholds u_k = fl32(U_k * T), U_k as above (foxhunt "CUDA
+ * Kernels": one threshold per sampling thread, uniform over the total). */
+void oracle_thresholds_iid(int64_t B, uint64_t seed, uint64_t offset, const float* u01,
+                           float T, float* u_out);
 /* searchsorted(right=False) == lower_bound; returns n-1 when every c[i] < u
  * (the clamp of [PF]). */
 int64_t oracle_lower_bound_f32(const float* c, int64_t n, float u);
@@ -81,9 +85,10 @@ void oracle_tree_build(const float* leaves, int64_t cap_pow2, float* tree);
  * if (u > L and R > 0) { u = fl32(u - L); j = 2j+1 } else j = 2j.
  * Returns the leaf index j - cap_pow2. */
 int64_t oracle_tree_descend(const float* tree, int64_t cap_pow2, float u);
-/* B stratified samples with T = tree[1]. */
+/* B samples with T = tree[1]: stratified thresholds, or with iid != 0 the
+ * i.i.d. thresholds of oracle_thresholds_iid. */
 void oracle_sample_tree(const float* tree, int64_t cap_pow2, int64_t B, uint64_t seed,
-                        uint64_t offset, const float* u01, int32_t* idx, float* u_out);
+                        uint64_t offset, const float* u01, int iid, int32_t* idx, float* u_out);
 
 /* ---- importance-sampling weights --------------------------------------- */
 /* P_i = pa_i / sum_{j<n_valid} pa_j (fp64); w_k = (n_valid * P_{idx_k})^-beta,

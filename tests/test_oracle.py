@@ -309,6 +309,46 @@ def test_tree_random_leaves_against_fp64_search():
     assert len(bad) <= 5
 
 
+def test_tree_iid_closed_forms():
+    """i.i.d. thresholds u_k = fl32(U_k * T) (foxhunt "CUDA Kernels"):
+    all-ones leaves with U_k = (k + 1/2)/B give u_k = k + 1/2 and leaf k;
+    U = 1 gives u = T and the last non-zero leaf; the smallest Philox U
+    (2^-24) gives the first non-zero leaf."""
+    cap = 1024
+    t = oracle.tree_build(np.ones(cap, np.float32))
+    B = cap
+    U = ((np.arange(B) + 0.5) / B).astype(np.float32)
+    u = oracle.thresholds_iid(B, 0, 0, float(t[1]), u01=U)
+    assert np.array_equal(u, (np.arange(B) + 0.5).astype(np.float32))
+    idx, _ = oracle.sample_tree(t, B, 0, 0, u01=U, iid=True)
+    assert np.array_equal(idx, np.arange(B))
+    leaves = np.zeros(cap, np.float32)
+    leaves[[3, 100, 700]] = [2.0, 5.0, 1.0]
+    t = oracle.tree_build(leaves)
+    ends = np.array([1.0, 2.0 ** -24], np.float32)
+    idx, u = oracle.sample_tree(t, 2, 0, 0, u01=ends, iid=True)
+    assert u[0] == t[1] and idx.tolist() == [700, 3]
+
+
+def test_tree_iid_thresholds_are_uniform_over_the_total():
+    """Philox i.i.d. thresholds lie in (0, T], are not sorted, and the
+    sampled frequencies match p_i / total (65,536 draws, 5 sigma)."""
+    leaves = np.array([1.0, 3.0, 0.0, 6.0, 2.0, 0.0, 4.0, 8.0], np.float32)
+    t = oracle.tree_build(leaves)
+    B = 1 << 16
+    idx, u = oracle.sample_tree(t, B, 42, 7, iid=True)
+    assert np.all(u > 0) and np.all(u <= t[1])
+    assert np.any(np.diff(u) < 0)
+    assert np.all(leaves[idx] > 0)
+    p = leaves / leaves.sum()
+    freq = np.bincount(idx, minlength=leaves.size) / B
+    assert np.all(np.abs(freq - p) <= 5 * np.sqrt(p * (1 - p) / B) + 1e-12)
+    # stratified thresholds of the same draws differ: one per stratum
+    _, us = oracle.sample_tree(t, B, 42, 7)
+    k = np.arange(B)
+    assert np.all((us > k * t[1] / B * (1 - 1e-6)) & (us <= (k + 1) * t[1] / B * (1 + 1e-6)))
+
+
 # ------------------------------------------------------------ IS weights ----
 
 def test_is_weights_closed_forms():
