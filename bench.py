@@ -387,6 +387,18 @@ def extras(per, torch, dev, peak):
                                       "timing": "graph of 8 steps between events, per step"}
     if per.per_check(ctx.handle) != 0:
         out["tree_sample_update_step"]["status"] = "device status not clean"
+
+    def iid_steps():  # the same step with i.i.d. thresholds (mode PER_TREE | PER_IID)
+        for s in range(8):
+            per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE | per.PER_IID, tidx)
+            per.per_update(ctx.handle, upd_idx[s], upd_p[s])
+    iid_steps()
+    us_i = time_graph(graph_of(iid_steps), 50, flush_l2=False, per_replay=8)
+    out["tree_iid_sample_update_step"] = {"capacity": cap, "B": T["B"], "us": round(us_i, 2),
+                                          "l2": "warm (the 4 MiB tree stays resident across steps)",
+                                          "timing": "graph of 8 steps between events, per step"}
+    if per.per_check(ctx.handle) != 0:
+        out["tree_iid_sample_update_step"]["status"] = "device status not clean"
     ctx.close()
 
     R = workloads.RESAMPLE

@@ -21,6 +21,7 @@ from . import _build
 PER_OK = 0
 PER_SCAN = 1
 PER_TREE = 2
+PER_IID = 4  # sampling-mode flag with PER_TREE: i.i.d. thresholds
 STATUS_NAMES = {0: "PER_OK", 1: "PER_ERR_ARG", 2: "PER_ERR_CUDA", 3: "PER_ERR_OOM", 4: "PER_ERR_TIMEOUT",
                 5: "PER_ERR_EMPTY", 6: "PER_ERR_STATE", 7: "PER_ERR_RANGE", 8: "PER_ERR_VALUE"}
 

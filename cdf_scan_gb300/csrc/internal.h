@@ -84,7 +84,7 @@ void per_note_launch(int n = 1);
 per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s);
 per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
                               int32_t* out, cudaStream_t s);
-per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01, bool iid,
                               int32_t* out, cudaStream_t s);
 per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta, float* out,
                              cudaStream_t s);

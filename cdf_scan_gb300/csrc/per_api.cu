@@ -181,9 +181,9 @@ per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, i
         if (ctx->size < 1) return PER_ERR_EMPTY;
         return launch_sample_scan(ctx, B, seed, offset, d_u01, d_out_idx, s);
     }
-    if (mode == static_cast<int>(PER_TREE)) {
+    if (mode == static_cast<int>(PER_TREE) || mode == static_cast<int>(PER_TREE | PER_IID)) {
         if (!(ctx->flags & PER_TREE)) return PER_ERR_STATE;
-        return launch_sample_tree(ctx, B, seed, offset, d_u01, d_out_idx, s);
+        return launch_sample_tree(ctx, B, seed, offset, d_u01, (mode & PER_IID) != 0, d_out_idx, s);
     }
     return PER_ERR_ARG;
 }
@@ -213,7 +213,9 @@ per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_p
                     float* d_out_w, void* stream) {
     if (!ctx || n_upd < 0 || (n_upd > 0 && (!d_upd_idx || !d_upd_prio))) return PER_ERR_ARG;
     if (B < 1 || B > (1 << 24) || !d_out_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f) return PER_ERR_ARG;
-    if (mode != static_cast<int>(PER_SCAN) && mode != static_cast<int>(PER_TREE)) return PER_ERR_ARG;
+    if (mode != static_cast<int>(PER_SCAN) && mode != static_cast<int>(PER_TREE) &&
+        mode != static_cast<int>(PER_TREE | PER_IID))
+        return PER_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (mode == static_cast<int>(PER_SCAN) && ctx->flags == PER_SCAN && ctx->size >= 1) {
         const per_status st =

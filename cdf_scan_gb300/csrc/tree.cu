@@ -41,6 +41,7 @@ struct TreeSampleParams {
     int B;
     uint64_t seed, offset;
     const float* __restrict__ u01;
+    bool iid;  // thresholds U_k * T (foxhunt "CUDA Kernels") instead of stratified
     int32_t* __restrict__ out;
     int* status;
 };
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(THREADS) sample_tree_kernel(TreeSampleParams P
     float u = 0.f;
     if (k < P.B) {
         const float U = P.u01 ? P.u01[k] : u01_open_closed(P.seed, P.offset + static_cast<uint64_t>(k));
-        u = stratified_threshold(k, U, static_cast<float>(P.B), T);
+        u = P.iid ? __fmul_rn(U, T) : stratified_threshold(k, U, static_cast<float>(P.B), T);
     }
     __syncthreads();  // barrier initialised before anyone waits on it
     if (!mbar_wait_bounded(&s_bar, 0)) atomicOr(P.status, ST_TIMEOUT);
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kSmallThreads) small_update_kernel(const int32
 
 // ======================================================== host launchers ====
 
-per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
+per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01, bool iid,
                               int32_t* out, cudaStream_t s) {
     TreeSampleParams P;
     P.tree = ctx->tree;
@@ -452,6 +453,7 @@ per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
     P.seed = seed;
     P.offset = offset;
     P.u01 = u01;
+    P.iid = iid;
     P.out = out;
     P.status = ctx->status;
     const size_t smem = std::max<size_t>(16, (static_cast<size_t>(2) << P.staged_levels) * sizeof(float));

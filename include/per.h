@@ -69,6 +69,7 @@ typedef enum {
 /* Structures kept by a context (flags of per_create) and sampling modes. */
 #define PER_SCAN 1u /* raw priorities + CDF built by per_build_cdf (PR #615) */
 #define PER_TREE 2u /* sum segment tree of priority^alpha (foxhunt) */
+#define PER_IID 4u  /* sampling-mode flag, with PER_TREE: i.i.d. thresholds (foxhunt "CUDA Kernels") */
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* per_status_str(per_status s);
@@ -161,6 +162,9 @@ per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, fl
 /*
  * per_sample -- draw B stratified samples (1 <= B <= 2^24):
  *   u_k = fl32(fl32(fl32(k + U_k) / B) * T),  U_k in (0, 1],
+ * or, with mode PER_TREE | PER_IID, B independent samples (foxhunt "CUDA
+ * Kernels": one threshold per sampling thread, uniform over the total):
+ *   u_k = fl32(U_k * T),
  * U_k = ((x >> 8) + 1) * 2^-24 with x the first word of Philox4x32-10 at
  * counter (offset + k, 0, 0) under key seed, or U_k = d_u01[k] when d_u01 is
  * not NULL (values in (0,1]).
@@ -173,6 +177,8 @@ per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, fl
  */
 per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, int mode,
                       const float* d_u01, int32_t* d_out_idx, void* stream);
+/* (PER_IID with PER_SCAN is PER_ERR_ARG: the scan path's staged windows rely
+ * on sorted thresholds.) */
 
 /*
  * per_is_weights -- importance-sampling weights for sampled items d_idx[0..B):

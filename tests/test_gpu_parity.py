@@ -364,3 +364,26 @@ def test_negative_priority_is_reported():
     per.per_build_cdf(ctx.handle)
     assert per.per_check(ctx.handle) == 8  # PER_ERR_VALUE
     assert per.per_check(ctx.handle) == 0  # cleared
+
+
+# ---------------------------------------------------- i.i.d. tree sampling ---
+
+@pytest.mark.parametrize("cap,B", [(1 << 19, 1024), (4096, 1), (1000, 65536)])
+def test_tree_iid_sampling_matches_oracle(cap, B):
+    """mode PER_TREE | PER_IID: thresholds U_k * T, one per sample (foxhunt
+    "CUDA Kernels"); indices bit-exact against the oracle's descent of the
+    GPU's own tree, with Philox draws and with a u01 override."""
+    p = workloads.lognormal(cap, workloads.rng(120, cap))
+    ctx = make_ctx(p, 0.6, TREE)
+    tree = host(per.read_tree(ctx.handle))
+    out = torch.empty(B, dtype=torch.int32, device="cuda")
+    per.per_sample(ctx.handle, B, 13, 77, TREE | per.PER_IID, out)
+    want, u = oracle.sample_tree(tree, B, 13, 77, iid=True)
+    assert np.array_equal(host(out), want)
+    assert np.all(p[host(out)] > 0)
+    U = workloads.uniform_open_closed(B, workloads.rng(121, B))
+    per.per_sample(ctx.handle, B, 0, 0, TREE | per.PER_IID, out, u01=dev(U))
+    assert np.array_equal(host(out), oracle.sample_tree(tree, B, 0, 0, u01=U, iid=True)[0])
+    with pytest.raises(per.PerError):
+        per.per_sample(ctx.handle, B, 0, 0, SCAN | per.PER_IID, out)
+    assert per.per_check(ctx.handle) == 0
