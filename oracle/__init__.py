@@ -83,6 +83,7 @@ def _load():
         "oracle_resample_row": (None, [_f32p, _i64, ctypes.c_float, _vp, _i32p, _vp]),
         "oracle_resample_row_on_cdf": (None, [_f32p, _i64, ctypes.c_float, _i32p]),
         "oracle_resample": (None, [_f32p, _i64, _i64, _u64, _u64, _vp, _i32p]),
+        "oracle_resample_gather": (None, [_f32p, _i64, _i64, _i64, _i32p, _f32p, _vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -268,3 +269,15 @@ def resample(lw, seed: int, offset: int, u_rows=None) -> np.ndarray:
     idx = np.empty((rows, P), np.int32)
     _load().oracle_resample(lw, rows, P, seed, offset, ptr, idx)
     return idx
+
+
+def resample_gather(state, idx):
+    """out_state[b, j] = state[b, idx[b, j]], out_logw = fl32(-log P) (the
+    particle filter's gather and weight reset)."""
+    state = np.ascontiguousarray(state, np.float32)
+    rows, P, D = state.shape
+    idx = np.ascontiguousarray(idx, np.int32)
+    out = np.empty_like(state)
+    lw = np.empty((rows, P), np.float32)
+    _load().oracle_resample_gather(state, rows, P, D, idx, out, lw.ctypes.data_as(ctypes.c_void_p))
+    return out, lw

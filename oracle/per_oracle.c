@@ -270,3 +270,19 @@ void oracle_resample(const float* lw, int64_t rows, int64_t P, uint64_t seed, ui
         oracle_resample_row(lw + b * P, P, U, NULL, idx + b * P, NULL);
     }
 }
+
+/* The rest of the particle-filter resample step (POPCORNBENCH particle
+ * filter, reference forward: the resampled particles are gathered along the
+ * particle axis and the log-weights of the new set are all -log P):
+ * out_state[b][j][:] = state[b][idx[b][j]][:], out_logw[b][j] = fl32(-log P). */
+void oracle_resample_gather(const float* state, int64_t rows, int64_t P, int64_t D, const int32_t* idx,
+                            float* out_state, float* out_logw) {
+    const float reset = (float)(-log((double)P));
+    for (int64_t b = 0; b < rows; ++b) {
+        for (int64_t j = 0; j < P; ++j) {
+            const int64_t i = idx[b * P + j];
+            for (int64_t d = 0; d < D; ++d) out_state[(b * P + j) * D + d] = state[(b * P + i) * D + d];
+            if (out_logw) out_logw[b * P + j] = reset;
+        }
+    }
+}

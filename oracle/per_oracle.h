@@ -107,6 +107,12 @@ void oracle_resample_row_on_cdf(const float* c, int64_t P, float U, int32_t* idx
 /* rows x P, U_b = u_rows[b] or Philox (offset + b) in [0,1). */
 void oracle_resample(const float* lw, int64_t rows, int64_t P, uint64_t seed, uint64_t offset,
                      const float* u_rows, int32_t* idx);
+/* Gather of the resampled particles and reset of the log-weights (the rest
+ * of the particle filter's resample step): state and out_state are
+ * float32[rows][P][D], idx int32[rows][P]; out_logw (may be NULL)
+ * float32[rows][P] = fl32(-log P). */
+void oracle_resample_gather(const float* state, int64_t rows, int64_t P, int64_t D, const int32_t* idx,
+                            float* out_state, float* out_logw);
 
 #ifdef __cplusplus
 }

@@ -407,3 +407,23 @@ def test_resample_rows_monotone_and_match_per_row():
         diff = np.nonzero(on32 != idx[b])[0]
         for j in diff:
             assert np.min(np.abs(C - float(u[j]))) <= 2e-6
+
+
+def test_resample_gather_pins():
+    """The particle filter's gather and log-weight reset: equal weights keep
+    every particle in place; a one-hot row copies the hot particle
+    everywhere; the reset weight is -log P rounded once to fp32."""
+    rows, P, D = 3, 1024, 4
+    g = workloads.rng(130, 1)
+    state = g.standard_normal((rows, P, D)).astype(np.float32)
+    lw = np.zeros((rows, P), np.float32)
+    lw[1] = -np.inf
+    lw[1, 17] = 0.0
+    idx = oracle.resample(lw, 5, 9)
+    assert np.array_equal(idx[0], np.arange(P)) and np.all(idx[1] == 17)
+    out, nlw = oracle.resample_gather(state, idx)
+    assert np.array_equal(out[0], state[0])
+    assert np.array_equal(out[1], np.broadcast_to(state[1, 17], (P, D)))
+    assert np.array_equal(out[2], state[2, idx[2]])
+    assert np.all(nlw == np.float32(-math.log(P)))
+    assert nlw[0, 0] == np.float32(-6.931471805599453)
