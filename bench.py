@@ -411,6 +411,19 @@ def extras(per, torch, dev, peak):
                        "gbs": round(rbytes / (us_r * 1e-6) / 1e9, 1),
                        "frac_of_measured_peak": round(rbytes / (us_r * 1e-6) / 1e9 / peak, 4),
                        "l2": "flushed before each rep"}
+    # the whole particle-filter resample step with D = 4 states per particle:
+    # indices, gathered states and the reset log-weights in one launch
+    D = 4
+    state = torch.randn((R["rows"], R["P"], D), generator=torch.Generator(device=dev).manual_seed(6), device=dev)
+    out_state = torch.empty_like(state)
+    out_lw = torch.empty_like(logw)
+    per.per_resample_step(logw, state, 6, 0, ridx, out_state, out_lw)
+    us_s = time_graph(graph_of(lambda: per.per_resample_step(logw, state, 6, 0, ridx, out_state, out_lw)), 20)
+    sbytes = R["rows"] * R["P"] * (4 + 4 + 4 + 8 * D)  # logw in, idx out, logw out, states in and out
+    out["resample_step_d4"] = {"rows": R["rows"], "P": R["P"], "D": D, "us": round(us_s, 2),
+                               "gbs": round(sbytes / (us_s * 1e-6) / 1e9, 1),
+                               "frac_of_measured_peak": round(sbytes / (us_s * 1e-6) / 1e9 / peak, 4),
+                               "l2": "flushed before each rep"}
     return out
 
 

@@ -51,6 +51,7 @@ SIGNATURES = {
     "per_tree_ptr": (_vp, [_vp]),
     "per_check": (ctypes.c_int, [_vp, _vp]),
     "per_resample": (ctypes.c_int, [_vp, _i32, _i32, _u64, _u64, _vp, _vp, _vp, _vp]),
+    "per_resample_step": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _u64, _u64, _vp, _vp, _vp, _vp, _vp]),
     "per_launch_count": (_u64, []),
 }
 
@@ -225,6 +226,21 @@ def per_resample(logw: torch.Tensor, seed: int, offset: int, out_idx: torch.Tens
         _ptr(out_idx, torch.int32, "out_idx", rows * P), _ptr(out_cdf, torch.float32, "out_cdf", rows * P),
         _stream(stream)))
     return out_idx
+
+
+def per_resample_step(logw: torch.Tensor, state: torch.Tensor, seed: int, offset: int, out_idx: torch.Tensor,
+                      out_state: torch.Tensor, out_logw: torch.Tensor | None = None,
+                      u_rows: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    rows, P = logw.shape
+    D = state.shape[-1]
+    if tuple(state.shape) != (rows, P, D):
+        raise ValueError("state must be [rows, P, D] for logw [rows, P]")
+    _check("per_resample_step", lib().per_resample_step(
+        _ptr(logw, torch.float32, "logw"), _ptr(state, torch.float32, "state"), rows, P, D, seed, offset,
+        _ptr(u_rows, torch.float32, "u_rows", rows), _ptr(out_idx, torch.int32, "out_idx", rows * P),
+        _ptr(out_state, torch.float32, "out_state", rows * P * D), _ptr(out_logw, torch.float32, "out_logw", rows * P),
+        _stream(stream)))
+    return out_state
 
 
 def per_launch_count() -> int:

@@ -96,6 +96,7 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
 per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n, cudaStream_t s);
 per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s);
 per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, uint64_t offset,
-                           const float* u_rows, int32_t* out, float* out_cdf, cudaStream_t s);
+                           const float* u_rows, int32_t* out, float* out_cdf, const float* state, int D,
+                           float* out_state, float* out_logw, float reset, cudaStream_t s);
 
 inline per_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PER_OK : PER_ERR_CUDA; }

@@ -1,6 +1,7 @@
 // per_api.cu -- the C ABI declared in include/per.h: context lifetime,
 // argument checking (before any launch) and dispatch to the kernels.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -291,8 +292,22 @@ per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t s
                         const float* d_u_rows, int32_t* d_out_idx, float* d_out_cdf, void* stream) {
     if (!d_logw || !d_out_idx || rows < 1 || P < 4 || (P & 3) != 0 || P > (1 << 23)) return PER_ERR_ARG;
     if (!aligned16(d_logw) || !aligned16(d_out_idx) || (d_out_cdf && !aligned16(d_out_cdf))) return PER_ERR_ARG;
-    return launch_resample(d_logw, rows, P, seed, offset, d_u_rows, d_out_idx, d_out_cdf,
-                           static_cast<cudaStream_t>(stream));
+    return launch_resample(d_logw, rows, P, seed, offset, d_u_rows, d_out_idx, d_out_cdf, nullptr, 0, nullptr,
+                           nullptr, 0.f, static_cast<cudaStream_t>(stream));
+}
+
+per_status per_resample_step(const float* d_logw, const float* d_state, int32_t rows, int32_t P, int32_t D,
+                             uint64_t seed, uint64_t offset, const float* d_u_rows, int32_t* d_out_idx,
+                             float* d_out_state, float* d_out_logw, void* stream) {
+    if (!d_logw || !d_out_idx || !d_state || !d_out_state || rows < 1 || P < 4 || (P & 3) != 0 || P > (1 << 23) ||
+        D < 1 || D > 4096)
+        return PER_ERR_ARG;
+    if (!aligned16(d_logw) || !aligned16(d_out_idx) || !aligned16(d_state) || !aligned16(d_out_state) ||
+        (d_out_logw && !aligned16(d_out_logw)))
+        return PER_ERR_ARG;
+    const float reset = static_cast<float>(-std::log(static_cast<double>(P)));
+    return launch_resample(d_logw, rows, P, seed, offset, d_u_rows, d_out_idx, nullptr, d_state, D, d_out_state,
+                           d_out_logw, reset, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -36,12 +36,19 @@ constexpr int kChunk = kThreads * kLane;   // 4096
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct ResampleParams {
-    const float* __restrict__ logw;
+    const float* logw;  // may also be out_logw
     int P;
     uint64_t seed, offset;
     const float* __restrict__ u_rows;
     int32_t* __restrict__ out;
     float* __restrict__ out_cdf;
+    // the rest of the particle filter's resample step (or null): the
+    // resampled particles' states and the reset log-weights
+    const float* __restrict__ state;  // [rows][P][D]
+    int D;
+    float* __restrict__ out_state;    // [rows][P][D]
+    float* out_logw;                  // [rows][P] (may be logw itself)
+    float reset;                      // fl32(-log P)
 };
 
 // Threshold u_j = fl32(fl32(j + U) / P); for a power of two P the division is
@@ -295,16 +302,45 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
                 for (int e = 0; e < kLane; ++e)
                     if (j0 + e >= j_lo && j0 + e < j_hi) orow[j0 + e] = v[e];
             }
+            if (R.out_state) {
+                // the block's particles in shared memory, then their states
+                // copied by consecutive threads for consecutive outputs
+                // (coalesced: neighbouring outputs hold neighbouring particles)
+                __syncthreads();  // every thread has read s_stage
+                *reinterpret_cast<int4*>(s_stage + t0) = make_int4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
+                __syncthreads();
+                const int D = R.D;
+                const float* srow = R.state + static_cast<size_t>(b) * P * D;
+                float* drow = R.out_state + static_cast<size_t>(b) * P * D;
+                for (int t = threadIdx.x; t < kChunk; t += kThreads) {
+                    const int j = b0 + t;
+                    if (j < j_lo || j >= j_hi) continue;
+                    const int i = s_stage[t];
+                    if ((D & 3) == 0) {
+                        for (int d = 0; d < D; d += 4)
+                            st_f4(drow + static_cast<size_t>(j) * D + d, ld_f4(srow + static_cast<size_t>(i) * D + d));
+                    } else {
+                        for (int d = 0; d < D; ++d) drow[static_cast<size_t>(j) * D + d] = srow[static_cast<size_t>(i) * D + d];
+                    }
+                }
+            }
             started = all;
             __syncthreads();  // s_stage and s_wmax are reused by the next block
         }
+    }
+    if (R.out_logw) {  // every read of the row's log-weights is done: the reset may overwrite them
+        float* lrow = R.out_logw + static_cast<size_t>(b) * P;
+        const float4 r4 = make_float4(R.reset, R.reset, R.reset, R.reset);
+        for (int i = threadIdx.x * 4; i < P; i += kThreads * 4) st_f4(lrow + i, r4);
     }
 }
 
 }  // namespace
 
 per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, uint64_t offset,
-                           const float* u_rows, int32_t* out, float* out_cdf, cudaStream_t s) {
+                           const float* u_rows, int32_t* out, float* out_cdf, const float* state, int D,
+                           float* out_state, float* out_logw, float reset, cudaStream_t s) {
     ResampleParams R;
     R.logw = logw;
     R.P = P;
@@ -313,6 +349,11 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     R.u_rows = u_rows;
     R.out = out;
     R.out_cdf = out_cdf;
+    R.state = state;
+    R.D = D;
+    R.out_state = out_state;
+    R.out_logw = out_logw;
+    R.reset = reset;
     resample_kernel<<<static_cast<unsigned>(rows), kThreads, 0, s>>>(R);
     per_note_launch();
     return cuda_status(cudaGetLastError());

@@ -263,6 +263,22 @@ per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t s
                         uint64_t offset, const float* d_u_rows, int32_t* d_out_idx,
                         float* d_out_cdf, void* stream);
 
+/*
+ * per_resample_step -- the particle filter's whole resample step
+ * (POPCORNBENCH particle filter, reference forward): per_resample of d_logw
+ * as above (indices to d_out_idx), then the resampled particles' states
+ * gathered along the particle axis,
+ *   d_out_state[b][j][:] = d_state[b][idx_j][:]   (float32[rows][P][D]),
+ * and, when d_out_logw is not NULL, every log-weight of the new set reset to
+ * fl32(-log P) (float32[rows][P]; d_out_logw may be d_logw itself).  One
+ * launch.  d_out_state must not overlap d_state.  All pointers 16-byte
+ * aligned; 1 <= D <= 4096 (D % 4 == 0 copies 16 bytes at a time).  Errors as
+ * per_resample.
+ */
+per_status per_resample_step(const float* d_logw, const float* d_state, int32_t rows, int32_t P, int32_t D,
+                             uint64_t seed, uint64_t offset, const float* d_u_rows, int32_t* d_out_idx,
+                             float* d_out_state, float* d_out_logw, void* stream);
+
 /* Number of this library's kernel launches issued by the calling process so
  * far (host-side counter; used to report launches per benchmark step). */
 uint64_t per_launch_count(void);

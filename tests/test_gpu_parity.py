@@ -387,3 +387,34 @@ def test_tree_iid_sampling_matches_oracle(cap, B):
     with pytest.raises(per.PerError):
         per.per_sample(ctx.handle, B, 0, 0, SCAN | per.PER_IID, out)
     assert per.per_check(ctx.handle) == 0
+
+
+# ------------------------------------------------ particle-filter resample step ---
+
+@pytest.mark.parametrize("rows,P,D", [(4, 1024, 4), (3, 4100, 3), (2, 65536, 8), (5, 256, 1)])
+def test_resample_step_gathers_states_and_resets_weights(rows, P, D):
+    """per_resample_step: the indices of per_resample, the states gathered
+    along the particle axis and the log-weights reset to -log P, bit for bit
+    against the oracle; the reset may be done in place."""
+    lw = workloads.resample_logw(rows=rows, P=P, seed=140 + D)
+    g = workloads.rng(141, P * D)
+    state = g.standard_normal((rows, P, D)).astype(np.float32)
+    d_lw, d_state = dev(lw), dev(state)
+    idx = torch.empty((rows, P), dtype=torch.int32, device="cuda")
+    out_state = torch.empty((rows, P, D), dtype=torch.float32, device="cuda")
+    out_lw = torch.empty((rows, P), dtype=torch.float32, device="cuda")
+    per.per_resample_step(d_lw, d_state, 8, 2, idx, out_state, out_lw)
+    idx2 = torch.empty((rows, P), dtype=torch.int32, device="cuda")
+    cdf = torch.empty((rows, P), dtype=torch.float32, device="cuda")
+    per.per_resample(d_lw, 8, 2, idx2, out_cdf=cdf)
+    got_idx, c = host(idx), host(cdf)
+    assert np.array_equal(got_idx, host(idx2))
+    for b in range(rows):  # bit-exact: the oracle's search of the GPU's CDF
+        assert np.array_equal(got_idx[b], oracle.resample_row_on_cdf(c[b], oracle.u01_closed_open(8, 2, b)))
+    want_state, want_lw = oracle.resample_gather(state, got_idx)
+    assert np.array_equal(host(out_state), want_state)
+    assert np.array_equal(host(out_lw), want_lw)
+    # in place: the log-weights themselves are reset
+    per.per_resample_step(d_lw, d_state, 8, 2, idx, out_state, d_lw)
+    assert np.array_equal(host(idx), got_idx)
+    assert np.array_equal(host(d_lw), want_lw)
