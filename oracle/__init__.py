@@ -84,6 +84,8 @@ def _load():
         "oracle_resample_row_on_cdf": (None, [_f32p, _i64, ctypes.c_float, _i32p]),
         "oracle_resample": (None, [_f32p, _i64, _i64, _u64, _u64, _vp, _i32p]),
         "oracle_resample_gather": (None, [_f32p, _i64, _i64, _i64, _i32p, _f32p, _vp]),
+        "oracle_rank_order": (None, [_f32p, _i64, _i32p]),
+        "oracle_rank_priorities": (None, [_i64, _f32p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -281,3 +283,21 @@ def resample_gather(state, idx):
     lw = np.empty((rows, P), np.float32)
     _load().oracle_resample_gather(state, rows, P, D, idx, out, lw.ctypes.data_as(ctypes.c_void_p))
     return out, lw
+
+
+# ---- rank-based PER --------------------------------------------------------
+
+def rank_order(p) -> np.ndarray:
+    """order[r] = item of rank r + 1 (highest priority first; ties: lower
+    index first)."""
+    p = _f32(p)
+    order = np.empty(p.size, np.int32)
+    _load().oracle_rank_order(p, p.size, order)
+    return order
+
+
+def rank_priorities(n: int) -> np.ndarray:
+    """q[r] = fl32(1 / (r + 1)), the priority of rank r + 1."""
+    q = np.empty(n, np.float32)
+    _load().oracle_rank_priorities(n, q)
+    return q

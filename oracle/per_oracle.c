@@ -286,3 +286,32 @@ void oracle_resample_gather(const float* state, int64_t rows, int64_t P, int64_t
         }
     }
 }
+
+/* ---- rank-based PER ------------------------------------------------------
+ * Named on the segment-tree page ("Non-Goals": rank-based PER is a separate
+ * code path) without a definition; the reading used here is the standard one:
+ * rank 1 is the highest stored priority (ties: lower index first), item i's
+ * priority is 1 / rank(i), and the proportional machinery (p^alpha, CDF,
+ * stratified thresholds, IS weights) runs over ranks. */
+
+static const float* g_rank_p; /* comparator context (the oracle is single-threaded) */
+
+static int rank_cmp(const void* a, const void* b) {
+    const int32_t i = *(const int32_t*)a, j = *(const int32_t*)b;
+    const float pi = g_rank_p[i] + 0.0f, pj = g_rank_p[j] + 0.0f; /* -0 ranks as +0 */
+    if (pi > pj) return -1;
+    if (pi < pj) return 1;
+    return (i > j) - (i < j);
+}
+
+/* order[r] = the item of rank r + 1. */
+void oracle_rank_order(const float* p, int64_t n, int32_t* order) {
+    for (int64_t i = 0; i < n; ++i) order[i] = (int32_t)i;
+    g_rank_p = p;
+    qsort(order, (size_t)n, sizeof(int32_t), rank_cmp);
+}
+
+/* q[r] = fl32(1 / (r + 1)): the priority of rank r + 1. */
+void oracle_rank_priorities(int64_t n, float* q) {
+    for (int64_t r = 0; r < n; ++r) q[r] = 1.0f / (float)(r + 1);
+}

@@ -107,6 +107,12 @@ void oracle_resample_row_on_cdf(const float* c, int64_t P, float U, int32_t* idx
 /* rows x P, U_b = u_rows[b] or Philox (offset + b) in [0,1). */
 void oracle_resample(const float* lw, int64_t rows, int64_t P, uint64_t seed, uint64_t offset,
                      const float* u_rows, int32_t* idx);
+/* Rank-based PER (reading: rank 1 = highest priority, ties by lower index;
+ * priority of rank r is 1/r; then the proportional path over ranks).
+ * order[r] = item of rank r + 1; q[r] = fl32(1 / (r + 1)). */
+void oracle_rank_order(const float* p, int64_t n, int32_t* order);
+void oracle_rank_priorities(int64_t n, float* q);
+
 /* Gather of the resampled particles and reset of the log-weights (the rest
  * of the particle filter's resample step): state and out_state are
  * float32[rows][P][D], idx int32[rows][P]; out_logw (may be NULL)

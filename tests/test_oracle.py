@@ -427,3 +427,22 @@ def test_resample_gather_pins():
     assert np.array_equal(out[2], state[2, idx[2]])
     assert np.all(nlw == np.float32(-math.log(P)))
     assert nlw[0, 0] == np.float32(-6.931471805599453)
+
+
+def test_rank_order_and_priorities_pins():
+    """Rank-based PER (reading of the named path): descending priority,
+    ties by lower index first, -0 ranked as +0; rank priorities 1/r; with
+    alpha = 1 the rank CDF's total is the harmonic number H_n."""
+    p = np.array([0.5, 2.0, 0.5, -0.0, 7.0, 0.0, 2.0], np.float32)
+    assert oracle.rank_order(p).tolist() == [4, 1, 6, 0, 2, 3, 5]
+    g = workloads.rng(150, 1)
+    x = g.permutation(1000).astype(np.float32)
+    assert np.array_equal(oracle.rank_order(x), np.argsort(-x, kind="stable"))
+    q = oracle.rank_priorities(5)
+    assert q.tolist() == [1.0, np.float32(0.5), np.float32(1 / 3), np.float32(0.25), np.float32(0.2)]
+    n = 4096
+    C = oracle.cdf64(oracle.rank_priorities(n), 1.0)
+    H = math.fsum(1.0 / k for k in range(1, n + 1))
+    assert abs(C[-1] - H) <= 2.0 ** -24 * H  # each 1/k rounded once to fp32
+    C0 = oracle.cdf64(oracle.rank_priorities(n), 0.0)
+    assert np.array_equal(C0, np.arange(1, n + 1, dtype=np.float64))  # alpha 0: uniform over ranks
