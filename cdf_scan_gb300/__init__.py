@@ -22,6 +22,7 @@ PER_OK = 0
 PER_SCAN = 1
 PER_TREE = 2
 PER_IID = 4  # sampling-mode flag with PER_TREE: i.i.d. thresholds
+PER_RANK = 8  # rank-based PER: a context flag on its own, and the sampling mode of such a context
 STATUS_NAMES = {0: "PER_OK", 1: "PER_ERR_ARG", 2: "PER_ERR_CUDA", 3: "PER_ERR_OOM", 4: "PER_ERR_TIMEOUT",
                 5: "PER_ERR_EMPTY", 6: "PER_ERR_STATE", 7: "PER_ERR_RANGE", 8: "PER_ERR_VALUE"}
 
@@ -49,6 +50,9 @@ SIGNATURES = {
     "per_priorities_ptr": (_vp, [_vp]),
     "per_cdf_ptr": (_vp, [_vp]),
     "per_tree_ptr": (_vp, [_vp]),
+    "per_rank_build": (ctypes.c_int, [_vp, _vp]),
+    "per_rank_order_ptr": (_vp, [_vp]),
+    "per_rank_cdf_ptr": (_vp, [_vp]),
     "per_check": (ctypes.c_int, [_vp, _vp]),
     "per_resample": (ctypes.c_int, [_vp, _i32, _i32, _u64, _u64, _vp, _vp, _vp, _vp]),
     "per_resample_step": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _u64, _u64, _vp, _vp, _vp, _vp, _vp]),
@@ -156,6 +160,10 @@ def per_build_cdf(ctx: int, stream=None) -> None:
     _check("per_build_cdf", lib().per_build_cdf(ctx, _stream(stream)))
 
 
+def per_rank_build(ctx: int, stream=None) -> None:
+    _check("per_rank_build", lib().per_rank_build(ctx, _stream(stream)))
+
+
 def per_build_cdf_noalloc(prio: torch.Tensor, alpha: float, out_cdf: torch.Tensor,
                           status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Context-free build_cdf whose scratch is a fixed array inside the
@@ -250,18 +258,18 @@ def per_launch_count() -> int:
 # ---- views of context-owned device buffers ----------------------------------
 
 class _DeviceArray:
-    """Zero-copy description of a context-owned float32 device buffer."""
+    """Zero-copy description of a context-owned float32 / int32 device buffer."""
 
-    def __init__(self, ptr: int, n: int):
-        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<f4", "data": (ptr, False),
+    def __init__(self, ptr: int, n: int, typestr: str = "<f4"):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, False),
                                          "version": 3, "strides": None}
 
 
-def _view(ptr: int, n: int) -> torch.Tensor:
-    """Copy n floats from a context-owned device pointer into a new tensor."""
+def _view(ptr: int, n: int, typestr: str = "<f4") -> torch.Tensor:
+    """Copy n elements from a context-owned device pointer into a new tensor."""
     if n == 0:
-        return torch.empty(0, dtype=torch.float32, device="cuda")
-    return torch.as_tensor(_DeviceArray(ptr, n), device="cuda").clone()
+        return torch.empty(0, dtype=torch.float32 if typestr == "<f4" else torch.int32, device="cuda")
+    return torch.as_tensor(_DeviceArray(ptr, n, typestr), device="cuda").clone()
 
 
 def read_cdf(ctx: int) -> torch.Tensor:
@@ -270,6 +278,15 @@ def read_cdf(ctx: int) -> torch.Tensor:
 
 def read_tree(ctx: int) -> torch.Tensor:
     return _view(lib().per_tree_ptr(ctx), 2 * per_capacity_pow2(ctx))
+
+
+def read_rank_order(ctx: int) -> torch.Tensor:
+    """order[r] = the item of rank r + 1 (PER_RANK contexts, after per_rank_build)."""
+    return _view(lib().per_rank_order_ptr(ctx), per_size(ctx), "<i4")
+
+
+def read_rank_cdf(ctx: int) -> torch.Tensor:
+    return _view(lib().per_rank_cdf_ptr(ctx), per_size(ctx))
 
 
 def read_priorities(ctx: int, n: int | None = None) -> torch.Tensor:

@@ -55,6 +55,22 @@ struct per_ctx {
                                       // (float bits) of even and odd calls
     unsigned long long* step_last;    // [kMaxWaveTiles * kDescStride] per_step: tagged last CDF value per tile
     unsigned long long* scan_xsum;    // [kScanXsumWords] chunk sums of the two-pass scan
+
+    // rank-based PER (PER_RANK): the radix sort's buffers, the order it
+    // leaves, and the rank priorities with their CDF (which depend on the
+    // size only, so they are rebuilt only when the size changes)
+    unsigned* rank_keys0;             // [capacity] sort keys (ping)
+    unsigned* rank_keys1;             // [capacity] sort keys (pong)
+    int32_t* rank_vals1;              // [capacity] item indices (pong)
+    int32_t* rank_order;              // [capacity] order[r] = the item of rank r + 1
+    int32_t* rank_of;                 // [capacity] rank_of[order[r]] = r
+    unsigned* rank_counts;            // [kRadixDigits * sort tiles] per-tile digit counts
+    unsigned* rank_totals;            // [kRadixDigits] digit totals of the running pass
+    float* rank_q;                    // [alloc_n] q[r] = 1 / (r + 1)
+    float* rank_cdf;                  // [alloc_n] inclusive prefix sum of q^alpha
+    float* rank_coarse;               // [coarse_n] every 64th rank-CDF value
+    int64_t rank_q_n;                 // size the rank priorities and CDF were built for (0: none)
+    int64_t rank_sorted_n;            // size of the last per_rank_build (0: none)
 };
 
 // Grid-barrier ticket words (per_ctx::tickets).
@@ -77,11 +93,23 @@ constexpr int kDescStride = 16;
 constexpr int64_t kMaxWaveTiles = 1024;
 inline int64_t scan_state_words(int64_t tiles) { return tiles * kDescStride + 1; }
 
+// Rank-based PER: 8-bit radix digits, 4096 keys per sort tile, and at most
+// 2^24 items (4096 tiles).
+constexpr int kRadixDigits = 256;
+constexpr int kRankTile = 4096;
+constexpr int64_t kRankMaxN = int64_t(1) << 24;
+
 // Host-side launch accounting (per_launch_count).
 void per_note_launch(int n = 1);
 
 // Launchers (each returns PER_OK or PER_ERR_CUDA after enqueueing).
 per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s);
+// The same scan over any n priorities p (16-byte aligned, alloc_n-padded)
+// into cdf / coarse, with the context's alpha and scan scratch.
+per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* cdf, float* coarse, cudaStream_t s);
+// Rank-based PER: sort the stored priorities (order, rank_of) and, when the
+// size changed, rebuild the rank priorities and their CDF.
+per_status launch_rank_build(per_ctx* ctx, cudaStream_t s);
 per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
                               int32_t* out, cudaStream_t s);
 per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01, bool iid,

@@ -42,6 +42,16 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->scan_xsum);
     cudaFree(c->step_min);
     cudaFree(c->step_last);
+    cudaFree(c->rank_keys0);
+    cudaFree(c->rank_keys1);
+    cudaFree(c->rank_vals1);
+    cudaFree(c->rank_order);
+    cudaFree(c->rank_of);
+    cudaFree(c->rank_counts);
+    cudaFree(c->rank_totals);
+    cudaFree(c->rank_q);
+    cudaFree(c->rank_cdf);
+    cudaFree(c->rank_coarse);
     std::free(c);
 }
 
@@ -72,7 +82,8 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     if (!out) return PER_ERR_ARG;
     *out = nullptr;
     if (capacity < 1 || capacity > kMaxCapacity || !(alpha >= 0.f) || alpha > 1e30f) return PER_ERR_ARG;
-    if (flags == 0 || (flags & ~(PER_SCAN | PER_TREE)) != 0) return PER_ERR_ARG;
+    if (flags == 0 || (flags & ~(PER_SCAN | PER_TREE | PER_RANK)) != 0) return PER_ERR_ARG;
+    if ((flags & PER_RANK) && (flags != PER_RANK || capacity > kRankMaxN)) return PER_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     per_ctx* c = static_cast<per_ctx*>(std::calloc(1, sizeof(per_ctx)));
     if (!c) return PER_ERR_OOM;
@@ -106,6 +117,20 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
              alloc_zero(&c->step_min, 3, s) == cudaSuccess &&
              alloc_zero(&c->step_last, static_cast<size_t>(kMaxWaveTiles * kDescStride), s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
+    if (ok && (flags & PER_RANK)) {
+        const size_t cap = static_cast<size_t>(capacity);
+        const size_t tiles = (cap + kRankTile - 1) / kRankTile;
+        ok = alloc_zero(&c->rank_keys0, cap, s) == cudaSuccess && alloc_zero(&c->rank_keys1, cap, s) == cudaSuccess &&
+             alloc_zero(&c->rank_vals1, cap, s) == cudaSuccess && alloc_zero(&c->rank_order, cap, s) == cudaSuccess &&
+             alloc_zero(&c->rank_of, cap, s) == cudaSuccess &&
+             alloc_zero(&c->rank_counts, kRadixDigits * tiles, s) == cudaSuccess &&
+             alloc_zero(&c->rank_totals, static_cast<size_t>(kRadixDigits), s) == cudaSuccess &&
+             alloc_zero(&c->rank_q, c->alloc_n, s) == cudaSuccess &&
+             alloc_zero(&c->rank_cdf, c->alloc_n, s) == cudaSuccess &&
+             alloc_zero(&c->rank_coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
+             alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
+             alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess;
+    }
     if (ok) {
         // epochs start at 1 (0 marks "never written"); the IS-weight minimum
         // starts above every non-negative float.
@@ -146,6 +171,8 @@ int64_t per_capacity_pow2(const per_ctx* ctx) { return ctx ? ctx->cap_pow2 : -1;
 const float* per_priorities_ptr(const per_ctx* ctx) { return ctx ? ctx->prio : nullptr; }
 const float* per_cdf_ptr(const per_ctx* ctx) { return ctx ? ctx->cdf : nullptr; }
 const float* per_tree_ptr(const per_ctx* ctx) { return ctx ? ctx->tree : nullptr; }
+const int32_t* per_rank_order_ptr(const per_ctx* ctx) { return ctx ? ctx->rank_order : nullptr; }
+const float* per_rank_cdf_ptr(const per_ctx* ctx) { return ctx ? ctx->rank_cdf : nullptr; }
 
 per_status per_set_priorities(per_ctx* ctx, const float* d_prio, int64_t n, void* stream) {
     if (!ctx || n < 0 || n > ctx->capacity || (n > 0 && (!d_prio || !aligned16(d_prio)))) return PER_ERR_ARG;
@@ -186,11 +213,25 @@ per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, i
         if (!(ctx->flags & PER_TREE)) return PER_ERR_STATE;
         return launch_sample_tree(ctx, B, seed, offset, d_u01, (mode & PER_IID) != 0, d_out_idx, s);
     }
+    if (mode == static_cast<int>(PER_RANK)) {
+        if (!(ctx->flags & PER_RANK)) return PER_ERR_STATE;
+        if (ctx->size < 1) return PER_ERR_EMPTY;
+        if (ctx->rank_sorted_n != ctx->size) return PER_ERR_STATE;  // per_rank_build first
+        return launch_sample_scan(ctx, B, seed, offset, d_u01, d_out_idx, s);
+    }
     return PER_ERR_ARG;
+}
+
+per_status per_rank_build(per_ctx* ctx, void* stream) {
+    if (!ctx) return PER_ERR_ARG;
+    if (!(ctx->flags & PER_RANK)) return PER_ERR_STATE;
+    if (ctx->size < 1) return PER_ERR_EMPTY;
+    return launch_rank_build(ctx, static_cast<cudaStream_t>(stream));
 }
 
 per_status per_is_weights(per_ctx* ctx, const int32_t* d_idx, int32_t B, float beta, float* d_out_w, void* stream) {
     if (!ctx || B < 1 || !d_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f) return PER_ERR_ARG;
+    if ((ctx->flags & PER_RANK) && (ctx->size < 1 || ctx->rank_sorted_n != ctx->size)) return PER_ERR_STATE;
     return launch_is_weights(ctx, d_idx, B, beta, d_out_w, static_cast<cudaStream_t>(stream));
 }
 
@@ -199,8 +240,9 @@ per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t 
     if (!ctx || B < 1 || B > (1 << 24) || !d_out_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f)
         return PER_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (mode == static_cast<int>(PER_SCAN) && (ctx->flags & PER_SCAN) && ctx->size >= 1 &&
-        !(ctx->flags & PER_TREE)) {
+    const bool scan_only = mode == static_cast<int>(PER_SCAN) && ctx->flags == PER_SCAN;
+    const bool rank = mode == static_cast<int>(PER_RANK) && ctx->flags == PER_RANK && ctx->rank_sorted_n == ctx->size;
+    if ((scan_only || rank) && ctx->size >= 1) {
         const per_status st = launch_sample_scan_weighted(ctx, B, seed, offset, d_u01, beta, d_out_idx, d_out_w, s);
         if (st != PER_ERR_STATE) return st;
     }
@@ -215,7 +257,7 @@ per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_p
     if (!ctx || n_upd < 0 || (n_upd > 0 && (!d_upd_idx || !d_upd_prio))) return PER_ERR_ARG;
     if (B < 1 || B > (1 << 24) || !d_out_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f) return PER_ERR_ARG;
     if (mode != static_cast<int>(PER_SCAN) && mode != static_cast<int>(PER_TREE) &&
-        mode != static_cast<int>(PER_TREE | PER_IID))
+        mode != static_cast<int>(PER_TREE | PER_IID) && mode != static_cast<int>(PER_RANK))
         return PER_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (mode == static_cast<int>(PER_SCAN) && ctx->flags == PER_SCAN && ctx->size >= 1) {
@@ -227,6 +269,10 @@ per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_p
     if (st != PER_OK) return st;
     if (ctx->flags & PER_SCAN) {
         st = per_build_cdf(ctx, stream);
+        if (st != PER_OK) return st;
+    }
+    if (ctx->flags & PER_RANK) {
+        st = per_rank_build(ctx, stream);
         if (st != PER_OK) return st;
     }
     return per_sample_weighted(ctx, B, seed, offset, mode, d_u01, beta, d_out_idx, d_out_w, stream);
@@ -243,6 +289,11 @@ per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream) {
         if (!(ctx->flags & PER_SCAN)) return PER_ERR_STATE;
         if (ctx->size < 1) return PER_ERR_EMPTY;
         src = ctx->cdf + ctx->size - 1;
+    } else if (mode == static_cast<int>(PER_RANK)) {
+        if (!(ctx->flags & PER_RANK)) return PER_ERR_STATE;
+        if (ctx->size < 1) return PER_ERR_EMPTY;
+        if (ctx->rank_q_n != ctx->size) return PER_ERR_STATE;
+        src = ctx->rank_cdf + ctx->size - 1;
     } else {
         return PER_ERR_ARG;
     }
@@ -260,6 +311,11 @@ per_status per_total_host(per_ctx* ctx, int mode, float* h_out, void* stream) {
         if (!(ctx->flags & PER_SCAN)) return PER_ERR_STATE;
         if (ctx->size < 1) return PER_ERR_EMPTY;
         src = ctx->cdf + ctx->size - 1;
+    } else if (mode == static_cast<int>(PER_RANK)) {
+        if (!(ctx->flags & PER_RANK)) return PER_ERR_STATE;
+        if (ctx->size < 1) return PER_ERR_EMPTY;
+        if (ctx->rank_q_n != ctx->size) return PER_ERR_STATE;
+        src = ctx->rank_cdf + ctx->size - 1;
     } else {
         return PER_ERR_ARG;
     }

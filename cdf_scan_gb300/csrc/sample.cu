@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
 #pragma unroll
     for (int s = 0; s < SPT; ++s) {
         const int k = k0 + threadIdx.x + s * THREADS;
-        if (k < kend) P.out[k] = res[s];
+        if (k < kend) P.out[k] = sample_item(P, res[s]);
     }
 }
 
@@ -218,7 +218,9 @@ per_status launch_coarse(const SampleParams& P, double ratio, cudaStream_t s) {
 
 SampleParams sample_params(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01, int32_t* out) {
     SampleParams P = {};
-    P.cdf = ctx->cdf;
+    const bool rank = (ctx->flags & PER_RANK) != 0;  // draw ranks from the rank CDF, write their items
+    P.cdf = rank ? ctx->rank_cdf : ctx->cdf;
+    P.order = rank ? ctx->rank_order : nullptr;
     P.n = static_cast<int>(ctx->size);
     P.B = B;
     P.seed = seed;
@@ -226,12 +228,13 @@ SampleParams sample_params(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, 
     P.u01 = u01;
     P.out = out;
     P.status = ctx->status;
-    P.coarse = ctx->coarse;
+    P.coarse = rank ? ctx->rank_coarse : ctx->coarse;
     return P;
 }
 
 bool coarse_fits(const per_ctx* ctx) {
-    return ctx->coarse && (ctx->size + kCoarseStride - 1) / kCoarseStride <= kCoarseCap;
+    const float* coarse = (ctx->flags & PER_RANK) ? ctx->rank_coarse : ctx->coarse;
+    return coarse && (ctx->size + kCoarseStride - 1) / kCoarseStride <= kCoarseCap;
 }
 
 }  // namespace
@@ -263,7 +266,7 @@ per_status launch_sample_scan_weighted(per_ctx* ctx, int B, uint64_t seed, uint6
                                        float beta, int32_t* out, float* out_w, cudaStream_t s) {
     if (!coarse_fits(ctx)) return PER_ERR_STATE;
     SampleParams P = sample_params(ctx, B, seed, offset, u01, out);
-    P.prio = ctx->prio;
+    P.prio = (ctx->flags & PER_RANK) ? ctx->rank_q : ctx->prio;  // weights of the drawn ranks
     P.alpha = ctx->alpha;
     P.alpha_one = ctx->alpha == 1.0f;
     P.beta = beta;

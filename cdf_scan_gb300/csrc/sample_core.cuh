@@ -32,7 +32,11 @@ struct SampleParams {
     float* slots;                // [gridDim.x] per-CTA minima
     unsigned long long* ticket;  // grid-barrier ticket
     unsigned* min_word;          // or one word every CTA atomicMin's (float bits; +inf on entry)
+    // rank-based PER: the CDF is over ranks and out[k] = order[rank] (nullptr: out[k] = the index drawn)
+    const int32_t* __restrict__ order;
 };
+
+__device__ __forceinline__ int32_t sample_item(const SampleParams& P, int r) { return P.order ? __ldg(P.order + r) : r; }
 
 __device__ __forceinline__ float draw_u(const SampleParams& P, int k) {
     return P.u01 ? P.u01[k] : u01_open_closed(P.seed, P.offset + static_cast<uint64_t>(k));
@@ -161,7 +165,7 @@ __device__ __forceinline__ void coarse_sample(const SampleParams& P, int k0, int
 #pragma unroll
         for (int s = 0; s < SPT; ++s) {
             const int k = k0 + threadIdx.x + s * THREADS;
-            if (k < kend) P.out[k] = res[s];
+            if (k < kend) P.out[k] = sample_item(P, res[s]);
         }
     }
     if (WEIGHTS) {

@@ -649,21 +649,25 @@ per_status scan_dispatch(ScanParams P, int num_sms, cudaStream_t s) {
 }  // namespace
 
 per_status launch_build_cdf(per_ctx* ctx, cudaStream_t s) {
+    return launch_build_cdf_of(ctx, ctx->prio, ctx->size, ctx->cdf, ctx->coarse, s);
+}
+
+per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* cdf, float* coarse, cudaStream_t s) {
     ScanParams P;
-    P.p = ctx->prio;
-    P.cdf = ctx->cdf;
-    P.n = ctx->size;
+    P.p = p;
+    P.cdf = cdf;
+    P.n = n;
     P.alpha = ctx->alpha;
     P.alpha_one = ctx->alpha == 1.0f;
     P.pow_mode = ctx->alpha == 1.0f ? 1 : (ctx->alpha == 0.0f ? 2 : 0);
     P.pow_lim = pow_limit(ctx->alpha);
-    P.cdf_v8 = (reinterpret_cast<uintptr_t>(ctx->cdf) & 31u) == 0;
+    P.cdf_v8 = (reinterpret_cast<uintptr_t>(cdf) & 31u) == 0;
     P.desc = ctx->scan_desc;
     P.desc_tiles = ctx->scan_desc_tiles;
     P.ctrs = ctx->ctrs;
     P.status = ctx->status;
     P.num_tiles = 0;
-    P.coarse = ctx->coarse;
+    P.coarse = coarse;
     P.xsum = ctx->scan_xsum;
     P.ticket = ctx->tickets + TK_SCAN;
     P.seg_tiles = 0;

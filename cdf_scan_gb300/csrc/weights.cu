@@ -27,6 +27,7 @@ struct IswParams {
     int B;
     const float* __restrict__ leaves;  // tree leaves (pa) or nullptr
     const float* __restrict__ prio;    // raw priorities when leaves == nullptr
+    const int32_t* __restrict__ rank_of;  // rank-based PER: pa = q[rank_of[i]]^alpha (prio = q), else nullptr
     float alpha;
     bool alpha_one;
     float beta;
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kThreads) is_weights_kernel(IswParams P) {
         } else if (P.leaves) {
             pa = __ldg(P.leaves + i);
         } else {
-            pa = pow_accurate(__ldg(P.prio + i), P.alpha, P.alpha_one);
+            pa = pow_accurate(__ldg(P.prio + (P.rank_of ? __ldg(P.rank_of + i) : i)), P.alpha, P.alpha_one);
         }
         P.out[k] = pa;
         m = fminf(m, pa);
@@ -94,11 +95,13 @@ per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta
     P.B = B;
     const bool tree = (ctx->flags & PER_TREE) != 0;
     P.leaves = tree ? ctx->tree + ctx->cap_pow2 : nullptr;
-    P.prio = ctx->prio;
+    const bool rank = (ctx->flags & PER_RANK) != 0;
+    P.prio = rank ? ctx->rank_q : ctx->prio;
+    P.rank_of = rank ? ctx->rank_of : nullptr;
     P.alpha = ctx->alpha;
     P.alpha_one = ctx->alpha == 1.0f;
     P.beta = beta;
-    P.capacity = ctx->capacity;
+    P.capacity = rank ? ctx->rank_sorted_n : ctx->capacity;  // only the sorted items have a rank
     P.out = out;
     P.slots = ctx->slots;
     P.ticket = ctx->tickets + TK_ISW;

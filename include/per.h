@@ -70,6 +70,7 @@ typedef enum {
 #define PER_SCAN 1u /* raw priorities + CDF built by per_build_cdf (PR #615) */
 #define PER_TREE 2u /* sum segment tree of priority^alpha (foxhunt) */
 #define PER_IID 4u  /* sampling-mode flag, with PER_TREE: i.i.d. thresholds (foxhunt "CUDA Kernels") */
+#define PER_RANK 8u /* rank-based PER: priority 1/rank (foxhunt "Non-Goals"); a context flag on its own */
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* per_status_str(per_status s);
@@ -78,7 +79,8 @@ const char* per_status_str(per_status s);
  * per_create -- allocate a context for `capacity` items (1 <= capacity <=
  * 2^30) with exponent `alpha` >= 0 (pa_i = p_i^alpha; foxhunt "Integration":
  * priority^alpha is applied inside the update, not kept as a separate
- * buffer).  `flags` is PER_SCAN, PER_TREE or both.  All device memory the
+ * buffer).  `flags` is PER_SCAN, PER_TREE or both, or PER_RANK alone (then
+ * capacity <= 2^24; see per_rank_build).  All device memory the
  * context will ever use is allocated here (raw priorities, the CDF, the tree
  * of 2*capacity_pow2 floats, scan descriptors, update scratch) and
  * zero-filled on `stream`, which is synchronised before returning.  The size
@@ -160,6 +162,28 @@ per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, fl
                                  void* stream);
 
 /*
+ * per_rank_build -- rank-based PER (PER_RANK contexts).  foxhunt's segment-
+ * tree page ("Non-Goals") lists rank-based PER as a separate code path and
+ * does not define it; this library reads it as the usual rank-based variant:
+ * the n valid items are ordered by descending raw priority, ties broken by
+ * the lower index first (-0 and +0 are equal; priorities must be >= 0 and
+ * not NaN, else PER_ERR_VALUE is recorded and the order is unspecified), the
+ * item of rank r (1-based) gets priority q_r = fl32(1 / r), and everything
+ * downstream is proportional PER over ranks: pa_r = q_r^alpha, the CDF
+ * cdf[r-1] = sum_{s<=r} pa_s (built with the per_build_cdf scan, exact
+ * carries, so bit-reproducible), stratified thresholds, IS weights.
+ * The sort is a stable LSD radix sort (four 8-bit passes); it leaves
+ * order[r-1] = the item of rank r (per_rank_order_ptr).  The rank CDF depends
+ * only on n and alpha, so it is rebuilt only when the size changed since the
+ * previous per_rank_build.  Call it after priorities change and before
+ * sampling: per_sample / per_is_weights / per_total with mode PER_RANK return
+ * PER_ERR_STATE when the size changed since the last per_rank_build (a
+ * per_update without a new per_rank_build samples from the previous order).
+ * Requires PER_RANK and size >= 1 (PER_ERR_EMPTY).
+ */
+per_status per_rank_build(per_ctx* ctx, void* stream);
+
+/*
  * per_sample -- draw B stratified samples (1 <= B <= 2^24):
  *   u_k = fl32(fl32(fl32(k + U_k) / B) * T),  U_k in (0, 1],
  * or, with mode PER_TREE | PER_IID, B independent samples (foxhunt "CUDA
@@ -173,6 +197,8 @@ per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, fl
  *   mode PER_TREE: T = tree[1]; root-to-leaf descent (foxhunt "Operations" /
  *     Sample): at node j with children L, R: if u > L and R > 0 then
  *     { u = u - L; go right } else go left.
+ *   mode PER_RANK: as PER_SCAN on the rank CDF (T = rank cdf[n-1]), giving a
+ *     rank r_k; idx_k = order[r_k], the item of that rank.
  * d_out_idx receives int32[B].  Total 0 records PER_ERR_EMPTY.
  */
 per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, int mode,
@@ -185,7 +211,9 @@ per_status per_sample(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t offset, i
  *   w_k = (N * P(idx_k))^-beta / max_k (N * P(idx_k))^-beta,
  * P(i) = pa_i / total, N = size -- computed as (pa_min / pa_{idx_k})^beta
  * with pa_min the smallest pa in the batch (the max-normalised form; N and the
- * total cancel).  pa comes from the tree leaves with PER_TREE, else p^alpha of
+ * total cancel).  pa comes from the tree leaves with PER_TREE, from
+ * q_{rank(i)}^alpha in a PER_RANK context (item indices must be < size and
+ * sorted by per_rank_build; others record PER_ERR_VALUE), else p^alpha of
  * the raw priorities.  d_out_w receives float32[B]; the largest weight is
  * exactly 1.  beta >= 0.  A batch containing a zero-priority item yields
  * non-finite weights.
@@ -209,7 +237,8 @@ per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t 
  * per_step -- one minibatch step of proportional PER (PufferLib PR #615: the
  * prefix sum is rebuilt once per minibatch update; foxhunt "Integration":
  * update, then sample with IS weights): per_update(d_upd_idx, d_upd_prio,
- * n_upd) when n_upd > 0, then per_build_cdf, then per_sample_weighted(B,
+ * n_upd) when n_upd > 0, then per_build_cdf (per_rank_build in a PER_RANK
+ * context, mode PER_RANK), then per_sample_weighted(B,
  * seed, offset, mode, d_u01, beta, d_out_idx, d_out_w) -- the same
  * arguments, checks and results as those calls, bit for bit.  For scan-only
  * contexts (PER_SCAN without PER_TREE, mode PER_SCAN) of size <= 262,144
@@ -223,7 +252,8 @@ per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_p
                     float* d_out_w, void* stream);
 
 /* per_total -- total priority (foxhunt "Integration" / total_priority):
- * mode PER_TREE reads tree[1], PER_SCAN reads cdf[n-1] (after per_build_cdf).
+ * mode PER_TREE reads tree[1], PER_SCAN reads cdf[n-1] (after per_build_cdf),
+ * PER_RANK the rank CDF's last value sum_r q_r^alpha (after per_rank_build).
  * per_total writes one float to device memory; per_total_host synchronises
  * `stream` and returns it in *h_out. */
 per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream);
@@ -236,6 +266,10 @@ per_status per_total_host(per_ctx* ctx, int mode, float* h_out, void* stream);
 const float* per_priorities_ptr(const per_ctx* ctx);
 const float* per_cdf_ptr(const per_ctx* ctx);
 const float* per_tree_ptr(const per_ctx* ctx);
+/* PER_RANK contexts (NULL otherwise): order int32[capacity] (first size
+ * entries: the item of rank 1, 2, ...) and the rank CDF float[capacity]. */
+const int32_t* per_rank_order_ptr(const per_ctx* ctx);
+const float* per_rank_cdf_ptr(const per_ctx* ctx);
 
 /*
  * per_check -- synchronise `stream`, read and clear the device status word.
