@@ -42,12 +42,17 @@ WORKLOAD = (f"minibatch N={N} fp32 |N(0,1)|+1e-6, alpha={ALPHA}, {ROUNDS} rounds
             f"(build_cdf, sample {B} stratified, IS weights beta={BETA}, update {B} at sampled indices)")
 L2_FLUSH_BYTES = 512 << 20
 
-# algorithmic bytes per launch
+# algorithmic bytes per launch: what each kernel must read and write at least
 KERNEL_BYTES = {
     "build_cdf": lambda: 8 * N,                          # 4 B read + 4 B write per item
     "sample_is_weights": lambda: 4 * N + 12 * B,         # CDF windows once; index, p gather, weight
     "update": lambda: 8 * B + 4 * B + 8 * B,             # idx + p read, priority write, winner slot
 }
+# Per key, the radix sort's four passes: pass 0 reads the priorities twice
+# (histogram, scatter) and writes keys and values (16 B); passes 1 and 2 read
+# the keys twice and the values once and write both (20 B each); pass 3 reads
+# the same and writes the order and its inverse (20 B).
+RANK_SORT_BYTES_PER_KEY = 16 + 20 + 20 + 20
 KERNEL_BYTES["step"] = lambda: sum(KERNEL_BYTES[k]() for k in ("update", "build_cdf", "sample_is_weights"))
 
 
@@ -411,6 +416,47 @@ def extras(per, torch, dev, peak):
                        "gbs": round(rbytes / (us_r * 1e-6) / 1e9, 1),
                        "frac_of_measured_peak": round(rbytes / (us_r * 1e-6) / 1e9 / peak, 4),
                        "l2": "flushed before each rep"}
+    # rank-based PER on the minibatch workload: per step, update the 8192
+    # sampled items, re-sort all 262,144 by priority, sample 8192 ranks with
+    # IS weights (per_step, mode PER_RANK)
+    Mb = workloads.MINIBATCH
+    ctx = per.PerContext(Mb["N"], Mb["alpha"], per.PER_RANK)
+    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
+    per.per_rank_build(ctx.handle)
+    ri = [torch.empty(Mb["B"], dtype=torch.int32, device=dev) for _ in range(2)]
+    rw = torch.empty(Mb["B"], dtype=torch.float32, device=dev)
+    rnew = [torch.from_numpy(workloads.minibatch_new_priorities(r)).to(dev) for r in range(8)]
+    per.per_sample(ctx.handle, Mb["B"], Mb["seed"], 0, per.PER_RANK, ri[0])
+
+    def rank_steps():
+        for r in range(8):
+            per.per_step(ctx.handle, ri[r & 1], rnew[r], Mb["B"], Mb["seed"], r * Mb["B"], per.PER_RANK,
+                         Mb["beta"], ri[(r + 1) & 1], rw)
+    rank_steps()
+    us_k = time_graph(graph_of(rank_steps), 30, flush_l2=False, per_replay=8)
+    us_b = time_graph(graph_of(lambda: per.per_rank_build(ctx.handle)), 30, flush_l2=False)
+    out["rank_minibatch_step"] = {"N": Mb["N"], "B": Mb["B"], "us": round(us_k, 2), "sort_us": round(us_b, 2),
+                                  "l2": "warm (the 1 MiB priorities stay resident across steps)",
+                                  "timing": "graph of 8 steps between events, per step"}
+    if per.per_check(ctx.handle) != 0:
+        out["rank_minibatch_step"]["status"] = "device status not clean"
+    ctx.close()
+    # the sort at 16M items (L2 flushed): four 8-bit passes, each reading the
+    # keys twice and the values once and writing both (pass 0 reads the
+    # priorities; the last writes the order and its inverse)
+    ctx = per.PerContext(n, S["alpha"], per.PER_RANK)
+    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
+    per.per_rank_build(ctx.handle)
+    us_16 = time_graph(graph_of(lambda: per.per_rank_build(ctx.handle)), 10)
+    sort_bytes = RANK_SORT_BYTES_PER_KEY * n
+    out["rank_sort_16M"] = {"N": n, "us": round(us_16, 2), "keys_per_s": n / (us_16 * 1e-6),
+                            "gbs": round(sort_bytes / (us_16 * 1e-6) / 1e9, 1),
+                            "frac_of_measured_peak": round(sort_bytes / (us_16 * 1e-6) / 1e9 / peak, 4),
+                            "bytes_per_key": RANK_SORT_BYTES_PER_KEY, "l2": "flushed before each rep"}
+    if per.per_check(ctx.handle) != 0:
+        out["rank_sort_16M"]["status"] = "device status not clean"
+    ctx.close()
+
     # the whole particle-filter resample step with D = 4 states per particle:
     # indices, gathered states and the reset log-weights in one launch
     D = 4
@@ -430,7 +476,8 @@ def extras(per, torch, dev, peak):
 # ------------------------------------------------------ kernel cases --------
 
 KERNEL_CASES = ("scan_stress", "scan_minibatch", "sample_stress", "sample_minibatch", "is_weights_minibatch",
-                "update_minibatch", "step_minibatch", "tree_step", "resample", "is_weights_heavy")
+                "update_minibatch", "step_minibatch", "tree_step", "resample", "is_weights_heavy",
+                "rank_sort_stress", "rank_step_minibatch")
 
 
 def kernel_case(name, reps):
@@ -491,6 +538,21 @@ def kernel_case(name, reps):
         def body():
             per.per_sample(ctx.handle, T["B"], 3, 0, per.PER_TREE, tidx)
             per.per_update(ctx.handle, d_ui, d_up)
+    elif name == "rank_sort_stress":
+        S = workloads.STRESS
+        ctx = per.PerContext(S["N"], S["alpha"], per.PER_RANK)
+        per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
+        body = lambda: per.per_rank_build(ctx.handle)  # noqa: E731
+    elif name == "rank_step_minibatch":
+        ctx = per.PerContext(N, ALPHA, per.PER_RANK)
+        per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
+        per.per_rank_build(ctx.handle)
+        idx = torch.empty(B, dtype=torch.int32, device=dev)
+        idx2 = torch.empty(B, dtype=torch.int32, device=dev)
+        w = torch.empty(B, dtype=torch.float32, device=dev)
+        newp = torch.from_numpy(workloads.minibatch_new_priorities(0)).to(dev)
+        per.per_sample(ctx.handle, B, W["seed"], 0, per.PER_RANK, idx)
+        body = lambda: per.per_step(ctx.handle, idx, newp, B, W["seed"], 0, per.PER_RANK, BETA, idx2, w)  # noqa: E731
     elif name == "resample":
         R = workloads.RESAMPLE
         logw = torch.from_numpy(workloads.resample_logw()).to(dev)

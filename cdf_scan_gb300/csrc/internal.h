@@ -64,7 +64,7 @@ struct per_ctx {
     int32_t* rank_vals1;              // [capacity] item indices (pong)
     int32_t* rank_order;              // [capacity] order[r] = the item of rank r + 1
     int32_t* rank_of;                 // [capacity] rank_of[order[r]] = r
-    unsigned* rank_counts;            // [kRadixDigits * sort tiles] per-tile digit counts
+    unsigned* rank_counts;            // [rank_count_words(capacity)] per-tile digit counts
     unsigned* rank_totals;            // [kRadixDigits] digit totals of the running pass
     float* rank_q;                    // [alloc_n] q[r] = 1 / (r + 1)
     float* rank_cdf;                  // [alloc_n] inclusive prefix sum of q^alpha
@@ -74,7 +74,7 @@ struct per_ctx {
 };
 
 // Grid-barrier ticket words (per_ctx::tickets).
-enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_SCAN = 3, TK_STEP = 4, NUM_TICKETS = 8 };
+enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_SCAN = 3, TK_STEP = 4, TK_RANK = 5, NUM_TICKETS = 8 };
 
 // Items per entry of the coarse CDF index: coarse[j] = cdf[min(64j+63, n-1)].
 constexpr int kCoarseStride = 64;
@@ -93,11 +93,14 @@ constexpr int kDescStride = 16;
 constexpr int64_t kMaxWaveTiles = 1024;
 inline int64_t scan_state_words(int64_t tiles) { return tiles * kDescStride + 1; }
 
-// Rank-based PER: 8-bit radix digits, 4096 keys per sort tile, and at most
-// 2^24 items (4096 tiles).
+// Rank-based PER: 8-bit radix digits, sort tiles of 4096 keys (2048 in the
+// one-launch sort of small sizes), at most 2^24 items.
 constexpr int kRadixDigits = 256;
 constexpr int kRankTile = 4096;
+constexpr int kRankSmallTile = 2048;
 constexpr int64_t kRankMaxN = int64_t(1) << 24;
+// Words of the per-tile digit counts for `cap` items (either tiling).
+inline int64_t rank_count_words(int64_t cap) { return kRadixDigits * ((cap + kRankSmallTile - 1) / kRankSmallTile); }
 
 // Host-side launch accounting (per_launch_count).
 void per_note_launch(int n = 1);

@@ -119,11 +119,10 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok && (flags & PER_RANK)) {
         const size_t cap = static_cast<size_t>(capacity);
-        const size_t tiles = (cap + kRankTile - 1) / kRankTile;
         ok = alloc_zero(&c->rank_keys0, cap, s) == cudaSuccess && alloc_zero(&c->rank_keys1, cap, s) == cudaSuccess &&
              alloc_zero(&c->rank_vals1, cap, s) == cudaSuccess && alloc_zero(&c->rank_order, cap, s) == cudaSuccess &&
              alloc_zero(&c->rank_of, cap, s) == cudaSuccess &&
-             alloc_zero(&c->rank_counts, kRadixDigits * tiles, s) == cudaSuccess &&
+             alloc_zero(&c->rank_counts, static_cast<size_t>(rank_count_words(capacity)), s) == cudaSuccess &&
              alloc_zero(&c->rank_totals, static_cast<size_t>(kRadixDigits), s) == cudaSuccess &&
              alloc_zero(&c->rank_q, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->rank_cdf, c->alloc_n, s) == cudaSuccess &&

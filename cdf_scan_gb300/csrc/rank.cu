@@ -13,17 +13,24 @@
 // kernels.  Sampling draws ranks from that CDF with the scan-path sampler and
 // writes order[rank].
 //
-// One radix pass is three launches:
-//   hist    -- per-tile digit counts, stored digit-major: counts[d][tile];
-//   scan    -- one CTA per digit: exclusive scan of counts[d][*] across the
-//              tiles, and the digit's total;
-//   scatter -- every CTA scans the 256 totals (the digits' first positions),
-//              ranks its tile's keys stably and writes them out.
-// Inside a tile, warp w owns the contiguous keys [w * 512, (w + 1) * 512) and
-// ranks them in 16 rounds of 32 with __match_any_sync peer groups and
-// warp-private digit counters; the warps then take digit offsets in warp
-// order.  Key order inside a tile is therefore kept, and across tiles the
-// scan keeps tile order: the sort is stable.
+// Every pass works tile by tile (256 threads, ITEMS keys each):
+//   rank   -- warp w owns the tile's keys [w * 32 * ITEMS, (w + 1) * 32 *
+//             ITEMS) and ranks them round by round: the lanes holding the
+//             same digit (found with one ballot per digit bit) take
+//             consecutive positions after the warp's running count of it;
+//   place  -- the warps take digit offsets in warp order, the digits take
+//             tile offsets in digit order, and each key goes to its slot of a
+//             tile-local sorted copy in shared memory;
+//   write  -- consecutive threads copy consecutive slots out, so the keys of
+//             one digit land in consecutive global positions (coalesced).
+// Key order inside a tile is kept, and the cross-tile offsets keep tile
+// order: the sort is stable.  The cross-tile offsets come from
+//   large sizes -- three launches per pass: per-tile digit histograms
+//             (digit-major), one CTA per digit scanning its row across the
+//             tiles, then the tile pass above;
+//   small sizes -- one cooperative launch for all four passes: each CTA
+//             publishes its tile's digit counts, and after a grid barrier
+//             sums the counts of all tiles itself.
 #include <algorithm>
 
 #include "common.cuh"
@@ -32,58 +39,269 @@
 namespace {
 
 constexpr int kSortThreads = 256;
-constexpr int kSortItems = kRankTile / kSortThreads;  // 16 keys per thread
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kWarpKeys = kRankTile / kSortWarps;     // 512 keys per warp
+constexpr int kBigItems = kRankTile / kSortThreads;  // 16 keys per thread, 4096 per tile
+constexpr int kSmallItems = 8;                       // 2048 keys per tile
+constexpr int kSmallMaxTiles = 128;                  // cooperative path: n <= 262,144
 constexpr int kScanThreads = 1024;
-constexpr int kRankMaxTiles = static_cast<int>(kRankMaxN / kRankTile);
+constexpr int kBigMaxTiles = static_cast<int>(kRankMaxN / kRankTile);
 static_assert(kSortThreads == kRadixDigits, "one thread per digit");
-static_assert(kWarpKeys == 32 * kSortItems, "a warp ranks 32 keys per round");
-static_assert(kRankMaxTiles <= 4 * kScanThreads, "the digit scan takes at most 4 tiles per thread");
+static_assert(kBigMaxTiles <= 4 * kScanThreads, "the digit scan takes at most 4 tiles per thread");
 
 // Ascending keys = descending priorities: non-negative floats order like
 // their bit patterns, and -0 and +0 share one key.
 __device__ __forceinline__ unsigned rank_key(float p) { return ~__float_as_uint(p + 0.f); }
 
 struct SortParams {
-    const float* prio;         // pass 0 reads keys from the priorities, values = item indices
-    const unsigned* keys_in;   // later passes
-    const int32_t* vals_in;
-    unsigned* keys_out;        // nullptr in the last pass
-    int32_t* vals_out;
-    int32_t* rank_of;          // last pass only: rank_of[item] = its position
-    unsigned* counts;          // [kRadixDigits][tiles]
-    unsigned* totals;          // [kRadixDigits]
+    const float* prio;
+    unsigned* keys0;
+    unsigned* keys1;
+    int32_t* vals1;
+    int32_t* order;
+    int32_t* rank_of;
+    unsigned* counts;  // large sizes: [kRadixDigits][tiles]; small: [tiles][kRadixDigits]
+    unsigned* totals;  // [kRadixDigits] (large sizes)
     int* status;
+    unsigned long long* ticket;
     int n;
     int tiles;
-    int shift;
-    bool first;
+    int pass;  // large sizes: the pass of this launch
 };
 
-__device__ __forceinline__ unsigned key_at(const SortParams& S, int i) {
-    return S.first ? rank_key(__ldg(S.prio + i)) : __ldg(S.keys_in + i);
+// Buffers of pass p: 0 reads the priorities and writes (keys1, vals1);
+// 1 -> (keys0, order); 2 -> (keys1, vals1); 3 -> order and rank_of.
+struct PassIO {
+    const unsigned* keys_in;
+    const int32_t* vals_in;
+    unsigned* keys_out;  // nullptr in the last pass
+    int32_t* vals_out;
+    int shift;
+    bool first, last;
+};
+
+__device__ __forceinline__ PassIO pass_io(const SortParams& S, int pass) {
+    PassIO io;
+    const bool odd = (pass & 1) != 0;
+    io.first = pass == 0;
+    io.last = pass == 3;
+    io.shift = 8 * pass;
+    io.keys_in = odd ? S.keys1 : S.keys0;
+    io.vals_in = odd ? S.vals1 : S.order;
+    io.keys_out = io.last ? nullptr : (odd ? S.keys0 : S.keys1);
+    io.vals_out = odd ? S.order : S.vals1;
+    return io;
 }
 
-__device__ __forceinline__ int32_t val_at(const SortParams& S, int i) { return S.first ? i : __ldg(S.vals_in + i); }
+template <int ITEMS>
+struct SortSmem {
+    unsigned keys[kSortThreads * ITEMS];         // the tile, sorted by digit
+    int32_t vals[kSortThreads * ITEMS];
+    unsigned cnt[kSortWarps][kRadixDigits];      // per-warp digit counts, then local offsets
+    int off[kRadixDigits];                       // global position - local slot, per digit
+    unsigned w[kSortWarps];
+};
 
-__global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) {
-    __shared__ unsigned h[kRadixDigits];
-    h[threadIdx.x] = 0u;
+// The lanes of the warp whose digit equals this lane's (valid lanes), or the
+// invalid lanes (invalid lanes, which pass d = 0): one ballot per digit bit.
+// Eight ballots cost far less than one __match_any_sync.
+__device__ __forceinline__ unsigned digit_peers(unsigned d, bool valid) {
+    const unsigned v = __ballot_sync(PER_FULL_MASK, valid);
+    unsigned peers = valid ? v : ~v;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const bool bit = ((d >> b) & 1u) != 0u;
+        const unsigned m = __ballot_sync(PER_FULL_MASK, bit);
+        peers &= bit ? m : ~m;
+    }
+    return peers;
+}
+
+// Exclusive scan of one value per thread over the CTA (thread order); *total
+// receives the sum.  Reuses s_w: callers separate two uses by a barrier.
+__device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* s_w, unsigned* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned y = __shfl_up_sync(PER_FULL_MASK, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) s_w[warp] = x;
     __syncthreads();
-    const int base = blockIdx.x * kRankTile;
-    bool bad = false;
-#pragma unroll 4
-    for (int e = 0; e < kSortItems; ++e) {
-        const int i = base + e * kSortThreads + threadIdx.x;
+    unsigned before = 0u, all = 0u;
+#pragma unroll
+    for (int w = 0; w < kSortWarps; ++w) {
+        const unsigned c = s_w[w];
+        if (w < warp) before += c;
+        all += c;
+    }
+    *total = all;
+    __syncthreads();
+    return before + (x - v);
+}
+
+// Rank step: the warp's keys of this tile and, per key, its position among
+// the warp's keys of the same digit; sm.cnt[warp][d] ends as the warp's count
+// of digit d (sm.cnt zeroed by the caller).
+template <int ITEMS>
+__device__ __forceinline__ void warp_rank(const SortParams& S, const PassIO& io, int tile_base,
+                                          unsigned (&key)[ITEMS], unsigned (&pos)[ITEMS], SortSmem<ITEMS>& sm,
+                                          bool& bad) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned lt = (1u << lane) - 1u;
+    const int base = tile_base + warp * 32 * ITEMS;
+    // all loads first, so that they are in flight together (the ballots below
+    // would otherwise keep each round's load waiting for the previous round)
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r) {
+        const int i = base + r * 32 + lane;
+        key[r] = 0u;
         if (i < S.n) {
-            if (S.first) bad |= !(__ldg(S.prio + i) >= 0.f);  // negative or NaN
-            atomicAdd(&h[(key_at(S, i) >> S.shift) & 255u], 1u);
+            if (io.first) {
+                const float p = __ldg(S.prio + i);
+                bad |= !(p >= 0.f);  // negative or NaN
+                key[r] = rank_key(p);
+            } else {
+                key[r] = __ldcg(io.keys_in + i);
+            }
         }
+    }
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r) {
+        const bool ok = base + r * 32 + lane < S.n;
+        const unsigned d = ok ? (key[r] >> io.shift) & 255u : 0u;
+        const unsigned peers = digit_peers(d, ok);
+        const int leader = __ffs(peers) - 1;
+        unsigned old = 0u;
+        if (ok && lane == leader) {
+            old = sm.cnt[warp][d];
+            sm.cnt[warp][d] = old + __popc(peers);
+        }
+        old = __shfl_sync(PER_FULL_MASK, old, leader);
+        pos[r] = old + __popc(peers & lt);
+        __syncwarp();
+    }
+}
+
+// Thread = digit d: turn the warps' counts of d into offsets in warp order;
+// returns the tile's count of d.
+template <int ITEMS>
+__device__ __forceinline__ unsigned warp_offsets(SortSmem<ITEMS>& sm) {
+    const int d = threadIdx.x;
+    unsigned run = 0u;
+#pragma unroll
+    for (int w = 0; w < kSortWarps; ++w) {
+        const unsigned c = sm.cnt[w][d];
+        sm.cnt[w][d] = run;
+        run += c;
+    }
+    return run;
+}
+
+// Place and write steps.  On entry sm.cnt[w][d] is the local slot of warp
+// w's first key of digit d and sm.off[d] = global position - local slot.
+template <int ITEMS>
+__device__ __forceinline__ void place_and_write(const SortParams& S, const PassIO& io, int tile_base,
+                                                const unsigned (&key)[ITEMS], const unsigned (&pos)[ITEMS],
+                                                SortSmem<ITEMS>& sm) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int base = tile_base + warp * 32 * ITEMS;
+    int32_t val[ITEMS];
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r) {  // loads first, all in flight together
+        const int i = base + r * 32 + lane;
+        val[r] = io.first ? i : (i < S.n ? __ldcg(io.vals_in + i) : 0);
+    }
+#pragma unroll
+    for (int r = 0; r < ITEMS; ++r) {
+        const int i = base + r * 32 + lane;
+        if (i >= S.n) continue;
+        const unsigned d = (key[r] >> io.shift) & 255u;
+        const unsigned slot = sm.cnt[warp][d] + pos[r];
+        if (slot >= static_cast<unsigned>(kSortThreads * ITEMS)) continue;  // only if the counts were inconsistent
+        sm.keys[slot] = key[r];
+        sm.vals[slot] = val[r];
+    }
+    __syncthreads();
+    const int valid = min(kSortThreads * ITEMS, S.n - tile_base);
+    bool bad = false;
+    for (int j = threadIdx.x; j < valid; j += kSortThreads) {
+        const unsigned k = sm.keys[j];
+        const int32_t v = sm.vals[j];
+        const unsigned dst = static_cast<unsigned>(sm.off[(k >> io.shift) & 255u] + j);
+        if (dst >= static_cast<unsigned>(S.n) || static_cast<unsigned>(v) >= static_cast<unsigned>(S.n)) {
+            // only if the counts were inconsistent
+            bad = true;
+            continue;
+        }
+        if (io.keys_out) io.keys_out[dst] = k;
+        io.vals_out[dst] = v;
+        if (io.last) S.rank_of[v] = static_cast<int32_t>(dst);
+    }
+    if (bad) atomicOr(S.status, ST_RANGE);
+}
+
+// ---- large sizes: three launches per pass ----------------------------------
+
+// Per-tile digit counts, stored digit-major: counts[d][tile].  Each warp keeps
+// its own sub-histogram and adds one count per peer group, so equal digits
+// (the exponent byte of similar priorities) do not serialise on one counter.
+__global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) {
+    __shared__ unsigned h[kSortWarps][kRadixDigits];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&h[0][0])[i] = 0u;
+    __syncthreads();
+    const PassIO io = pass_io(S, S.pass);
+    const int tile_base = blockIdx.x * kRankTile;
+    bool bad = false;
+    unsigned k[kBigItems];
+    bool ok[kBigItems];
+#pragma unroll
+    for (int e = 0; e < kBigItems / 4; ++e) {  // all loads first, in flight together
+        const int i0 = tile_base + (e * kSortThreads + threadIdx.x) * 4;
+        if (i0 + 3 < S.n) {
+            if (io.first) {
+                const float4 p = __ldg(reinterpret_cast<const float4*>(S.prio + i0));
+                bad |= !(p.x >= 0.f) || !(p.y >= 0.f) || !(p.z >= 0.f) || !(p.w >= 0.f);
+                k[4 * e] = rank_key(p.x); k[4 * e + 1] = rank_key(p.y);
+                k[4 * e + 2] = rank_key(p.z); k[4 * e + 3] = rank_key(p.w);
+            } else {
+                const uint4 q = __ldcg(reinterpret_cast<const uint4*>(io.keys_in + i0));
+                k[4 * e] = q.x; k[4 * e + 1] = q.y; k[4 * e + 2] = q.z; k[4 * e + 3] = q.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ok[4 * e + c] = true;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = i0 + c;
+                ok[4 * e + c] = i < S.n;
+                k[4 * e + c] = 0u;
+                if (i < S.n) {
+                    if (io.first) {
+                        const float p = __ldg(S.prio + i);
+                        bad |= !(p >= 0.f);
+                        k[4 * e + c] = rank_key(p);
+                    } else {
+                        k[4 * e + c] = __ldcg(io.keys_in + i);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < kBigItems; ++c) {
+        const unsigned d = ok[c] ? (k[c] >> io.shift) & 255u : 0u;
+        const unsigned peers = digit_peers(d, ok[c]);
+        if (ok[c] && lane == __ffs(peers) - 1) h[warp][d] += __popc(peers);
+        __syncwarp();
     }
     if (bad) atomicOr(S.status, ST_VALUE);
     __syncthreads();
-    S.counts[threadIdx.x * S.tiles + blockIdx.x] = h[threadIdx.x];
+    unsigned sum = 0u;
+#pragma unroll
+    for (int w = 0; w < kSortWarps; ++w) sum += h[w][threadIdx.x];
+    S.counts[threadIdx.x * S.tiles + blockIdx.x] = sum;
 }
 
 // CTA d: counts[d][t] becomes the number of keys with digit d in tiles < t,
@@ -125,76 +343,75 @@ __global__ void __launch_bounds__(kScanThreads) radix_digit_scan_kernel(unsigned
     if (threadIdx.x == 0) totals[blockIdx.x] = s_w[31];
 }
 
-__global__ void __launch_bounds__(kSortThreads) radix_scatter_kernel(SortParams S) {
-    __shared__ unsigned s_cnt[kSortWarps][kRadixDigits];  // per-warp digit counts, then the warps' offsets
-    __shared__ unsigned s_base[kRadixDigits];             // this tile's first position per digit
-    __shared__ unsigned s_w[kSortWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&s_cnt[0][0])[i] = 0u;
-    {  // exclusive scan of the digit totals (thread = digit), plus this tile's offset
-        const unsigned t = S.totals[threadIdx.x];
-        unsigned x = t;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const unsigned y = __shfl_up_sync(PER_FULL_MASK, x, d);
-            if (lane >= d) x += y;
-        }
-        if (lane == 31) s_w[warp] = x;
-        __syncthreads();
-        unsigned before = 0u;
-        for (int w = 0; w < warp; ++w) before += s_w[w];
-        s_base[threadIdx.x] = before + (x - t) + S.counts[threadIdx.x * S.tiles + blockIdx.x];
-    }
+// The tile pass of large sizes: rank, place against the offsets of the
+// histogram and digit-scan launches, write.
+__global__ void __launch_bounds__(kSortThreads, 2) radix_scatter_kernel(SortParams S) {
+    __shared__ SortSmem<kBigItems> sm;
+    const PassIO io = pass_io(S, S.pass);
+    const int d = threadIdx.x;
+    for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&sm.cnt[0][0])[i] = 0u;
     __syncthreads();
-    const unsigned lt = (1u << lane) - 1u;
-    const int base = blockIdx.x * kRankTile + warp * kWarpKeys;
-    unsigned key[kSortItems];
-    unsigned pos[kSortItems];  // position among the warp's keys of the same digit
-#pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        const int i = base + r * 32 + lane;
-        const bool ok = i < S.n;
-        key[r] = ok ? key_at(S, i) : 0u;
-        const unsigned d = ok ? (key[r] >> S.shift) & 255u : 256u;  // 256: past the end, no counter
-        const unsigned peers = __match_any_sync(PER_FULL_MASK, d);
-        const int leader = __ffs(peers) - 1;
-        unsigned old = 0u;
-        if (ok && lane == leader) {
-            old = s_cnt[warp][d];
-            s_cnt[warp][d] = old + __popc(peers);
-        }
-        old = __shfl_sync(PER_FULL_MASK, old, leader);
-        pos[r] = old + __popc(peers & lt);
-    }
+    const int tile_base = blockIdx.x * kRankTile;
+    unsigned key[kBigItems], pos[kBigItems];
+    bool bad = false;  // reported by the histogram launch
+    warp_rank<kBigItems>(S, io, tile_base, key, pos, sm, bad);
     __syncthreads();
-    {  // per digit (thread = digit): the warps' offsets inside the tile, in warp order
-        const int d = threadIdx.x;
-        unsigned run = 0u;
+    const unsigned cnt_d = warp_offsets(sm);
+    unsigned tile_total = 0u, all = 0u;
+    const unsigned start_d = block_excl_scan(cnt_d, sm.w, &tile_total);
+    const unsigned digit_start = block_excl_scan(S.totals[d], sm.w, &all);
+    const unsigned gbase = digit_start + S.counts[d * S.tiles + blockIdx.x];
 #pragma unroll
-        for (int w = 0; w < kSortWarps; ++w) {
-            const unsigned c = s_cnt[w][d];
-            s_cnt[w][d] = run;
-            run += c;
-        }
-    }
+    for (int w = 0; w < kSortWarps; ++w) sm.cnt[w][d] += start_d;
+    sm.off[d] = static_cast<int>(gbase) - static_cast<int>(start_d);
     __syncthreads();
+    place_and_write<kBigItems>(S, io, tile_base, key, pos, sm);
+}
+
+// ---- small sizes: all four passes in one cooperative launch ----------------
+//
+// One CTA per 2048-key tile, all resident.  Per pass: rank the tile, publish
+// its digit counts (tile-major), grid barrier, sum every tile's counts (the
+// keys before this tile per digit, and the digit totals), place and write,
+// grid barrier.  Keys, values and counts written in the launch are read
+// through L2 (ld.global.cg).
+__global__ void __launch_bounds__(kSortThreads) radix_sort_small_kernel(SortParams S) {
+    __shared__ SortSmem<kSmallItems> sm;
+    const int d = threadIdx.x;
+    const int tile_base = blockIdx.x * kSortThreads * kSmallItems;
     bool bad = false;
+    for (int pass = 0; pass < 4; ++pass) {
+        const PassIO io = pass_io(S, pass);
+        for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&sm.cnt[0][0])[i] = 0u;
+        __syncthreads();
+        unsigned key[kSmallItems], pos[kSmallItems];
+        warp_rank<kSmallItems>(S, io, tile_base, key, pos, sm, bad);
+        __syncthreads();
+        const unsigned cnt_d = warp_offsets(sm);
+        unsigned tile_total = 0u, all = 0u;
+        const unsigned start_d = block_excl_scan(cnt_d, sm.w, &tile_total);
+        S.counts[blockIdx.x * kRadixDigits + d] = cnt_d;
+        if (!grid_barrier(S.ticket, S.status, ST_TIMEOUT)) return;
+        unsigned before = 0u, total = 0u;
+        for (int t0 = 0; t0 < S.tiles; t0 += 16) {  // 16 independent loads in flight
+            unsigned c[16];
 #pragma unroll
-    for (int r = 0; r < kSortItems; ++r) {
-        const int i = base + r * 32 + lane;
-        if (i >= S.n) continue;
-        const unsigned d = (key[r] >> S.shift) & 255u;
-        const unsigned dst = s_base[d] + s_cnt[warp][d] + pos[r];
-        if (dst >= static_cast<unsigned>(S.n)) {  // only if the counts were inconsistent
-            bad = true;
-            continue;
+            for (int e = 0; e < 16; ++e) c[e] = t0 + e < S.tiles ? __ldcg(S.counts + (t0 + e) * kRadixDigits + d) : 0u;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                before += t0 + e < static_cast<int>(blockIdx.x) ? c[e] : 0u;
+                total += c[e];
+            }
         }
-        const int32_t v = val_at(S, i);
-        if (S.keys_out) S.keys_out[dst] = key[r];
-        S.vals_out[dst] = v;
-        if (S.rank_of) S.rank_of[v] = static_cast<int32_t>(dst);
+        const unsigned digit_start = block_excl_scan(total, sm.w, &all);
+#pragma unroll
+        for (int w = 0; w < kSortWarps; ++w) sm.cnt[w][d] += start_d;
+        sm.off[d] = static_cast<int>(digit_start + before) - static_cast<int>(start_d);
+        __syncthreads();
+        place_and_write<kSmallItems>(S, io, tile_base, key, pos, sm);
+        if (pass < 3 && !grid_barrier(S.ticket, S.status, ST_TIMEOUT)) return;
     }
-    if (bad) atomicOr(S.status, ST_RANGE);
+    if (bad) atomicOr(S.status, ST_VALUE);
 }
 
 // q[r] = fl32(1 / (r + 1)), correctly rounded (r + 1 <= 2^24 is exact in fp32).
@@ -205,33 +422,57 @@ __global__ void rank_priorities_kernel(float* q, int n) {
 
 }  // namespace
 
+static_assert(kSortThreads * kSmallItems == kRankSmallTile, "count buffer sized for the small tiles");
+
 per_status launch_rank_build(per_ctx* ctx, cudaStream_t s) {
     const int n = static_cast<int>(ctx->size);
     if (n < 1 || n > kRankMaxN) return PER_ERR_STATE;
-    const int tiles = (n + kRankTile - 1) / kRankTile;
     SortParams S = {};
     S.prio = ctx->prio;
+    S.keys0 = ctx->rank_keys0;
+    S.keys1 = ctx->rank_keys1;
+    S.vals1 = ctx->rank_vals1;
+    S.order = ctx->rank_order;
+    S.rank_of = ctx->rank_of;
     S.counts = ctx->rank_counts;
     S.totals = ctx->rank_totals;
     S.status = ctx->status;
+    S.ticket = ctx->tickets + TK_RANK;
     S.n = n;
-    S.tiles = tiles;
-    // pass 0: priorities -> (keys1, vals1); 1 -> (keys0, order); 2 -> (keys1, vals1); 3 -> order
-    for (int pass = 0; pass < 4; ++pass) {
-        S.first = pass == 0;
-        S.shift = 8 * pass;
-        const bool odd = (pass & 1) != 0;
-        S.keys_in = odd ? ctx->rank_keys1 : ctx->rank_keys0;
-        S.vals_in = odd ? ctx->rank_vals1 : ctx->rank_order;
-        S.keys_out = pass == 3 ? nullptr : (odd ? ctx->rank_keys0 : ctx->rank_keys1);
-        S.vals_out = odd ? ctx->rank_order : ctx->rank_vals1;
-        S.rank_of = pass == 3 ? ctx->rank_of : nullptr;
-        radix_hist_kernel<<<static_cast<unsigned>(tiles), kSortThreads, 0, s>>>(S);
-        radix_digit_scan_kernel<<<kRadixDigits, kScanThreads, 0, s>>>(ctx->rank_counts, ctx->rank_totals, tiles);
-        radix_scatter_kernel<<<static_cast<unsigned>(tiles), kSortThreads, 0, s>>>(S);
+    static int per_sm = 0;  // resident CTAs per SM of the cooperative kernel
+    if (per_sm == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, radix_sort_small_kernel, kSortThreads, 0) !=
+            cudaSuccess)
+            return PER_ERR_CUDA;
+        if (per_sm < 1) per_sm = 1;
     }
-    per_note_launch(12);
-    if (cudaGetLastError() != cudaSuccess) return PER_ERR_CUDA;
+    const int small_tiles = (n + kRankSmallTile - 1) / kRankSmallTile;
+    if (small_tiles <= kSmallMaxTiles && small_tiles <= per_sm * ctx->num_sms) {
+        S.tiles = small_tiles;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(small_tiles));
+        cfg.blockDim = dim3(kSortThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, radix_sort_small_kernel, S);
+        per_note_launch();
+        if (e != cudaSuccess) return PER_ERR_CUDA;
+    } else {
+        S.tiles = (n + kRankTile - 1) / kRankTile;
+        for (int pass = 0; pass < 4; ++pass) {
+            S.pass = pass;
+            radix_hist_kernel<<<static_cast<unsigned>(S.tiles), kSortThreads, 0, s>>>(S);
+            radix_digit_scan_kernel<<<kRadixDigits, kScanThreads, 0, s>>>(ctx->rank_counts, ctx->rank_totals,
+                                                                          S.tiles);
+            radix_scatter_kernel<<<static_cast<unsigned>(S.tiles), kSortThreads, 0, s>>>(S);
+        }
+        per_note_launch(12);
+        if (cudaGetLastError() != cudaSuccess) return PER_ERR_CUDA;
+    }
     ctx->rank_sorted_n = n;
     if (ctx->rank_q_n != n) {  // q and its CDF depend on n (and the context's alpha) only
         const unsigned grid = static_cast<unsigned>(std::min(1024, (n + 255) / 256));
