@@ -687,7 +687,7 @@ per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* c
 // priorities and the output CDF and nothing is ever allocated.
 //
 // The array is part of the library image: every GPU that loads the library
-// holds it (about 165 KiB) until the process exits.  All calls on a device
+// holds it (about 160 KiB) until the process exits.  All calls on a device
 // share it and it keeps the previous call's contents (its counters are left
 // ready for the next call by the kernel itself), so two calls whose kernels
 // overlap on the GPU -- different streams without ordering between them --

@@ -146,7 +146,7 @@ per_status per_build_cdf(per_ctx* ctx, void* stream);
  * the inclusive prefix sum of d_prio^alpha, with the same kernel and the same
  * bit-exact result as per_build_cdf, and allocates nothing.
  *
- * Its scratch (tile aggregates for the lookback and a few counters) is a fixed ~33 KiB
+ * Its scratch (tile aggregates for the lookback, chunk sums and a few counters) is a fixed ~160 KiB
  * array compiled into the library, held by every GPU that loads the library
  * until the process exits; hence n <= 16,777,216 (2^24), larger n returns
  * PER_ERR_ARG without launching.  The first call on each device performs a
