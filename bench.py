@@ -416,6 +416,32 @@ def extras(per, torch, dev, peak):
                        "gbs": round(rbytes / (us_r * 1e-6) / 1e9, 1),
                        "frac_of_measured_peak": round(rbytes / (us_r * 1e-6) / 1e9 / peak, 4),
                        "l2": "flushed before each rep"}
+    # the minibatch step that also returns the sampled transitions: rows of
+    # 64 floats (256 B) per item, copied inside the step's launch
+    Mb = workloads.MINIBATCH
+    ctx = per.PerContext(Mb["N"], Mb["alpha"], per.PER_SCAN)
+    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
+    trans = torch.randn((Mb["N"], 64), generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+    gi = [torch.empty(Mb["B"], dtype=torch.int32, device=dev) for _ in range(2)]
+    gw = torch.empty(Mb["B"], dtype=torch.float32, device=dev)
+    grows = torch.empty((Mb["B"], 64), dtype=torch.float32, device=dev)
+    gnew = [torch.from_numpy(workloads.minibatch_new_priorities(r)).to(dev) for r in range(8)]
+    per.per_build_cdf(ctx.handle)
+    per.per_sample(ctx.handle, Mb["B"], Mb["seed"], 0, per.PER_SCAN, gi[0])
+
+    def gather_steps():
+        for r in range(8):
+            per.per_step_gather(ctx.handle, gi[r & 1], gnew[r], Mb["B"], Mb["seed"], r * Mb["B"], per.PER_SCAN,
+                                Mb["beta"], gi[(r + 1) & 1], gw, trans, grows)
+    gather_steps()
+    us_g = time_graph(graph_of(gather_steps), 30, flush_l2=False, per_replay=8)
+    out["step_gather_minibatch_256B"] = {"N": Mb["N"], "B": Mb["B"], "row_bytes": 256, "us": round(us_g, 2),
+                                         "l2": "warm (the transitions stay resident across steps)",
+                                         "timing": "graph of 8 steps between events, per step"}
+    if per.per_check(ctx.handle) != 0:
+        out["step_gather_minibatch_256B"]["status"] = "device status not clean"
+    ctx.close()
+
     # rank-based PER on the minibatch workload: per step, update the 8192
     # sampled items, re-sort all 262,144 by priority, sample 8192 ranks with
     # IS weights (per_step, mode PER_RANK)
@@ -477,7 +503,7 @@ def extras(per, torch, dev, peak):
 
 KERNEL_CASES = ("scan_stress", "scan_minibatch", "sample_stress", "sample_minibatch", "is_weights_minibatch",
                 "update_minibatch", "step_minibatch", "tree_step", "resample", "is_weights_heavy",
-                "rank_sort_stress", "rank_step_minibatch")
+                "rank_sort_stress", "rank_step_minibatch", "resample_step")
 
 
 def kernel_case(name, reps):
@@ -553,12 +579,19 @@ def kernel_case(name, reps):
         newp = torch.from_numpy(workloads.minibatch_new_priorities(0)).to(dev)
         per.per_sample(ctx.handle, B, W["seed"], 0, per.PER_RANK, idx)
         body = lambda: per.per_step(ctx.handle, idx, newp, B, W["seed"], 0, per.PER_RANK, BETA, idx2, w)  # noqa: E731
-    elif name == "resample":
+    elif name in ("resample", "resample_step"):
         R = workloads.RESAMPLE
         logw = torch.from_numpy(workloads.resample_logw()).to(dev)
         out = torch.empty((R["rows"], R["P"]), dtype=torch.int32, device=dev)
         ctx = None
-        body = lambda: per.per_resample(logw, 6, 0, out)  # noqa: E731
+        if name == "resample":
+            body = lambda: per.per_resample(logw, 6, 0, out)  # noqa: E731
+        else:  # D = 4 states per particle, log-weights reset into a second buffer
+            state = torch.randn((R["rows"], R["P"], 4), generator=torch.Generator(device=dev).manual_seed(6),
+                                device=dev)
+            out_state = torch.empty_like(state)
+            out_lw = torch.empty_like(logw)
+            body = lambda: per.per_resample_step(logw, state, 6, 0, out, out_state, out_lw)  # noqa: E731
     else:
         raise SystemExit(f"unknown kernel case {name!r}; one of {', '.join(KERNEL_CASES)}")
     if ctx is not None:

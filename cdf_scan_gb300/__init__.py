@@ -45,6 +45,9 @@ SIGNATURES = {
     "per_is_weights": (ctypes.c_int, [_vp, _vp, _i32, _f32, _vp, _vp]),
     "per_sample_weighted": (ctypes.c_int, [_vp, _i32, _u64, _u64, ctypes.c_int, _vp, _f32, _vp, _vp, _vp]),
     "per_step": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _u64, _u64, ctypes.c_int, _vp, _f32, _vp, _vp, _vp]),
+    "per_gather": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i32, _vp, _vp]),
+    "per_step_gather": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _u64, _u64, ctypes.c_int, _vp, _f32, _vp, _vp,
+                                       _vp, _i64, _vp, _vp]),
     "per_total": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp]),
     "per_total_host": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(_f32), _vp]),
     "per_priorities_ptr": (_vp, [_vp]),
@@ -206,6 +209,40 @@ def per_step(ctx: int, upd_idx: torch.Tensor | None, upd_prio: torch.Tensor | No
         ctx, _ptr(upd_idx, torch.int32, "upd_idx"), _ptr(upd_prio, torch.float32, "upd_prio", n), n, B, seed,
         offset, mode, _ptr(u01, torch.float32, "u01", B), beta, _ptr(out_idx, torch.int32, "out_idx", B),
         _ptr(out_w, torch.float32, "out_w", B), _stream(stream)))
+    return out_idx
+
+
+def _rows(t: torch.Tensor, name: str) -> tuple[int, int]:
+    """(pointer, bytes per row) of a contiguous CUDA tensor of rows (first dim = rows)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous() or t.dim() < 1:
+        raise ValueError(f"{name}: expected a contiguous CUDA tensor of rows")
+    return t.data_ptr(), t[0].numel() * t.element_size() if t.shape[0] > 0 else 0
+
+
+def per_gather(ctx: int, rows: torch.Tensor, idx: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """out[k] = rows[idx[k]] (rows: one row per item, any dtype, row bytes a multiple of 16)."""
+    rp, rb = _rows(rows, "rows")
+    op, ob = _rows(out, "out")
+    if ob != rb or out.shape[0] < idx.numel() or out.dtype != rows.dtype:
+        raise ValueError("out: expected rows of the same size and dtype as `rows`, one per index")
+    _check("per_gather", lib().per_gather(ctx, rp, rb, _ptr(idx, torch.int32, "idx"), idx.numel(), op,
+                                          _stream(stream)))
+    return out
+
+
+def per_step_gather(ctx: int, upd_idx: torch.Tensor | None, upd_prio: torch.Tensor | None, B: int, seed: int,
+                    offset: int, mode: int, beta: float, out_idx: torch.Tensor, out_w: torch.Tensor,
+                    rows: torch.Tensor, out_rows: torch.Tensor, u01: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    n = 0 if upd_idx is None else upd_idx.numel()
+    rp, rb = _rows(rows, "rows")
+    op, ob = _rows(out_rows, "out_rows")
+    if ob != rb or out_rows.shape[0] < B or out_rows.dtype != rows.dtype:
+        raise ValueError("out_rows: expected B rows of the same size and dtype as `rows`")
+    _check("per_step_gather", lib().per_step_gather(
+        ctx, _ptr(upd_idx, torch.int32, "upd_idx"), _ptr(upd_prio, torch.float32, "upd_prio", n), n, B, seed,
+        offset, mode, _ptr(u01, torch.float32, "u01", B), beta, _ptr(out_idx, torch.int32, "out_idx", B),
+        _ptr(out_w, torch.float32, "out_w", B), rp, rb, op, _stream(stream)))
     return out_idx
 
 

@@ -122,8 +122,14 @@ per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta
 // PER_ERR_STATE (nothing launched) when the fused path does not apply.
 per_status launch_sample_scan_weighted(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, const float* u01,
                                        float beta, int32_t* out, float* out_w, cudaStream_t s);
+// With `rows` (row_bytes a multiple of 16), also out_rows[k] = rows[out[k]].
 per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p, int n_upd, int B, uint64_t seed,
-                       uint64_t offset, const float* u01, float beta, int32_t* out, float* out_w, cudaStream_t s);
+                       uint64_t offset, const float* u01, float beta, int32_t* out, float* out_w, const void* rows,
+                       int64_t row_bytes, void* out_rows, cudaStream_t s);
+// out[k] = rows[idx[k]] for k in [0, B), rows of row_bytes (a multiple of 16)
+// indexed by item in [0, capacity); other indices flag ST_VALUE.
+per_status launch_gather(per_ctx* ctx, const void* rows, int64_t row_bytes, const int32_t* idx, int B, void* out,
+                         cudaStream_t s);
 per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n, cudaStream_t s);
 per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s);
 per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, uint64_t offset,

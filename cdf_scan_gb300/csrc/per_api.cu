@@ -14,6 +14,7 @@ std::atomic<uint64_t> g_launches{0};
 
 constexpr int64_t kMaxCapacity = int64_t(1) << 30;
 constexpr int64_t kPad = 16384;  // buffer padding: vector loads of a ragged tail stay in bounds
+constexpr int64_t kMaxRowBytes = int64_t(1) << 20;  // per_gather / per_step_gather row size limit
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -250,18 +251,34 @@ per_status per_sample_weighted(per_ctx* ctx, int32_t B, uint64_t seed, uint64_t 
     return per_is_weights(ctx, d_out_idx, B, beta, d_out_w, stream);
 }
 
-per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
-                    uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta, int32_t* d_out_idx,
-                    float* d_out_w, void* stream) {
+per_status per_gather(per_ctx* ctx, const void* d_rows, int64_t row_bytes, const int32_t* d_idx, int32_t B,
+                      void* d_out, void* stream) {
+    if (!ctx || !d_rows || !d_idx || !d_out || B < 1 || row_bytes < 16 || row_bytes > kMaxRowBytes ||
+        (row_bytes & 15) != 0 || !aligned16(d_rows) || !aligned16(d_out))
+        return PER_ERR_ARG;
+    return launch_gather(ctx, d_rows, row_bytes, d_idx, B, d_out, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// per_step, with the copy of the sampled rows when d_rows is not NULL.
+per_status step_impl(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
+                     uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta, int32_t* d_out_idx,
+                     float* d_out_w, const void* d_rows, int64_t row_bytes, void* d_out_rows, void* stream) {
     if (!ctx || n_upd < 0 || (n_upd > 0 && (!d_upd_idx || !d_upd_prio))) return PER_ERR_ARG;
     if (B < 1 || B > (1 << 24) || !d_out_idx || !d_out_w || !(beta >= 0.f) || beta > 1e30f) return PER_ERR_ARG;
     if (mode != static_cast<int>(PER_SCAN) && mode != static_cast<int>(PER_TREE) &&
         mode != static_cast<int>(PER_TREE | PER_IID) && mode != static_cast<int>(PER_RANK))
         return PER_ERR_ARG;
+    if (d_rows && (!d_out_rows || row_bytes < 16 || row_bytes > kMaxRowBytes || (row_bytes & 15) != 0 ||
+                   !aligned16(d_rows) || !aligned16(d_out_rows)))
+        return PER_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (mode == static_cast<int>(PER_SCAN) && ctx->flags == PER_SCAN && ctx->size >= 1) {
-        const per_status st =
-            launch_step(ctx, d_upd_idx, d_upd_prio, n_upd, B, seed, offset, d_u01, beta, d_out_idx, d_out_w, s);
+        const per_status st = launch_step(ctx, d_upd_idx, d_upd_prio, n_upd, B, seed, offset, d_u01, beta, d_out_idx,
+                                          d_out_w, d_rows, row_bytes, d_out_rows, s);
         if (st != PER_ERR_STATE) return st;
     }
     per_status st = per_update(ctx, d_upd_idx, d_upd_prio, n_upd, stream);
@@ -274,7 +291,29 @@ per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_p
         st = per_rank_build(ctx, stream);
         if (st != PER_OK) return st;
     }
-    return per_sample_weighted(ctx, B, seed, offset, mode, d_u01, beta, d_out_idx, d_out_w, stream);
+    st = per_sample_weighted(ctx, B, seed, offset, mode, d_u01, beta, d_out_idx, d_out_w, stream);
+    if (st != PER_OK || !d_rows) return st;
+    return launch_gather(ctx, d_rows, row_bytes, d_out_idx, B, d_out_rows, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
+                    uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta, int32_t* d_out_idx,
+                    float* d_out_w, void* stream) {
+    return step_impl(ctx, d_upd_idx, d_upd_prio, n_upd, B, seed, offset, mode, d_u01, beta, d_out_idx, d_out_w,
+                     nullptr, 0, nullptr, stream);
+}
+
+per_status per_step_gather(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
+                           uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta,
+                           int32_t* d_out_idx, float* d_out_w, const void* d_rows, int64_t row_bytes,
+                           void* d_out_rows, void* stream) {
+    if (!d_rows) return PER_ERR_ARG;
+    return step_impl(ctx, d_upd_idx, d_upd_prio, n_upd, B, seed, offset, mode, d_u01, beta, d_out_idx, d_out_w,
+                     d_rows, row_bytes, d_out_rows, stream);
 }
 
 per_status per_total(per_ctx* ctx, int mode, float* d_out, void* stream) {

@@ -294,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
 #pragma unroll
             for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
             const int j0 = b0 + t0;
-            if (j0 >= j_lo && j0 + kLane <= j_hi) {
-                *reinterpret_cast<int4*>(orow + j0) = make_int4(v[0], v[1], v[2], v[3]);
-                *reinterpret_cast<int4*>(orow + j0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
+            if (j0 >= j_lo && j0 + kLane <= j_hi) {  // written once: evict-first stores
+                __stcs(reinterpret_cast<int4*>(orow + j0), make_int4(v[0], v[1], v[2], v[3]));
+                __stcs(reinterpret_cast<int4*>(orow + j0 + 4), make_int4(v[4], v[5], v[6], v[7]));
             } else {
 #pragma unroll
                 for (int e = 0; e < kLane; ++e)
@@ -305,7 +305,10 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
             if (R.out_state) {
                 // the block's particles in shared memory, then their states
                 // copied by consecutive threads for consecutive outputs
-                // (coalesced: neighbouring outputs hold neighbouring particles)
+                // (coalesced: neighbouring outputs hold neighbouring particles).
+                // States are read and written once: evict-first loads and
+                // stores, so that they do not push the rows' log-weights,
+                // which the row's later passes read again, out of L2.
                 __syncthreads();  // every thread has read s_stage
                 *reinterpret_cast<int4*>(s_stage + t0) = make_int4(v[0], v[1], v[2], v[3]);
                 *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
@@ -319,9 +322,11 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
                     const int i = s_stage[t];
                     if ((D & 3) == 0) {
                         for (int d = 0; d < D; d += 4)
-                            st_f4(drow + static_cast<size_t>(j) * D + d, ld_f4(srow + static_cast<size_t>(i) * D + d));
+                            __stcs(reinterpret_cast<float4*>(drow + static_cast<size_t>(j) * D + d),
+                                   __ldcs(reinterpret_cast<const float4*>(srow + static_cast<size_t>(i) * D + d)));
                     } else {
-                        for (int d = 0; d < D; ++d) drow[static_cast<size_t>(j) * D + d] = srow[static_cast<size_t>(i) * D + d];
+                        for (int d = 0; d < D; ++d)
+                            __stcs(drow + static_cast<size_t>(j) * D + d, __ldcs(srow + static_cast<size_t>(i) * D + d));
                     }
                 }
             }
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     if (R.out_logw) {  // every read of the row's log-weights is done: the reset may overwrite them
         float* lrow = R.out_logw + static_cast<size_t>(b) * P;
         const float4 r4 = make_float4(R.reset, R.reset, R.reset, R.reset);
-        for (int i = threadIdx.x * 4; i < P; i += kThreads * 4) st_f4(lrow + i, r4);
+        for (int i = threadIdx.x * 4; i < P; i += kThreads * 4) __stcs(reinterpret_cast<float4*>(lrow + i), r4);
     }
 }
 

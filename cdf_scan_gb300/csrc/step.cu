@@ -13,6 +13,7 @@
 // capture is the launch-overhead fix; foxhunt "GPU Segment Tree for PER
 // Sampling" section "Integration": update, then sample, with the IS weights
 // of the batch.)
+#include "gather_core.cuh"
 #include "sample_core.cuh"
 #include "scan_core.cuh"
 
@@ -39,6 +40,10 @@ struct StepParams {
     unsigned long long* ticket;  // grid-barrier word
     unsigned long long* last;    // [tile * kDescStride]: tagged last CDF value of each tile
     unsigned* step_min;          // call counter, then the batch-minimum word of even and odd calls
+    // optional copy of the sampled transitions: out_rows[k] = rows[out[k]]
+    const uint4* rows;           // [capacity][row_chunks] x 16 bytes, or nullptr
+    int row_chunks;
+    uint4* out_rows;             // [B][row_chunks] x 16 bytes
 };
 
 // Bounded wait for a tagged word (tag << 32 | float bits) of this call.
@@ -75,6 +80,8 @@ __device__ __forceinline__ float wait_tagged(const unsigned long long* w, unsign
 //      -- searches them in shared memory and computes p^alpha of the hits;
 //   4. the batch minimum of p^alpha goes through one atomicMin word and one
 //      grid barrier, then the weights.
+// With `rows`, step 3 also copies each hit's transition row to out_rows[k]
+// (one warp per round's hits, gather_core.cuh) before the barrier.
 // Thresholds are Philox draws (U in (0, 1]), so u_k lies within a rounding
 // margin of stratum k's interval (k T/B, (k+1) T/B]; the CTA evaluates the
 // strata whose interval meets its range widened by that margin.
@@ -89,6 +96,8 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
     __shared__ float s_bound[3];  // previous tile's last value, own last value, T
     __shared__ int s_krange[2];   // strata [k_lo, k_hi) this CTA evaluates
     __shared__ float s_min;
+    __shared__ int s_gk[THREADS / 32][32];  // a warp's hits for the row copy
+    __shared__ int s_gi[THREADS / 32][32];
 
     const int c = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
     const int n = static_cast<int>(S.scan.n);
@@ -200,21 +209,29 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
     float m = __int_as_float(0x7f800000);  // +inf
     int k_first = -1;                      // this thread's hit in the first round (weights from registers)
     float pa_first = 0.f;
-    for (int k0 = k_lo; k0 < k_hi; k0 += THREADS) {
+    const int warp = threadIdx.x >> 5;
+    for (int k0 = k_lo; k0 < k_hi; k0 += THREADS) {  // uniform bound: whole warps run every round
         const int k = k0 + threadIdx.x;
-        if (k >= k_hi) continue;
-        const float u = stratified_threshold(k, u01_open_closed(S.seed, S.offset + static_cast<uint64_t>(k)), fB, T);
-        if (!mine(u)) continue;
-        const int idx = min(lo + smem_lower_bound(s_cdf, 0, valid, u), n - 1);
-        S.out[k] = idx;
-        const float pa = pow_accurate(s_p[idx - lo], S.alpha, S.alpha_one);
-        m = fminf(m, pa);
-        if (k0 == k_lo) {
-            k_first = k;
-            pa_first = pa;
-        } else {
-            S.out_w[k] = pa;  // staged until the minimum is known
+        bool hit = false;
+        int idx = 0;
+        if (k < k_hi) {
+            const float u =
+                stratified_threshold(k, u01_open_closed(S.seed, S.offset + static_cast<uint64_t>(k)), fB, T);
+            if (mine(u)) {
+                hit = true;
+                idx = min(lo + smem_lower_bound(s_cdf, 0, valid, u), n - 1);
+                S.out[k] = idx;
+                const float pa = pow_accurate(s_p[idx - lo], S.alpha, S.alpha_one);
+                m = fminf(m, pa);
+                if (k0 == k_lo) {
+                    k_first = k;
+                    pa_first = pa;
+                } else {
+                    S.out_w[k] = pa;  // staged until the minimum is known
+                }
+            }
         }
+        if (S.rows) gather_hits_warp(S.rows, S.capacity, S.row_chunks, S.out_rows, hit, k, idx, s_gk[warp], s_gi[warp]);
     }
 
     // ---- 4. the batch minimum, then the weights --------------------------------
@@ -241,7 +258,8 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
 // 2048-item tiles, with Philox thresholds; PER_ERR_STATE (nothing launched)
 // when it does not apply.
 per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p, int n_upd, int B, uint64_t seed,
-                       uint64_t offset, const float* u01, float beta, int32_t* out, float* out_w, cudaStream_t s) {
+                       uint64_t offset, const float* u01, float beta, int32_t* out, float* out_w, const void* rows,
+                       int64_t row_bytes, void* out_rows, cudaStream_t s) {
     constexpr int TILE = kStepTile;
     const int64_t n = ctx->size;
     if (ctx->flags != PER_SCAN || u01 || !ctx->step_last || n < 1 || n > (int64_t(1) << 19)) return PER_ERR_STATE;
@@ -287,6 +305,9 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
     S.ticket = ctx->tickets + TK_STEP;
     S.last = ctx->step_last;
     S.step_min = ctx->step_min;
+    S.rows = static_cast<const uint4*>(rows);
+    S.row_chunks = static_cast<int>(row_bytes / 16);
+    S.out_rows = static_cast<uint4*>(out_rows);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles));
     cfg.blockDim = dim3(kStepThreads);

@@ -251,6 +251,33 @@ per_status per_step(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_p
                     uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta, int32_t* d_out_idx,
                     float* d_out_w, void* stream);
 
+/*
+ * per_gather -- copy the sampled transitions out of a replay buffer laid out
+ * as one fixed-size row per item (PufferLib PR #615 samples a minibatch of
+ * transitions by index from its prioritized buffers):
+ *   d_out[k][:] = d_rows[d_idx[k]][:]   for k in [0, B),
+ * rows of row_bytes bytes (16 <= row_bytes <= 2^20, a multiple of 16; d_rows
+ * and d_out 16-byte aligned; d_rows holds `capacity` rows).  An index outside
+ * [0, capacity) records PER_ERR_VALUE and leaves its output row unwritten.
+ * d_out must not overlap d_rows.
+ */
+per_status per_gather(per_ctx* ctx, const void* d_rows, int64_t row_bytes, const int32_t* d_idx, int32_t B,
+                      void* d_out, void* stream);
+
+/*
+ * per_step_gather -- per_step followed by per_gather(d_rows, row_bytes,
+ * d_out_idx, B, d_out_rows): one whole PER step that also returns the sampled
+ * transitions, with the same results as the two calls.  On per_step's fused
+ * path the copy runs inside the same launch (each CTA copies the rows of the
+ * samples it drew); otherwise the gather is a separate launch.  When nothing
+ * can be sampled (PER_ERR_EMPTY recorded) the output rows are unspecified.
+ * d_rows must not be NULL.  Errors as per_step and per_gather.
+ */
+per_status per_step_gather(per_ctx* ctx, const int32_t* d_upd_idx, const float* d_upd_prio, int32_t n_upd, int32_t B,
+                           uint64_t seed, uint64_t offset, int mode, const float* d_u01, float beta,
+                           int32_t* d_out_idx, float* d_out_w, const void* d_rows, int64_t row_bytes,
+                           void* d_out_rows, void* stream);
+
 /* per_total -- total priority (foxhunt "Integration" / total_priority):
  * mode PER_TREE reads tree[1], PER_SCAN reads cdf[n-1] (after per_build_cdf),
  * PER_RANK the rank CDF's last value sum_r q_r^alpha (after per_rank_build).
