@@ -53,7 +53,6 @@ struct per_ctx {
     int slot_n;
     unsigned* step_min;               // [3] per_step: call counter, then the batch minimum of p^alpha
                                       // (float bits) of even and odd calls
-    unsigned long long* step_last;    // [kMaxWaveTiles * kDescStride] per_step: tagged last CDF value per tile
     unsigned long long* scan_xsum;    // [kScanXsumWords] chunk sums of the two-pass scan
 
     // rank-based PER (PER_RANK): the radix sort's buffers, the order it

@@ -42,7 +42,6 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->slots);
     cudaFree(c->scan_xsum);
     cudaFree(c->step_min);
-    cudaFree(c->step_last);
     cudaFree(c->rank_keys0);
     cudaFree(c->rank_keys1);
     cudaFree(c->rank_vals1);
@@ -115,8 +114,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
              alloc_zero(&c->coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
              alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
              alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess &&
-             alloc_zero(&c->step_min, 3, s) == cudaSuccess &&
-             alloc_zero(&c->step_last, static_cast<size_t>(kMaxWaveTiles * kDescStride), s) == cudaSuccess;
+             alloc_zero(&c->step_min, 3, s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok && (flags & PER_RANK)) {
         const size_t cap = static_cast<size_t>(capacity);

@@ -163,7 +163,8 @@ __device__ __forceinline__ void slice_values(const ScanParams& P, const float* b
 // Writes one run of a slice: hi + (lo + local) with the slice's carry
 // cy = (hi, lo, fl32(E), fl32(E')), clamped to [fl32(E), fl32(E')] when the
 // run's first or last value falls outside (the values are monotone along the
-// run), and its coarse-index entries.  FAST: full tile, 32-byte aligned cdf.
+// run), and its coarse-index entries; item n-1 gets fl32(E') itself, the
+// correctly rounded exact total.  FAST: full tile, 32-byte aligned cdf.
 template <bool FAST, int TILE>
 __device__ __forceinline__ void emit_run(const ScanParams& P, float (&v)[8], float4 cy, int64_t tile_base, int i0,
                                          int valid, int lane) {
@@ -174,6 +175,11 @@ __device__ __forceinline__ void emit_run(const ScanParams& P, float (&v)[8], flo
     if (!(first >= cy.z && last <= cy.w)) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = fminf(fmaxf(v[e], cy.z), cy.w);
+    }
+    if (tile_base + i0 <= P.n - 1 && P.n - 1 < tile_base + i0 + 8) {  // the last value is fl32(E_total) exactly
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (tile_base + i0 + e == P.n - 1) v[e] = cy.w;
     }
     // coarse[k] = cdf[min(64k + 63, n - 1)].  In a full tile the entries are
     // the items 64k + 63 (n - 1 is one when it ends the tile): the last item
@@ -258,10 +264,6 @@ struct TwoPassLoads {
 // slots[2][kScanMaxGrid][2] | totals[2][2] | ready.  Parity = segment & 1.
 constexpr int64_t kXsumTotals = 4 * kScanMaxGrid;
 constexpr int64_t kXsumReady = kXsumTotals + 4;
-
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 
 // Exchange of the two-pass kernel, run by the compute warps of every CTA of
 // the co-resident grid once per segment, after each CTA has written its

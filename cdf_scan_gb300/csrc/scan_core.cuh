@@ -122,9 +122,12 @@ __device__ __forceinline__ ScanState scan_state(const ScanParams& P) {
 // Gives up after kWaitLimitNs (ST_TIMEOUT) and returns what it has.
 constexpr int kLookQ = 16;  // aggregates per lane per chunk (512 tiles)
 
+// With `below`, also the sum over tiles [lo, split) and, in *before, the fp32
+// sum word of tile split - 1 (when split > lo).
 __device__ u128 sum_aggregates(const ScanState& S, int64_t lo, int64_t hi, unsigned tag_agg, int lane,
-                               int* status) {
-    u128 acc = 0;
+                               int* status, int64_t split = -1, u128* below = nullptr, float* before = nullptr) {
+    u128 acc = 0, acc_below = 0;  // acc_below: the tiles before `split` (when `below` is given)
+    float pv = 0.f;               // the word of tile split - 1, on the lane that reads it
     uint64_t t0 = 0;
     for (int64_t j0 = lo; j0 < hi; j0 += 32 * kLookQ) {
         unsigned pending = 0;
@@ -140,21 +143,27 @@ __device__ u128 sum_aggregates(const ScanState& S, int64_t lo, int64_t hi, unsig
             for (int q = 0; q < kLookQ; ++q) {
                 if (((pending >> q) & 1u) && static_cast<unsigned>(w[q] >> 32) == tag_agg) {
                     bool err = false;  // range errors are flagged by the tile's owner
-                    acc += to_fixed(__uint_as_float(static_cast<unsigned>(w[q])), err);
+                    const u128 a = to_fixed(__uint_as_float(static_cast<unsigned>(w[q])), err);
+                    acc += a;
+                    if (j0 + lane + 32 * q < split) acc_below += a;
+                    if (j0 + lane + 32 * q == split - 1) pv = __uint_as_float(static_cast<unsigned>(w[q]));
                     pending &= ~(1u << q);
                 }
             }
             if (!__any_sync(PER_FULL_MASK, pending != 0u)) break;
-            const uint64_t now = global_ns();
+            // lane 0's clock for the whole warp, so every lane takes the same branch
+            const uint64_t now = __shfl_sync(PER_FULL_MASK, global_ns(), 0);
             if (t0 == 0) {
                 t0 = now;
             } else if (now - t0 > kWaitLimitNs) {
                 if (lane == 0) atomicOr(status, ST_TIMEOUT);
-                return warp_sum_u128(acc);
+                break;
             }
             __nanosleep(128);
         }
     }
+    if (below) *below = warp_sum_u128(acc_below);
+    if (before && split > lo) *before = __shfl_sync(PER_FULL_MASK, pv, static_cast<int>((split - 1 - lo) & 31));
     return warp_sum_u128(acc);
 }
 
@@ -184,13 +193,23 @@ __device__ __forceinline__ void advance_scan_epoch(const ScanParams& P, unsigned
 // as fp32 hi + lo; the clamp bounds are monotone in c, so the CDF is
 // non-decreasing.  `src` points at the tile's first priority (global memory,
 // or a shared-memory copy); when `s_out` is not null the tile's CDF values
-// are also left there (shared memory, TILE floats).  Returns the epoch the
-// tile was tagged with; the caller advances it once every tile is done
-// (advance_scan_epoch).
+// are also left there (shared memory, TILE floats).  The CDF's last value
+// cdf[n-1] is the correctly rounded exact total fl32(E_G) (the last tile's
+// upper clamp bound).  When `s_bounds` is not null (shared memory, 3
+// floats), warp 0 also sums the words of every tile (P.num_tiles of them)
+// and leaves there, without waiting for any other tile's local scan:
+//   [0] the previous tile's last CDF value (c > 0): a full tile's last local
+//       value is its fp32 sum word (both are the same left fold of the warp
+//       totals), so it is clamp(hi' + (lo' + a_{c-1}), fl32(E_{c-1}),
+//       fl32(E_c)) with E_{c-1} = E_c - a_{c-1}, as that tile writes it;
+//   [1] this tile's last CDF value, the same way;
+//   [2] T = cdf[n-1] = fl32(E_G).
+// Returns the epoch the tile was tagged with; the caller advances it once
+// every tile is done (advance_scan_epoch).
 
 template <int THREADS>
 __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t c, const float* src,
-                                                   float* s_out) {
+                                                   float* s_out, float* s_bounds = nullptr) {
     constexpr int ITEMS = 8;
     constexpr int WARPS = THREADS / 32;
     constexpr int TILE = THREADS * ITEMS;
@@ -257,13 +276,31 @@ __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t 
         *reinterpret_cast<volatile unsigned long long*>(P.desc + c * kDescStride) =
             (static_cast<unsigned long long>(tag_agg) << 32) | __float_as_uint(agg);
     if (warp == 0) {
-        const u128 excl = sum_aggregates(scan_state(P), 0, c, tag_agg, lane, P.status);
+        u128 excl = 0, total = 0;
+        float a_prev = 0.f;
+        if (s_bounds)  // every tile's word: the total, and the tiles before c on the way
+            total = sum_aggregates(scan_state(P), 0, P.num_tiles, tag_agg, lane, P.status, c, &excl, &a_prev);
+        else
+            excl = sum_aggregates(scan_state(P), 0, c, tag_agg, lane, P.status);
         if (lane == 0) {
             bool range_err = false;
             const u128 a_fix = to_fixed(agg, range_err);
             float hi, lo;
             fixed_to_float2(excl, hi, lo);
-            s_carry = make_float4(hi, lo, hi, fixed_to_float(excl + a_fix));
+            const float e_next = fixed_to_float(excl + a_fix);
+            s_carry = make_float4(hi, lo, hi, e_next);
+            if (s_bounds) {
+                const float T = fixed_to_float(total);
+                if (c > 0) {
+                    bool unused = false;
+                    const u128 e_prev = excl - to_fixed(a_prev, unused);
+                    float hp, lp;
+                    fixed_to_float2(e_prev, hp, lp);
+                    s_bounds[0] = fminf(fmaxf(hp + (lp + a_prev), hp), hi);
+                }
+                s_bounds[1] = base + TILE >= P.n ? T : fminf(fmaxf(hi + (lo + agg), hi), e_next);
+                s_bounds[2] = T;
+            }
             if (range_err) atomicOr(P.status, ST_RANGE);
         }
     }
@@ -273,7 +310,10 @@ __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t 
     const float4 cy = s_carry;
     float o[ITEMS];
 #pragma unroll
-    for (int e = 0; e < ITEMS; ++e) o[e] = fminf(fmaxf(cy.x + (cy.y + (off + v[e])), cy.z), cy.w);
+    for (int e = 0; e < ITEMS; ++e) {
+        o[e] = fminf(fmaxf(cy.x + (cy.y + (off + v[e])), cy.z), cy.w);
+        if (base + i0 + e == P.n - 1) o[e] = cy.w;  // the last value is fl32(E_G) exactly
+    }
     if (s_out) {  // the tile's CDF values for the caller (shared memory)
         *reinterpret_cast<float4*>(s_out + i0) = make_float4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<float4*>(s_out + i0 + 4) = make_float4(o[4], o[5], o[6], o[7]);

@@ -38,30 +38,12 @@ struct StepParams {
     int64_t capacity;
     float* prio;                 // the buffer the updates write (== scan.p)
     unsigned long long* ticket;  // grid-barrier word
-    unsigned long long* last;    // [tile * kDescStride]: tagged last CDF value of each tile
     unsigned* step_min;          // call counter, then the batch-minimum word of even and odd calls
     // optional copy of the sampled transitions: out_rows[k] = rows[out[k]]
     const uint4* rows;           // [capacity][row_chunks] x 16 bytes, or nullptr
     int row_chunks;
     uint4* out_rows;             // [B][row_chunks] x 16 bytes
 };
-
-// Bounded wait for a tagged word (tag << 32 | float bits) of this call.
-__device__ __forceinline__ float wait_tagged(const unsigned long long* w, unsigned tag, int* status) {
-    uint64_t t0 = 0;
-    for (;;) {
-        const unsigned long long x = ld_relaxed_u64(w);
-        if (static_cast<unsigned>(x >> 32) == tag) return __uint_as_float(static_cast<unsigned>(x));
-        const uint64_t now = global_ns();
-        if (t0 == 0) {
-            t0 = now;
-        } else if (now - t0 > kWaitLimitNs) {
-            atomicOr(status, ST_TIMEOUT);
-            return __int_as_float(0x7fc00000);
-        }
-        __nanosleep(32);
-    }
-}
 
 // CTA c owns items [c * TILE, (c + 1) * TILE) (the grid is exactly the
 // tiles; capacity <= tiles * TILE when there are updates):
@@ -72,12 +54,15 @@ __device__ __forceinline__ float wait_tagged(const unsigned long long* w, unsign
 //      to the buffer and to the shared copy -- no other CTA touches these
 //      items, so no grid barrier;
 //   2. the tile is scanned from the shared copy (wave_scan_tile); its CDF
-//      values stay in shared memory and its last one is published as a
-//      tagged word;
-//   3. with T = the last tile's last value and the previous tile's last
-//      value, the CTA takes exactly the strata k whose threshold u_k falls
-//      in (previous last, own last] -- their lower_bound lies in this tile
-//      -- searches them in shared memory and computes p^alpha of the hits;
+//      values stay in shared memory, and warp 0's lookback, which reads every
+//      tile's sum word, also gives the previous tile's last CDF value, this
+//      tile's and T;
+//   3. with T = cdf[n-1] = fl32 of the exact total and the previous tile's
+//      last value (neither waits for another tile's scan), the CTA takes
+//      exactly the strata k whose
+//      threshold u_k falls in (previous last, own last] -- their lower_bound
+//      lies in this tile -- searches them in shared memory and computes
+//      p^alpha of the hits;
 //   4. the batch minimum of p^alpha goes through one atomicMin word and one
 //      grid barrier, then the weights.
 // With `rows`, step 3 also copies each hit's transition row to out_rows[k]
@@ -160,36 +145,33 @@ __global__ void __launch_bounds__(kStepThreads) per_step_kernel(StepParams S) {
     if (bad) atomicOr(status, ST_VALUE);
 
     // ---- 2. the scan of this tile ---------------------------------------------
-    const unsigned epoch = wave_scan_tile<THREADS>(S.scan, c, s_p, s_cdf);
+    // s_bound = the previous tile's last CDF value, this tile's, and T, from
+    // warp 0's lookback alone (no other tile's local scan is waited for)
+    const unsigned epoch = wave_scan_tile<THREADS>(S.scan, c, s_p, s_cdf, s_bound);
     __syncthreads();  // s_cdf complete
-    const unsigned tag = 2u * epoch + 1u;
     if (threadIdx.x == 0) {
-        const float own = s_cdf[valid - 1];
-        *reinterpret_cast<volatile unsigned long long*>(S.last + static_cast<int64_t>(c) * kDescStride) =
-            (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(own);
-        s_bound[0] = c == 0 ? -__int_as_float(0x7f800000)
-                            : wait_tagged(S.last + static_cast<int64_t>(c - 1) * kDescStride, tag, status);
-        s_bound[1] = own;
-        const float T = c == G - 1 ? own : wait_tagged(S.last + static_cast<int64_t>(G - 1) * kDescStride, tag, status);
-        s_bound[2] = T;
+        if (c == 0) s_bound[0] = -__int_as_float(0x7f800000);
+        const float own = s_bound[1], T = s_bound[2];
         // strata whose interval (k T/B, (k+1) T/B], widened by the rounding
-        // margin of the threshold, meets (prev, own] (once, in fp64)
+        // margin of the threshold, meets (prev, own].  k = x B / T in fp32:
+        // fl32(B / T) and the product each err by at most 2^-24 relative, so
+        // for x <= T the computed k is within B * 2^-23 <= 2 of the exact one
+        // (B <= 2^24), covered by 3 more strata of margin; the strata are
+        // then decided one by one (mine), so a wider range costs only time.
         const int B = S.B;
-        const int margin = 2 + (B >> 20);
-        const double scale = static_cast<double>(B) / static_cast<double>(T);
-        s_krange[0] = c == 0 ? 0 : max(0, static_cast<int>(floor(static_cast<double>(s_bound[0]) * scale)) - margin);
-        s_krange[1] = c == G - 1 ? B : min(B, static_cast<int>(ceil(static_cast<double>(own) * scale)) + margin + 1);
+        const int margin = 2 + (B >> 20) + 3;
+        const float scale = __fdiv_rn(static_cast<float>(B), T);
+        s_krange[0] = c == 0 ? 0 : max(0, __float2int_rd(__fmul_rn(s_bound[0], scale)) - margin);
+        s_krange[1] = c == G - 1 ? B : min(B, __float2int_ru(__fmul_rn(own, scale)) + margin + 1);
     }
     __syncthreads();
     const float prev = s_bound[0], own = s_bound[1], T = s_bound[2];
     const int B = S.B;
-    // every tile's scan is done once T is known (the last tile's carry needed
-    // all of them), so the epoch and the call counter may move on
+    // once T is known every tile has read the epoch and published its word
+    // (T needed all of them), so the epoch and the call counter may move on
     auto finish = [&]() {
         if (c == 0 && threadIdx.x == 0) {
             advance_scan_epoch(S.scan, epoch);
-            if (epoch + 1u >= (1u << 30))  // the epoch wrapped: clear the tagged words once
-                for (int64_t i = 0; i < kMaxWaveTiles; ++i) S.last[i * kDescStride] = 0ull;
             S.step_min[1 + (s_parity ^ 1u)] = 0x7f800000u;  // +inf for the next call
             S.step_min[0] = S.step_min[0] + 1u;
         }
@@ -262,7 +244,7 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
                        int64_t row_bytes, void* out_rows, cudaStream_t s) {
     constexpr int TILE = kStepTile;
     const int64_t n = ctx->size;
-    if (ctx->flags != PER_SCAN || u01 || !ctx->step_last || n < 1 || n > (int64_t(1) << 19)) return PER_ERR_STATE;
+    if (ctx->flags != PER_SCAN || u01 || !ctx->step_min || n < 1 || n > (int64_t(1) << 19)) return PER_ERR_STATE;
     const int64_t tiles = (n + TILE - 1) / TILE;
     if (tiles > ctx->scan_desc_tiles) return PER_ERR_STATE;
     // every index an update may name lies in some CTA's tile
@@ -303,7 +285,6 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
     S.capacity = ctx->capacity;
     S.prio = ctx->prio;
     S.ticket = ctx->tickets + TK_STEP;
-    S.last = ctx->step_last;
     S.step_min = ctx->step_min;
     S.rows = static_cast<const uint4*>(rows);
     S.row_chunks = static_cast<int>(row_bytes / 16);
