@@ -282,22 +282,24 @@ __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t 
             total = sum_aggregates(scan_state(P), 0, P.num_tiles, tag_agg, lane, P.status, c, &excl, &a_prev);
         else
             excl = sum_aggregates(scan_state(P), 0, c, tag_agg, lane, P.status);
+        // the conversions to fp32 run side by side on lanes 0-3 (the u128
+        // values are the same on every lane): lane 0 the carry E_c, lane 1
+        // E_{c+1}, lane 2 the total, lane 3 E_{c-1} = E_c - a_{c-1}
+        bool range_err = false, unused = false;
+        const u128 a_fix = to_fixed(agg, range_err);
+        const u128 x = lane == 1 ? excl + a_fix
+                     : lane == 2 ? total
+                     : lane == 3 ? excl - to_fixed(a_prev, unused) : excl;
+        float xh, xl;
+        fixed_to_float2(x, xh, xl);
+        const float hi = __shfl_sync(PER_FULL_MASK, xh, 0), lo = __shfl_sync(PER_FULL_MASK, xl, 0);
+        const float e_next = __shfl_sync(PER_FULL_MASK, xh, 1);
+        const float T = __shfl_sync(PER_FULL_MASK, xh, 2);
+        const float hp = __shfl_sync(PER_FULL_MASK, xh, 3), lp = __shfl_sync(PER_FULL_MASK, xl, 3);
         if (lane == 0) {
-            bool range_err = false;
-            const u128 a_fix = to_fixed(agg, range_err);
-            float hi, lo;
-            fixed_to_float2(excl, hi, lo);
-            const float e_next = fixed_to_float(excl + a_fix);
             s_carry = make_float4(hi, lo, hi, e_next);
             if (s_bounds) {
-                const float T = fixed_to_float(total);
-                if (c > 0) {
-                    bool unused = false;
-                    const u128 e_prev = excl - to_fixed(a_prev, unused);
-                    float hp, lp;
-                    fixed_to_float2(e_prev, hp, lp);
-                    s_bounds[0] = fminf(fmaxf(hp + (lp + a_prev), hp), hi);
-                }
+                if (c > 0) s_bounds[0] = fminf(fmaxf(hp + (lp + a_prev), hp), hi);
                 s_bounds[1] = base + TILE >= P.n ? T : fminf(fmaxf(hi + (lo + agg), hi), e_next);
                 s_bounds[2] = T;
             }

@@ -314,6 +314,32 @@ def test_per_step_equals_the_separate_calls(N, B, n_upd, flags):
     assert per.per_check(b.handle) == 0
 
 
+def test_per_step_heavy_duplicates_across_rounds():
+    """20,000 updates (several rounds of the fused update) that all hit 300
+    items around a tile boundary: the last occurrence of each index wins, as
+    in per_update and in the oracle."""
+    N, B, n_upd = 262144, 4096, 20000
+    g = workloads.rng(506, 1)
+    p = workloads.abs_normal(N, g)
+    a, b = new_ctx(p, 0.6, SCAN), new_ctx(p, 0.6, SCAN)
+    idx = (2048 * 37 - 150 + g.integers(0, 300, size=n_upd)).astype(np.int32)
+    newp = workloads.abs_normal(n_upd, g)
+    ia = torch.empty(B, dtype=torch.int32, device="cuda")
+    wa = torch.empty(B, dtype=torch.float32, device="cuda")
+    ib = torch.empty(B, dtype=torch.int32, device="cuda")
+    wb = torch.empty(B, dtype=torch.float32, device="cuda")
+    per.per_step(a.handle, dev(idx), dev(newp), B, 3, 0, SCAN, 0.4, ia, wa)
+    per.per_update(b.handle, dev(idx), dev(newp))
+    per.per_build_cdf(b.handle)
+    per.per_sample_weighted(b.handle, B, 3, 0, SCAN, 0.4, ib, wb)
+    want = oracle.apply_updates(p, idx, newp)
+    assert np.array_equal(host(per.read_priorities(a.handle, N)), want)
+    assert np.array_equal(host(per.read_priorities(b.handle, N)), want)
+    assert np.array_equal(host(ia), host(ib))
+    assert np.array_equal(host(wa), host(wb))
+    assert per.per_check(a.handle) == 0
+
+
 def test_minibatch_loop_with_per_step_matches_oracle():
     """The minibatch workload through per_step: round r applies round r-1's
     updates, rebuilds and samples; checked against the oracle every round."""
