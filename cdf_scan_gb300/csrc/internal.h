@@ -98,8 +98,13 @@ constexpr int kRadixDigits = 256;
 constexpr int kRankTile = 4096;
 constexpr int kRankSmallTile = 2048;
 constexpr int64_t kRankMaxN = int64_t(1) << 24;
-// Words of the per-tile digit counts for `cap` items (either tiling).
-inline int64_t rank_count_words(int64_t cap) { return kRadixDigits * ((cap + kRankSmallTile - 1) / kRankSmallTile); }
+// Words of the per-tile digit counts for `cap` items: 32-bit counts of
+// 4096-key tiles, or 16-bit counts of up to 128 2048-key tiles in rows padded
+// to 8 tiles (at least 256 x 128 halves).
+inline int64_t rank_count_words(int64_t cap) {
+    const int64_t tiles = (cap + kRankSmallTile - 1) / kRankSmallTile;
+    return kRadixDigits * (tiles > 64 ? tiles : 64);
+}
 
 // Host-side launch accounting (per_launch_count).
 void per_note_launch(int n = 1);

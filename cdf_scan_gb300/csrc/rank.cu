@@ -29,8 +29,10 @@
 //             (digit-major), one CTA per digit scanning its row across the
 //             tiles, then the tile pass above;
 //   small sizes -- one cooperative launch for all four passes: each CTA
-//             publishes its tile's digit counts, and after a grid barrier
-//             sums the counts of all tiles itself.
+//             publishes its tile's digit counts (16 bits each, digit-major),
+//             and after a grid barrier sums the counts of all tiles itself:
+//             thread d reads digit d's row with at most 16 independent
+//             16-byte loads, so the sum costs one round trip to L2.
 #include <algorithm>
 
 #include "common.cuh"
@@ -59,7 +61,8 @@ struct SortParams {
     int32_t* vals1;
     int32_t* order;
     int32_t* rank_of;
-    unsigned* counts;  // large sizes: [kRadixDigits][tiles]; small: [tiles][kRadixDigits]
+    unsigned* counts;  // large sizes: [kRadixDigits][tiles]; small: 16-bit, [kRadixDigits][row], row = tiles
+                       // rounded up to 8
     unsigned* totals;  // [kRadixDigits] (large sizes)
     int* status;
     unsigned long long* ticket;
@@ -390,17 +393,24 @@ __global__ void __launch_bounds__(kSortThreads) radix_sort_small_kernel(SortPara
         const unsigned cnt_d = warp_offsets(sm);
         unsigned tile_total = 0u, all = 0u;
         const unsigned start_d = block_excl_scan(cnt_d, sm.w, &tile_total);
-        S.counts[blockIdx.x * kRadixDigits + d] = cnt_d;
+        const int row = (S.tiles + 7) & ~7;
+        unsigned short* c16 = reinterpret_cast<unsigned short*>(S.counts);
+        c16[d * row + static_cast<int>(blockIdx.x)] = static_cast<unsigned short>(cnt_d);  // <= 2048
         if (!grid_barrier(S.ticket, S.status, ST_TIMEOUT)) return;
+        const uint4* rp = reinterpret_cast<const uint4*>(c16 + d * row);
+        uint4 q[kSmallMaxTiles / 8];
+#pragma unroll
+        for (int u = 0; u < kSmallMaxTiles / 8; ++u) q[u] = 8 * u < S.tiles ? __ldcg(rp + u) : make_uint4(0u, 0u, 0u, 0u);
         unsigned before = 0u, total = 0u;
-        for (int t0 = 0; t0 < S.tiles; t0 += 16) {  // 16 independent loads in flight
-            unsigned c[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) c[e] = t0 + e < S.tiles ? __ldcg(S.counts + (t0 + e) * kRadixDigits + d) : 0u;
+        for (int u = 0; u < kSmallMaxTiles / 8; ++u) {
+            const unsigned w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                before += t0 + e < static_cast<int>(blockIdx.x) ? c[e] : 0u;
-                total += c[e];
+            for (int h = 0; h < 8; ++h) {
+                const int t = 8 * u + h;
+                const unsigned v = (w[h >> 1] >> (16 * (h & 1))) & 0xffffu;
+                if (t < S.tiles) total += v;
+                if (t < static_cast<int>(blockIdx.x)) before += v;
             }
         }
         const unsigned digit_start = block_excl_scan(total, sm.w, &all);
