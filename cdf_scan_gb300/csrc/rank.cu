@@ -246,12 +246,12 @@ __device__ __forceinline__ void place_and_write(const SortParams& S, const PassI
 
 // ---- large sizes: three launches per pass ----------------------------------
 
-// Per-tile digit counts, stored digit-major: counts[d][tile].  Each warp keeps
-// its own sub-histogram and adds one count per peer group, so equal digits
-// (the exponent byte of similar priorities) do not serialise on one counter.
+// Per-tile digit counts, stored digit-major: counts[d][tile], from per-warp
+// sub-histograms of shared-memory atomics (plain atomics measured faster here
+// than adding once per peer group found with ballots or __match_any_sync).
 __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) {
     __shared__ unsigned h[kSortWarps][kRadixDigits];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&h[0][0])[i] = 0u;
     __syncthreads();
     const PassIO io = pass_io(S, S.pass);
@@ -293,12 +293,8 @@ __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) 
         }
     }
 #pragma unroll
-    for (int c = 0; c < kBigItems; ++c) {
-        const unsigned d = ok[c] ? (k[c] >> io.shift) & 255u : 0u;
-        const unsigned peers = digit_peers(d, ok[c]);
-        if (ok[c] && lane == __ffs(peers) - 1) h[warp][d] += __popc(peers);
-        __syncwarp();
-    }
+    for (int c = 0; c < kBigItems; ++c)
+        if (ok[c]) atomicAdd(&h[warp][(k[c] >> io.shift) & 255u], 1u);
     if (bad) atomicOr(S.status, ST_VALUE);
     __syncthreads();
     unsigned sum = 0u;
