@@ -71,25 +71,18 @@ __device__ __forceinline__ int count_le(float c, float U, int P, float fP, float
 }
 
 // count_le for a power-of-two P without loops.  u_j <= c exactly when
-// fl32(j + U) <= C = c * P (both products by a power of two are exact), and
-// fl32(j + U) is non-decreasing in j with fl32(j + U) <= C for j + U <= C - 1
-// and > C for j + U >= C + 1 (C < 2^24), so the last such j lies within one of
-// floor(C - U); the fp32 rounding of C - U moves the guess by at most one more:
-// two exact checks each way settle it.
+// fl32(j + U) <= C = c * P (both products by a power of two are exact).  With
+// f = floor(C): every j <= f - 2 counts, since fl32(j + U) <= j + 1 <= C (j + 1
+// is exact below 2^24 and U < 1); every j >= f + 1 does not, since
+// fl32(j + U) >= j > C.  So two exact tests, at j = f - 1 and j = f, settle
+// the count (the test is monotone in j, so the two indicators add up).
 __device__ __forceinline__ int count_le_pow2(float c, float U, int P, float fP) {
     const float C = __fmul_rn(c, fP);
-    const float g = __fsub_rn(C, U);
-    int j;
-    if (!(g >= 0.f)) j = -1;
-    else if (g >= fP) j = P - 1;
-    else j = static_cast<int>(g);
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-        if (j + 1 < P && __fadd_rn(__int2float_rn(j + 1), U) <= C) ++j;
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-        if (j >= 0 && __fadd_rn(__int2float_rn(j), U) > C) --j;
-    return j + 1;
+    const int f = __float2int_rd(C);  // C >= 0 (NaN gives some f; the result stays in [0, P])
+    int n = min(max(f - 1, 0), P);
+    if (f - 1 >= 0 && f - 1 < P && __fadd_rn(__int2float_rn(f - 1), U) <= C) ++n;
+    if (f >= 0 && f < P && __fadd_rn(__int2float_rn(f), U) <= C) ++n;
+    return n;
 }
 
 // floor(w * 2^40) for w = exp(x - m) in [0, 1], from the float's exponent and
