@@ -61,6 +61,28 @@ def env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def rank_seed(rank):
+    """Workload seed of one replica: every rank draws its own buffer."""
+    return W["seed"] + 1000 * rank
+
+
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest value of x over the ranks of the default process group
+    (x itself without one): the job's time is its slowest replica's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(steps, world, t_ms):
+    """Samples per second of the whole job: every rank's samples over the
+    slowest rank's time."""
+    return steps * ROUNDS * B * world / (t_ms / 1e3)
+
+
 def config_dict(n_gpus):
     return {"workload": WORKLOAD, "N": N, "B": B, "rounds_per_step": ROUNDS, "alpha": ALPHA, "beta": BETA,
             "parallelism": f"replicas x{n_gpus}", "l2": "flushed (512 MiB write) between timed steps"}
@@ -141,7 +163,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local_rank)
-    seed = W["seed"] + 1000 * rank
+    seed = rank_seed(rank)
     p0 = workloads.minibatch_priorities(seed=seed)
     newp = np.stack([workloads.minibatch_new_priorities(r, seed=seed) for r in range(ROUNDS)])
     d_p0 = torch.from_numpy(p0).to(dev)
@@ -241,16 +263,8 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status after timing: {per.per_status_str(status)}")
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    t_ms = max_over_ranks(t_ms)
-    e2e_ms = max_over_ranks(e2e_ms)
-    samples = args.steps * ROUNDS * B * world
+    t_ms = max_over_ranks(t_ms, dist, dev)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     result = None
     if rank == 0:
         peak, peak_kind = load_peaks()
@@ -263,11 +277,11 @@ def run_ours(args, rank, world, local_rank):
                     "traffic": traffic_for(name), "avg_launch_us": round(avg_s * 1e6, 3),
                     "algorithmic_bytes_per_launch": algo}
         result = {
-            "metric": METRIC, "value": samples / (t_ms / 1e3), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": job_throughput(args.steps, world, t_ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded Philox draws; no dataset)", "config": config_dict(world),
-            "e2e": {"value": samples / (e2e_ms / 1e3), "unit": UNIT,
+            "e2e": {"value": job_throughput(args.steps, world, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": int(ROUNDS * B * 4),
                     "d2h_bytes_per_step": int(ROUNDS * B * 8)},
             "gpu_launches": int(kernels_per_step * args.steps),
