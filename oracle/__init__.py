@@ -11,8 +11,8 @@ Each wrapper names the page and section its C function follows.
 
 Parity pins: every function here is checked by ``tests/test_oracle.py``
 against something other than itself (closed forms, exact integer sums,
-brute-force enumeration, the published Philox known-answer vectors, numpy's
-own Philox4x64).  No function is "parity unpinned".
+brute-force enumeration, cuRAND's host-side Philox4x32-10 generator and numpy's
+Philox4x64 -- two independent implementations of the published bijection).  No function is "parity unpinned".
 """
 from __future__ import annotations
 

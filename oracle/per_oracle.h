@@ -26,8 +26,8 @@
  *
  * Parity pins: every function below is pinned by a CPU test in
  * tests/test_oracle.py against something other than itself (closed forms,
- * exact integer arithmetic, brute-force enumeration, published known-answer
- * vectors, numpy's independent Philox4x64 implementation).
+ * exact integer arithmetic, brute-force enumeration, and the independent
+ * Philox implementations of cuRAND's host generator (4x32) and numpy (4x64)).
  */
 #ifndef PER_ORACLE_H
 #define PER_ORACLE_H
