@@ -380,6 +380,25 @@ def extras(per, torch, dev, peak):
     if per.per_check(ctx.handle) != 0:
         out["stress_build_cdf"]["status"] = "device status not clean"
     ctx.close()
+    # comparator, context only: the same CDF and sampling with library kernels
+    # (torch.cumsum of p**alpha in fp32, torch.searchsorted of the stratified
+    # thresholds), timed the same way
+    tp = torch.from_numpy(workloads.stress_priorities()).to(dev)
+    tcdf = torch.empty_like(tp)
+    tu = ((torch.arange(S["B"], device=dev, dtype=torch.float32) + 0.5) / S["B"])
+    tidx = torch.empty(S["B"], dtype=torch.int64, device=dev)
+
+    def torch_cdf():
+        torch.cumsum(tp.pow(S["alpha"]), 0, out=tcdf)
+
+    def torch_sample():
+        torch.searchsorted(tcdf, tu * tcdf[-1], out=tidx)
+    torch_cdf()
+    us_tc = time_graph(graph_of(torch_cdf), 30)
+    us_ts = time_graph(graph_of(torch_sample), 20)
+    out["torch_comparator_16M"] = {"build_cdf_us": round(us_tc, 2), "sample_us": round(us_ts, 2),
+                                   "note": "torch.cumsum(p**alpha) and torch.searchsorted on the stress input "
+                                           "(library kernels); context only", "l2": "flushed before each rep"}
 
     T = workloads.TREE
     cap = T["capacity"]
