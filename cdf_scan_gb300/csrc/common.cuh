@@ -35,12 +35,6 @@ __device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
     return v;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -418,16 +412,6 @@ __device__ __forceinline__ void pow_alpha_warp(float (&v)[N], float alpha, float
         if (!(x >= 0.f)) bad = true;
         v[e] = fabsf(v[e]) < lim ? hw_ex2_ftz(__fmul_rn(alpha, v[e])) : pow_split(x, alpha);
     }
-}
-
-// p^alpha; alpha == 1 skips the power (exact).  `bad` is set for negative
-// and NaN inputs.
-__device__ __forceinline__ float pow_alpha(float x, float alpha, bool identity, bool& bad) {
-    if (identity) {
-        bad |= !(x >= 0.f);
-        return x;
-    }
-    return pow_fast(x, alpha, bad);
 }
 
 // Accurate power (CUDA powf), for quantities with a tight error budget.
