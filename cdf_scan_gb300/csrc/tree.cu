@@ -46,6 +46,45 @@ struct TreeSampleParams {
     int* status;
 };
 
+// One step of the descent (foxhunt "Operations" / Sample, with the guard of
+// the zero-sum right child): from node j with child sums L and R.
+__device__ __forceinline__ void descend_step(float& u, unsigned& j, float L, float R) {
+    if (u > L && R > 0.f) {
+        u = __fsub_rn(u, L);
+        j = 2 * j + 1;
+    } else {
+        j = 2 * j;
+    }
+}
+
+// The N sums of one contiguous level run (N = 4, 8, 16: float4 loads; the
+// run starts at a multiple of N floats, so they are aligned).
+template <int N>
+__device__ __forceinline__ void load_run(const float* p, float (&r)[N]) {
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(p) + q);
+        r[4 * q] = v.x;
+        r[4 * q + 1] = v.y;
+        r[4 * q + 2] = v.z;
+        r[4 * q + 3] = v.w;
+    }
+}
+
+// One descent step inside a loaded run: the node at position r of the level
+// above has its children at 2r and 2r + 1 of this run (selects, no indexed
+// register access).
+template <int N>
+__device__ __forceinline__ void descend_run(float& u, unsigned& r, const float (&run)[N]) {
+    float L = run[0], R = run[1];
+#pragma unroll
+    for (int q = 1; q < N / 2; ++q) {
+        L = r == static_cast<unsigned>(q) ? run[2 * q] : L;
+        R = r == static_cast<unsigned>(q) ? run[2 * q + 1] : R;
+    }
+    descend_step(u, r, L, R);
+}
+
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) sample_tree_kernel(TreeSampleParams P) {
     extern __shared__ __align__(128) float s_top[];
@@ -72,24 +111,30 @@ __global__ void __launch_bounds__(THREADS) sample_tree_kernel(TreeSampleParams P
         P.out[k] = 0;
         return;
     }
-    const unsigned staged = 1u << P.staged_levels;
     unsigned j = 1;
-    for (int d = 0; d < P.log2cap; ++d) {
-        float L, R;
-        if (j < staged) {
-            L = s_top[2 * j];
-            R = s_top[2 * j + 1];
-        } else {
-            const float2 lr = __ldg(reinterpret_cast<const float2*>(P.tree + 2 * static_cast<size_t>(j)));
-            L = lr.x;
-            R = lr.y;
-        }
-        if (u > L && R > 0.f) {
-            u = __fsub_rn(u, L);
-            j = 2 * j + 1;
-        } else {
-            j = 2 * j;
-        }
+    int d = 0;
+    for (; d < P.staged_levels && d < P.log2cap; ++d)  // the staged levels, from shared memory
+        descend_step(u, j, s_top[2 * j], s_top[2 * j + 1]);
+    // the rest in groups of up to 4 levels: the nodes e levels below j are
+    // the contiguous run [j * 2^e, (j + 1) * 2^e), so the 2 + 4 + 8 + 16
+    // sums any 4 decisions can need come in one round of independent loads
+    while (d < P.log2cap) {
+        const int g = min(4, P.log2cap - d);
+        const float* t = P.tree;
+        float r1[2], r2[4], r3[8], r4[16];
+        const float2 a = __ldg(reinterpret_cast<const float2*>(t + (static_cast<size_t>(j) << 1)));
+        r1[0] = a.x;
+        r1[1] = a.y;
+        if (g >= 2) load_run<4>(t + (static_cast<size_t>(j) << 2), r2);
+        if (g >= 3) load_run<8>(t + (static_cast<size_t>(j) << 3), r3);
+        if (g >= 4) load_run<16>(t + (static_cast<size_t>(j) << 4), r4);
+        unsigned r = 0;  // position below j at the current level
+        descend_run<2>(u, r, r1);
+        if (g >= 2) descend_run<4>(u, r, r2);
+        if (g >= 3) descend_run<8>(u, r, r3);
+        if (g >= 4) descend_run<16>(u, r, r4);
+        j = (j << g) + r;
+        d += g;
     }
     P.out[k] = static_cast<int32_t>(j - (1u << P.log2cap));
 }
