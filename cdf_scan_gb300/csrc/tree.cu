@@ -354,6 +354,62 @@ __device__ __forceinline__ void recompute_subtrees(float* tree, const unsigned* 
     }
 }
 
+// The same for subtrees of width 32 * M (M = 4 or 8: seven or eight levels):
+// lane l folds bottom nodes [l*M, (l+1)*M) through log2(M) levels in
+// registers, writing each level, then five shuffle levels fold the 32 lane
+// values -- the same sums, always left + right, as the pairwise rebuild.
+template <int M, int JB>
+__device__ __forceinline__ void recompute_wide(float* tree, const unsigned* first, int count, int lane) {
+    static_assert(M == 4 || M == 8, "four or eight bottom nodes per lane");
+    constexpr int LM = M == 4 ? 2 : 3;
+    float v[JB];
+    unsigned node[JB];
+#pragma unroll
+    for (int j = 0; j < JB; ++j) {
+        v[j] = 0.f;
+        node[j] = 0u;
+        if (j < count) {
+            unsigned at = first[j] + M * lane;  // node of x[0]; plain loads: written earlier by this CTA
+            float x[M];
+#pragma unroll
+            for (int q = 0; q < M / 4; ++q) {
+                const float4 t = *reinterpret_cast<const float4*>(tree + at + 4 * q);
+                x[4 * q] = t.x;
+                x[4 * q + 1] = t.y;
+                x[4 * q + 2] = t.z;
+                x[4 * q + 3] = t.w;
+            }
+#pragma unroll
+            for (int l = 0, m = M / 2; l < LM; ++l, m /= 2) {
+                at >>= 1;
+#pragma unroll
+                for (int q = 0; q < m; ++q) {
+                    x[q] = __fadd_rn(x[2 * q], x[2 * q + 1]);
+                    tree[at + q] = x[q];
+                }
+            }
+            v[j] = x[0];
+            node[j] = at;
+        }
+    }
+#pragma unroll
+    for (int l = 1; l <= 5; ++l) {
+        const unsigned delta = 1u << (l - 1);
+        const bool writer = (lane & ((1 << l) - 1)) == 0;
+        float right[JB];
+#pragma unroll
+        for (int j = 0; j < JB; ++j) right[j] = __shfl_down_sync(PER_FULL_MASK, v[j], delta);
+#pragma unroll
+        for (int j = 0; j < JB; ++j) {
+            node[j] >>= 1;
+            if (writer) {
+                v[j] = __fadd_rn(v[j], right[j]);
+                if (j < count) tree[node[j]] = v[j];
+            }
+        }
+    }
+}
+
 // Append `value` to list[*count] for every lane with `take`, one shared
 // atomic per warp.
 __device__ __forceinline__ void warp_append(bool take, unsigned value, unsigned* list, int* count, int lane) {
@@ -442,9 +498,9 @@ __global__ void __launch_bounds__(kSmallThreads) small_update_kernel(const int32
     __syncthreads();
     const int n_leaf = S.n_leaf;
 
-    // ---- (2) recompute this CTA's dirty subtrees, six levels per pass ---------
+    // ---- (2) recompute this CTA's dirty subtrees, up to eight levels per pass --
     for (int bottom = log2cap; bottom > top;) {
-        const int levels = bottom - top < 6 ? bottom - top : 6;
+        const int levels = bottom - top < 8 ? bottom - top : 8;
         const int width = 1 << levels;
         const int shift = (log2cap - bottom) + levels;  // leaf >> shift = subtree number
         if (tid == 0) S.n_job = 0;
@@ -461,13 +517,19 @@ __global__ void __launch_bounds__(kSmallThreads) small_update_kernel(const int32
         }
         __syncthreads();
         const int n_job = S.n_job;
-        for (int j0 = warp * kJobBatch; j0 < n_job; j0 += kWarpsPerCta * kJobBatch) {
+        const int jb = width <= 64 ? kJobBatch : kJobBatch / 2;  // subtrees per warp at once
+        for (int j0 = warp * jb; j0 < n_job; j0 += kWarpsPerCta * jb) {
             unsigned first[kJobBatch];
-            const int count = n_job - j0 < kJobBatch ? n_job - j0 : kJobBatch;
+            const int count = n_job - j0 < jb ? n_job - j0 : jb;
 #pragma unroll
             for (int j = 0; j < kJobBatch; ++j)
                 first[j] = j < count ? (1u << bottom) + S.job[j0 + j] * static_cast<unsigned>(width) : 0u;
-            recompute_subtrees(tree, first, count, width, lane);
+            if (width <= 64)
+                recompute_subtrees(tree, first, count, width, lane);
+            else if (width == 128)
+                recompute_wide<4, kJobBatch / 2>(tree, first, count, lane);
+            else
+                recompute_wide<8, kJobBatch / 2>(tree, first, count, lane);
         }
         for (int i = tid; i < kHashSlots; i += kSmallThreads) S.claim[i] = kEmpty;
         __syncthreads();  // this pass's nodes written (visible to the CTA) and claims cleared
