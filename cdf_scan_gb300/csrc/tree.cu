@@ -362,35 +362,38 @@ template <int M, int JB>
 __device__ __forceinline__ void recompute_wide(float* tree, const unsigned* first, int count, int lane) {
     static_assert(M == 4 || M == 8, "four or eight bottom nodes per lane");
     constexpr int LM = M == 4 ? 2 : 3;
+    // every job's loads first: the stores below may alias them as far as the
+    // compiler knows, so loads issued after a store would wait one by one
+    float x[JB][M];
+#pragma unroll
+    for (int j = 0; j < JB; ++j) {
+#pragma unroll
+        for (int q = 0; q < M / 4; ++q) {
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < count)  // plain loads: written earlier by this CTA
+                t = *reinterpret_cast<const float4*>(tree + first[j] + M * lane + 4 * q);
+            x[j][4 * q] = t.x;
+            x[j][4 * q + 1] = t.y;
+            x[j][4 * q + 2] = t.z;
+            x[j][4 * q + 3] = t.w;
+        }
+    }
     float v[JB];
     unsigned node[JB];
 #pragma unroll
     for (int j = 0; j < JB; ++j) {
-        v[j] = 0.f;
-        node[j] = 0u;
-        if (j < count) {
-            unsigned at = first[j] + M * lane;  // node of x[0]; plain loads: written earlier by this CTA
-            float x[M];
+        unsigned at = first[j] + M * lane;  // node of x[j][0]
 #pragma unroll
-            for (int q = 0; q < M / 4; ++q) {
-                const float4 t = *reinterpret_cast<const float4*>(tree + at + 4 * q);
-                x[4 * q] = t.x;
-                x[4 * q + 1] = t.y;
-                x[4 * q + 2] = t.z;
-                x[4 * q + 3] = t.w;
+        for (int l = 0, m = M / 2; l < LM; ++l, m /= 2) {
+            at >>= 1;
+#pragma unroll
+            for (int q = 0; q < m; ++q) {
+                x[j][q] = __fadd_rn(x[j][2 * q], x[j][2 * q + 1]);
+                if (j < count) tree[at + q] = x[j][q];
             }
-#pragma unroll
-            for (int l = 0, m = M / 2; l < LM; ++l, m /= 2) {
-                at >>= 1;
-#pragma unroll
-                for (int q = 0; q < m; ++q) {
-                    x[q] = __fadd_rn(x[2 * q], x[2 * q + 1]);
-                    tree[at + q] = x[q];
-                }
-            }
-            v[j] = x[0];
-            node[j] = at;
         }
+        v[j] = x[j][0];
+        node[j] = at;
     }
 #pragma unroll
     for (int l = 1; l <= 5; ++l) {
