@@ -3,8 +3,12 @@
 // the particle axis, u_j = (j + U_b)/P with one U_b per row, searchsorted
 // (right=False), clamp to P-1).
 //
-// One CTA of 512 threads per row (every row of a 256-row batch resident at
-// once), three passes over the row -- the last two served by L2:
+// A cluster of K <= 8 CTAs (512 threads each) per row, CTA k owning a
+// contiguous segment of whole 4096-particle chunks, so that a batch of 256
+// rows spreads evenly over the SMs; three passes over the segment -- the
+// last two served by L2 -- with two exchanges between the cluster's CTAs in
+// distributed shared memory (the row maximum; the segments' exact totals,
+// whose exclusive prefix is the segment's carry):
 //   1. the row maximum m;
 //   2. the exact total Q of q_i = fix40(exp(lw_i - m)) (40 fractional bits,
 //      64-bit integer sums: order-independent);
@@ -23,8 +27,12 @@
 // exp is the hardware ex2 of (lw - m) * log2(e): its relative error (~2^-22)
 // stays far inside the CDF tolerance.  For a power-of-two P the threshold
 // division is an exact multiplication by 2^-k.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
@@ -34,6 +42,8 @@ constexpr int kLane = 8;                   // consecutive particles per lane per
 constexpr int kBatch = 8;                  // float4 loads in flight per thread in passes 1 and 2
 constexpr int kChunk = kThreads * kLane;   // 4096
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxSplit = 8;      // CTAs per row at most (one cluster, the portable size limit)
+constexpr int kMinSegChunks = 4;  // chunks per CTA below which splitting needs a spare wave
 
 struct ResampleParams {
     const float* logw;  // may also be out_logw
@@ -49,6 +59,7 @@ struct ResampleParams {
     float* __restrict__ out_state;    // [rows][P][D]
     float* out_logw;                  // [rows][P] (may be logw itself)
     float reset;                      // fl32(-log P)
+    int seg;                          // particles per CTA of a row's cluster (a multiple of kChunk)
 };
 
 // Threshold u_j = fl32(fl32(j + U) / P); for a power of two P the division is
@@ -117,24 +128,31 @@ __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long x
 __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R) {
     __shared__ float s_f[kWarps];
     __shared__ unsigned long long s_u[kWarps];
+    __shared__ float s_cmax;                // this segment's maximum, read by the cluster
+    __shared__ unsigned long long s_cq;     // this segment's exact total, read by the cluster
+    __shared__ float s_rmax;
+    __shared__ unsigned long long s_rq[2];  // the row's total; the segments' before this one
     __shared__ unsigned long long s_off[kWarps + 1];
     __shared__ __align__(16) int s_stage[kChunk];  // one block of outputs: run starts, then filled
     __shared__ int s_wmax[kWarps];
     __shared__ int s_range[2];                      // the chunk's outputs [j_lo, j_hi)
-    const int b = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int K = static_cast<int>(cluster.num_blocks()), k = static_cast<int>(cluster.block_rank());
+    const int b = blockIdx.x / K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int P = R.P;
+    const int s0 = k * R.seg, s1 = min(P, s0 + R.seg);  // this CTA's particles (s0 < s1)
     const float* row = R.logw + static_cast<size_t>(b) * P;
     int32_t* orow = R.out + static_cast<size_t>(b) * P;
 
     // ---- 1: row maximum (kBatch loads in flight per thread) -----------------
     float m = -INFINITY;
-    for (int i0 = threadIdx.x * 4; i0 < P; i0 += kThreads * 4 * kBatch) {
+    for (int i0 = s0 + threadIdx.x * 4; i0 < s1; i0 += kThreads * 4 * kBatch) {
         float4 q[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int i = i0 + u * kThreads * 4;
-            q[u] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) m = fmaxf(m, fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)));
@@ -143,17 +161,29 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(PER_FULL_MASK, m, o));
     if (lane == 0) s_f[warp] = m;
     __syncthreads();
-    float rmax = s_f[0];
-    for (int w = 1; w < kWarps; ++w) rmax = fmaxf(rmax, s_f[w]);
+    if (threadIdx.x == 0) {
+        float mk = s_f[0];
+        for (int w = 1; w < kWarps; ++w) mk = fmaxf(mk, s_f[w]);
+        s_cmax = mk;
+    }
+    cluster.sync();  // every segment's maximum is visible to the cluster
+    if (warp == 0) {
+        float mr = lane < K ? *cluster.map_shared_rank(&s_cmax, lane) : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(PER_FULL_MASK, mr, o));
+        if (lane == 0) s_rmax = mr;
+    }
+    __syncthreads();
+    const float rmax = s_rmax;
 
     // ---- 2: exact total -------------------------------------------------------------
     unsigned long long acc = 0ull;
-    for (int i0 = threadIdx.x * 4; i0 < P; i0 += kThreads * 4 * kBatch) {
+    for (int i0 = s0 + threadIdx.x * 4; i0 < s1; i0 += kThreads * 4 * kBatch) {
         float4 q[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int i = i0 + u * kThreads * 4;
-            q[u] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
@@ -163,8 +193,27 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(PER_FULL_MASK, acc, o);
     if (lane == 0) s_u[warp] = acc;
     __syncthreads();
-    unsigned long long Q = 0ull;
-    for (int w = 0; w < kWarps; ++w) Q += s_u[w];
+    if (threadIdx.x == 0) {
+        unsigned long long qk = 0ull;
+        for (int w = 0; w < kWarps; ++w) qk += s_u[w];
+        s_cq = qk;
+    }
+    cluster.sync();  // every segment's total is visible to the cluster (and every maximum read)
+    if (warp == 0) {
+        const unsigned long long qr = lane < K ? *cluster.map_shared_rank(&s_cq, lane) : 0ull;
+        const unsigned long long incl = warp_incl_u64(qr, lane);
+        const unsigned long long all = __shfl_sync(PER_FULL_MASK, incl, 31);
+        const unsigned long long before = __shfl_sync(PER_FULL_MASK, incl - qr, k);
+        if (lane == 0) {
+            s_rq[0] = all;
+            s_rq[1] = before;
+        }
+    }
+    // the cluster's CTAs may not leave while a peer can still read their
+    // totals: arrive here, wait before the exit
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    __syncthreads();
+    const unsigned long long Q = s_rq[0];
     // c = fl32(E) * fl32(1 / Q): monotone in E, c(Q) ~= 1
     const float inv = __fdiv_rn(1.0f, u64_to_f32(Q));
     const float fP = static_cast<float>(P);
@@ -177,19 +226,18 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
     float4 nxt[kLane / 4];
 #pragma unroll
     for (int h = 0; h < kLane / 4; ++h) {
-        const int i = threadIdx.x * kLane + 4 * h;
-        nxt[h] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        const int i = s0 + threadIdx.x * kLane + 4 * h;
+        nxt[h] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
-    unsigned long long carry = 0ull;
-    for (int c0 = 0; c0 < P; c0 += kChunk) {
+    unsigned long long carry = s_rq[1];  // the exact total of the segments before this one
+    for (int c0 = s0; c0 < s1; c0 += kChunk) {
         const int i0 = c0 + threadIdx.x * kLane;
-        const int valid = min(kChunk, P - c0);  // particles of this chunk (P % 4 == 0)
         float4 cur[kLane / 4];
 #pragma unroll
         for (int h = 0; h < kLane / 4; ++h) {
             cur[h] = nxt[h];
             const int i = i0 + kChunk + 4 * h;
-            nxt[h] = i < P ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            nxt[h] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
         unsigned long long r[kLane];
         unsigned long long run = 0ull;
@@ -327,11 +375,12 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
             __syncthreads();  // s_stage and s_wmax are reused by the next block
         }
     }
-    if (R.out_logw) {  // every read of the row's log-weights is done: the reset may overwrite them
+    if (R.out_logw) {  // every read of the segment's log-weights is done: the reset may overwrite them
         float* lrow = R.out_logw + static_cast<size_t>(b) * P;
         const float4 r4 = make_float4(R.reset, R.reset, R.reset, R.reset);
-        for (int i = threadIdx.x * 4; i < P; i += kThreads * 4) __stcs(reinterpret_cast<float4*>(lrow + i), r4);
+        for (int i = s0 + threadIdx.x * 4; i < s1; i += kThreads * 4) __stcs(reinterpret_cast<float4*>(lrow + i), r4);
     }
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
@@ -352,7 +401,35 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     R.out_state = out_state;
     R.out_logw = out_logw;
     R.reset = reset;
-    resample_kernel<<<static_cast<unsigned>(rows), kThreads, 0, s>>>(R);
+    // K <= kMaxSplit CTAs per row, each a whole number of chunks, none
+    // empty.  Splitting evens out the SMs' loads when rows outnumber them,
+    // but short segments (fewer than kMinSegChunks chunks) only pay off when
+    // the split rows still fit one wave of resident CTAs: the passes over a
+    // short segment are latency-bound, so extra waves of them cost more than
+    // the imbalance they remove.
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PER_ERR_CUDA;
+    const int64_t slots = 2 * static_cast<int64_t>(sms);  // resident CTAs (two per SM)
+    const int chunks = (P + kChunk - 1) / kChunk;
+    int K = min(kMaxSplit, chunks);
+    while (K > 1 && (chunks + K - 1) / K < kMinSegChunks && static_cast<int64_t>(rows) * K > slots) --K;
+    const int seg_chunks = (chunks + K - 1) / K;
+    K = (chunks + seg_chunks - 1) / seg_chunks;
+    R.seg = seg_chunks * kChunk;
+    if (static_cast<int64_t>(rows) * K > 0x7fffffffll) return PER_ERR_ARG;  // grid limit
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows) * static_cast<unsigned>(K));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(K);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, resample_kernel, R);
     per_note_launch();
-    return cuda_status(cudaGetLastError());
+    return cuda_status(e);
 }

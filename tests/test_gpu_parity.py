@@ -292,7 +292,8 @@ def test_is_weights_equal_priorities_and_beta_zero():
 
 # -------------------------------------------------------------- resample ----
 
-@pytest.mark.parametrize("rows,P", [(1, 4), (3, 1024), (4, 4100), (16, 65536)])
+@pytest.mark.parametrize("rows,P", [(1, 4), (3, 1024), (4, 4100), (16, 65536), (5, 5 * 4096 + 100),
+                                    (2, 3 * 4096 + 4)])
 def test_resample_matches_oracle(rows, P):
     lw = workloads.resample_logw(rows=rows, P=P, seed=110 + rows)
     out = torch.empty((rows, P), dtype=torch.int32, device="cuda")
@@ -330,6 +331,35 @@ def test_resample_skewed_rows(P):
         assert np.array_equal(got[b], oracle.resample_row_on_cdf(c[b], U)), f"row {b}"
         assert np.all(np.diff(got[b]) >= 0)
         assert got[b].min() >= 0 and got[b].max() < P
+
+
+@pytest.mark.parametrize("P", [5 * 4096 + 100, 65536])
+def test_resample_mass_at_segment_edges(P):
+    """A row is split into contiguous runs of whole 4096-particle chunks
+    (up to four runs, scanned side by side): mass right before, right
+    after and straddling the run edges, and runs that own no mass at all,
+    must give the same outputs as one scan over the row."""
+    seg = ((P + 4095) // 4096 + 3) // 4 * 4096
+    rows = 5
+    lw = np.full((rows, P), -np.inf, np.float32)
+    lw[0, seg - 1] = 0.0                            # last particle of the first run
+    lw[1, seg] = 0.0                                # first particle of the second run
+    lw[2, 2 * seg - 1], lw[2, 2 * seg] = 0.0, 0.0   # straddling the second edge
+    lw[3, seg - 2:seg + 2] = [0.0, -0.5, -1.0, -2.0]
+    lw[3, P - 1] = -3.0                             # the last particle too
+    lw[4] = workloads.resample_logw(rows=1, P=P, seed=17)[0]
+    lw[4, :seg] = -np.inf                           # the first run owns nothing
+    out = torch.empty((rows, P), dtype=torch.int32, device="cuda")
+    cdf = torch.empty((rows, P), dtype=torch.float32, device="cuda")
+    per.per_resample(dev(lw), 4, 11, out, out_cdf=cdf)
+    got, c = host(out), host(cdf)
+    for b in range(rows):
+        U = oracle.u01_closed_open(4, 11, b)
+        assert np.array_equal(got[b], oracle.resample_row_on_cdf(c[b], U)), f"row {b}"
+        want, C, u = oracle.resample_row(lw[b], U)
+        assert np.max(np.abs(c[b] - C)) <= 2e-6
+        band_check(C, got[b], want, u, 2e-6)
+        assert np.all(np.diff(got[b]) >= 0)
 
 
 def test_resample_equal_weights_identity_and_u_override():
