@@ -294,11 +294,13 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
         if (threadIdx.x == kThreads - 1) s_range[1] = c0 + kChunk >= P ? P : nend[kLane - 1];
         __syncthreads();
         const int j_lo = s_range[0], j_hi = s_range[1];
-        // outputs in blocks of kChunk aligned to absolute output positions:
-        // each non-empty run writes its particle at its first output, and a
+        // outputs in blocks of kChunk from the chunk's first output (rounded
+        // down to 8, so that a thread's 8 outputs start 32-byte aligned): a
+        // chunk of about kChunk outputs mostly needs one block.  Each
+        // non-empty run writes its particle at its first output, and a
         // prefix max fills every output with the particle whose run covers it
         int started = -1;  // the last particle started in earlier blocks
-        for (int b0 = j_lo & ~(kChunk - 1); b0 < j_hi; b0 += kChunk) {
+        for (int b0 = j_lo & ~(kLane - 1); b0 < j_hi; b0 += kChunk) {
             const int t0 = threadIdx.x * kLane;  // this thread's outputs in the block: b0 + t0 .. + 7
             *reinterpret_cast<int4*>(s_stage + t0) = make_int4(-1, -1, -1, -1);
             *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(-1, -1, -1, -1);
@@ -325,12 +327,17 @@ __global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R)
             int before = __shfl_up_sync(PER_FULL_MASK, x, 1);
             if (lane == 0) before = -1;
             __syncthreads();
-            int wb = started, all = started;
+            // the maxima of the warps before this one and of all warps: one
+            // max-scan over the kWarps warp maxima (lane w holds warp w's)
+            int wm = lane < kWarps ? s_wmax[lane] : -1;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                if (w < warp) wb = max(wb, s_wmax[w]);
-                all = max(all, s_wmax[w]);
+            for (int d = 1; d < kWarps; d <<= 1) {
+                const int y = __shfl_up_sync(PER_FULL_MASK, wm, d);
+                if (lane >= d) wm = max(wm, y);
             }
+            const int wb_in = __shfl_sync(PER_FULL_MASK, wm, warp > 0 ? warp - 1 : 0);
+            const int wb = max(started, warp > 0 ? wb_in : -1);
+            const int all = max(started, __shfl_sync(PER_FULL_MASK, wm, kWarps - 1));
             before = max(before, wb);
 #pragma unroll
             for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
