@@ -20,10 +20,11 @@
 //      from c*P - U corrected by a couple of exact threshold evaluations) and
 //      owns outputs [n(c_{i-1}), n(c_i)) -- exactly the outputs whose
 //      lower_bound lands on i, the last particle's run extending to P (the
-//      clamp).  The outputs are written in blocks of 4096 aligned to output
-//      positions: each non-empty run puts its particle at its first output in
-//      shared memory, and a block-wide prefix max fills every output with the
-//      particle whose run covers it (16-byte stores; no per-output search).
+//      clamp).  The outputs are written in blocks of 4096 starting at the
+//      chunk's first output (rounded down to 8): each non-empty run puts its
+//      particle at its first output in shared memory, and a block-wide prefix
+//      max fills every output with the particle whose run covers it (16-byte
+//      stores; no per-output search).
 // exp is the hardware ex2 of (lw - m) * log2(e): its relative error (~2^-22)
 // stays far inside the CDF tolerance.  For a power-of-two P the threshold
 // division is an exact multiplication by 2^-k.
