@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kScanThreads) radix_digit_scan_kernel(unsigned
 
 // The tile pass of large sizes: rank, place against the offsets of the
 // histogram and digit-scan launches, write.
-__global__ void __launch_bounds__(kSortThreads, 2) radix_scatter_kernel(SortParams S) {
+__global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(SortParams S) {
     __shared__ SortSmem<kBigItems> sm;
     const PassIO io = pass_io(S, S.pass);
     const int d = threadIdx.x;
