@@ -317,8 +317,9 @@ per_status per_check(per_ctx* ctx, void* stream);
  * int32[rows][P].  If d_out_cdf (16-byte aligned) is not NULL it receives the
  * float32[rows][P] CDF that was searched.  Needs no context and no scratch.
  * A row whose log-weights are all -inf or contain NaN gives unspecified
- * indices in [0, P).  PER_ERR_ARG: null or misaligned pointers, rows < 1,
- * P < 4, P % 4 != 0, P > 2^23.
+ * indices in [0, P).  A row is scanned by up to 8 CTAs (one cluster).
+ * PER_ERR_ARG: null or misaligned pointers, rows < 1, P < 4, P % 4 != 0,
+ * P > 2^23, or so many rows that the grid would exceed 2^31 - 1 CTAs.
  */
 per_status per_resample(const float* d_logw, int32_t rows, int32_t P, uint64_t seed,
                         uint64_t offset, const float* d_u_rows, int32_t* d_out_idx,
