@@ -252,8 +252,12 @@ __device__ __forceinline__ void place_and_write(const SortParams& S, const PassI
 __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) {
     __shared__ unsigned h[kSortWarps][kRadixDigits];
     const int warp = threadIdx.x >> 5;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the digit scan may be scheduled
     for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&h[0][0])[i] = 0u;
     __syncthreads();
+    // launched as a programmatic dependent of the previous pass's tile pass
+    // (passes 1-3): its keys are complete only once that launch is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const PassIO io = pass_io(S, S.pass);
     const int tile_base = blockIdx.x * kRankTile;
     bool bad = false;
@@ -308,6 +312,10 @@ __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) 
 __global__ void __launch_bounds__(kScanThreads) radix_digit_scan_kernel(unsigned* counts, unsigned* totals,
                                                                         int tiles) {
     __shared__ unsigned s_w[kScanThreads / 32];
+    // the tile pass may start now: it loads and ranks its keys before it
+    // waits for these offsets
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the histogram launch's counts
     unsigned* row = counts + static_cast<int64_t>(blockIdx.x) * tiles;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t0 = threadIdx.x * 4;
@@ -346,6 +354,7 @@ __global__ void __launch_bounds__(kScanThreads) radix_digit_scan_kernel(unsigned
 // histogram and digit-scan launches, write.
 __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(SortParams S) {
     __shared__ SortSmem<kBigItems> sm;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next histogram may be scheduled
     const PassIO io = pass_io(S, S.pass);
     const int d = threadIdx.x;
     for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&sm.cnt[0][0])[i] = 0u;
@@ -358,6 +367,9 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(SortPara
     const unsigned cnt_d = warp_offsets(sm);
     unsigned tile_total = 0u, all = 0u;
     const unsigned start_d = block_excl_scan(cnt_d, sm.w, &tile_total);
+    // the digit-scan launch's offsets: launched as its programmatic
+    // dependent, this CTA waits here for that launch to finish
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const unsigned digit_start = block_excl_scan(S.totals[d], sm.w, &all);
     const unsigned gbase = digit_start + S.counts[d * S.tiles + blockIdx.x];
 #pragma unroll
@@ -469,15 +481,38 @@ per_status launch_rank_build(per_ctx* ctx, cudaStream_t s) {
         if (e != cudaSuccess) return PER_ERR_CUDA;
     } else {
         S.tiles = (n + kRankTile - 1) / kRankTile;
-        for (int pass = 0; pass < 4; ++pass) {
+        // Each launch is a programmatic dependent of the one before it (but
+        // the first, which follows whatever the stream ran before): it is
+        // scheduled while that launch finishes and waits for it
+        // (griddepcontrol.wait) before its first dependent read.
+        auto launch = [&](auto kernel, unsigned grid, unsigned block, bool dependent, auto... args) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(grid);
+            cfg.blockDim = dim3(block);
+            cfg.stream = s;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = dependent ? 1 : 0;
+            return cudaLaunchKernelEx(&cfg, kernel, args...);
+        };
+        int launched = 0;
+        cudaError_t e = cudaSuccess;
+        for (int pass = 0; pass < 4 && e == cudaSuccess; ++pass) {
             S.pass = pass;
-            radix_hist_kernel<<<static_cast<unsigned>(S.tiles), kSortThreads, 0, s>>>(S);
-            radix_digit_scan_kernel<<<kRadixDigits, kScanThreads, 0, s>>>(ctx->rank_counts, ctx->rank_totals,
-                                                                          S.tiles);
-            radix_scatter_kernel<<<static_cast<unsigned>(S.tiles), kSortThreads, 0, s>>>(S);
+            const unsigned tiles = static_cast<unsigned>(S.tiles);
+            if ((e = launch(radix_hist_kernel, tiles, kSortThreads, pass > 0, S)) != cudaSuccess) break;
+            ++launched;
+            if ((e = launch(radix_digit_scan_kernel, static_cast<unsigned>(kRadixDigits), kScanThreads, true,
+                            ctx->rank_counts, ctx->rank_totals, S.tiles)) != cudaSuccess)
+                break;
+            ++launched;
+            if ((e = launch(radix_scatter_kernel, tiles, kSortThreads, true, S)) != cudaSuccess) break;
+            ++launched;
         }
-        per_note_launch(12);
-        if (cudaGetLastError() != cudaSuccess) return PER_ERR_CUDA;
+        per_note_launch(launched);
+        if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return PER_ERR_CUDA;
     }
     ctx->rank_sorted_n = n;
     if (ctx->rank_q_n != n) {  // q and its CDF depend on n (and the context's alpha) only
