@@ -91,6 +91,10 @@ __global__ void __launch_bounds__(THREADS) sample_tree_kernel(TreeSampleParams P
     __shared__ __align__(8) uint64_t s_bar;
     // at least 16 bytes (the bulk-copy granule; the tree allocation is padded)
     const unsigned top_bytes = max(16u, (2u << P.staged_levels) * 4u);
+    // launched as a programmatic dependent of the previous launch (typically
+    // the previous update): nothing is read from global memory before it ends
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
         mbar_init(&s_bar, 1);
         mbar_arrive_expect_tx(&s_bar, top_bytes);
@@ -463,6 +467,10 @@ __global__ void __launch_bounds__(kSmallThreads) small_update_kernel(const int32
         S.claim[i] = kEmpty;
     }
     if (tid == 0) S.n_leaf = 0;
+    // launched as a programmatic dependent of the previous launch (typically
+    // the sampler): nothing is read from global memory before it ends
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     __syncthreads();
 
     // ---- (1) the last occurrence of each index wins ---------------------------
@@ -569,10 +577,20 @@ per_status launch_sample_tree(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
     const size_t smem = std::max<size_t>(16, (static_cast<size_t>(2) << P.staged_levels) * sizeof(float));
     const int threads = B >= 64 * ctx->num_sms ? 256 : 128;
     const unsigned grid = static_cast<unsigned>((B + threads - 1) / threads);
-    if (threads == 256) sample_tree_kernel<256><<<grid, 256, smem, s>>>(P);
-    else sample_tree_kernel<128><<<grid, 128, smem, s>>>(P);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's first lines
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = threads == 256 ? cudaLaunchKernelEx(&cfg, sample_tree_kernel<256>, P)
+                                         : cudaLaunchKernelEx(&cfg, sample_tree_kernel<128>, P);
     per_note_launch();
-    return cuda_status(cudaGetLastError());
+    return cuda_status(e);
 }
 
 per_status launch_tree_from_prio(per_ctx* ctx, cudaStream_t s) {
@@ -625,13 +643,15 @@ per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n
         cfg.blockDim = dim3(kSmallThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(C);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see the kernel's first lines
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         const cudaError_t e = cudaLaunchKernelEx(&cfg, small_update_kernel, idx, p, n, ctx->capacity, ctx->prio,
                                                  ctx->tree, ctx->log2_cap, ctx->alpha, ctx->alpha == 1.0f,
                                                  ctx->status);
