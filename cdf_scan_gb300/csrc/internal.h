@@ -47,6 +47,8 @@ struct per_ctx {
     unsigned* ctrs;                   // [NUM_CTRS]
     int* status;                      // device status word
     float* coarse;                    // [coarse_n] every 64th CDF value (PER_SCAN)
+    int* sample_bounds;               // [2 * sample_bounds_n] window ends of the sampler's CTAs (PER_SCAN, PER_RANK)
+    int64_t sample_bounds_n;
     int64_t coarse_n;
     unsigned long long* tickets;      // [NUM_TICKETS] grid-barrier tickets
     float* slots;                     // [slot_n] per-CTA partial results

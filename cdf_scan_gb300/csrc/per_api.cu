@@ -38,6 +38,7 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->ctrs);
     cudaFree(c->status);
     cudaFree(c->coarse);
+    cudaFree(c->sample_bounds);
     cudaFree(c->tickets);
     cudaFree(c->slots);
     cudaFree(c->scan_xsum);
@@ -102,6 +103,8 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     c->flags = flags;
     c->scan_desc_tiles = std::min<int64_t>((c->alloc_n + 1023) / 1024, kMaxWaveTiles);
     c->coarse_n = c->alloc_n / kCoarseStride + 1;
+    // the sampler's CTAs: at most max(B / 1024, n / 4096) + 1 of them
+    c->sample_bounds_n = std::max<int64_t>(int64_t(1) << 14, c->alloc_n / 4096) + 2;
     c->slot_n = 16 * c->num_sms;
     bool ok = alloc_zero(&c->prio, c->alloc_n, s) == cudaSuccess &&
               alloc_zero(&c->winner, static_cast<size_t>(capacity), s) == cudaSuccess &&
@@ -112,6 +115,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     if (ok && (flags & PER_SCAN))
         ok = alloc_zero(&c->cdf, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
+             alloc_zero(&c->sample_bounds, 2 * static_cast<size_t>(c->sample_bounds_n), s) == cudaSuccess &&
              alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
              alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess &&
              alloc_zero(&c->step_min, 3, s) == cudaSuccess;
@@ -126,6 +130,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
              alloc_zero(&c->rank_q, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->rank_cdf, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->rank_coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
+             (c->sample_bounds || alloc_zero(&c->sample_bounds, 2 * static_cast<size_t>(c->sample_bounds_n), s) == cudaSuccess) &&
              alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
              alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess;
     }

@@ -43,14 +43,36 @@ __device__ int warp_lower_bound(const float* __restrict__ c, int n, float u, int
     return ans < n ? ans : n - 1;
 }
 
+// The window ends of every CTA of sample_scan_kernel, one warp per end:
+// bounds[2j] = lower_bound of CTA j's first threshold, bounds[2j + 1] of its
+// last (the thresholds and the searches the sampler would make itself, so
+// they are the same values).  The ends of all CTAs are searched at once,
+// instead of one CTA after another in front of each window copy.
+__global__ void __launch_bounds__(256) sample_bounds_kernel(SampleParams P, int per_cta, int ctas) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the sampler may be scheduled
+    const int lane = threadIdx.x & 31;
+    const int w = static_cast<int>((blockIdx.x * 256u + threadIdx.x) >> 5);
+    if (w >= 2 * ctas) return;
+    const float T = __ldg(P.cdf + P.n - 1);
+    if (!(T > 0.f)) return;  // the sampler reports the empty buffer
+    const int j = w >> 1;
+    const int k0 = j * per_cta;
+    const int k = (w & 1) ? min(P.B, k0 + per_cta) - 1 : k0;
+    const float u = stratified_threshold(k, draw_u(P, k), static_cast<float>(P.B), T);
+    const int b = warp_lower_bound(P.cdf, P.n, u, lane);
+    if (lane == 0) P.bounds[w] = b;
+}
+
+// One CTA per THREADS x SPT consecutive strata: the thresholds, then (after
+// the bounds launch, of which this launch is a programmatic dependent) the
+// window [lower_bound(first), lower_bound(last)] staged by one bulk copy and
+// searched in shared memory.
 template <int THREADS, int SPT>
 __global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
     extern __shared__ __align__(128) float s_win[];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ int s_lo, s_hi;
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
     const int k0 = blockIdx.x * THREADS * SPT;
     const int kend = min(P.B, k0 + THREADS * SPT);  // exclusive
     const float T = __ldg(P.cdf + P.n - 1);
@@ -64,23 +86,17 @@ __global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
     }
     const float fB = static_cast<float>(P.B);
 
-    // window ends: first and last threshold of this CTA
-    if (warp == 0) {
-        const float uf = stratified_threshold(k0, draw_u(P, k0), fB, T);
-        const int lo = warp_lower_bound(P.cdf, P.n, uf, lane);
-        if (lane == 0) s_lo = lo;
-    }
-    if (warp == (THREADS > 32 ? 1 : 0)) {
-        const float ul = stratified_threshold(kend - 1, draw_u(P, kend - 1), fB, T);
-        const int hi = warp_lower_bound(P.cdf, P.n, ul, lane);
-        if (lane == 0) s_hi = hi;
-    }
-
     float u[SPT];
 #pragma unroll
     for (int s = 0; s < SPT; ++s) {
         const int k = k0 + threadIdx.x + s * THREADS;
         u[s] = k < kend ? stratified_threshold(k, draw_u(P, k), fB, T) : 0.f;
+    }
+    // the window ends: from the bounds launch
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+        s_lo = __ldcg(P.bounds + 2 * blockIdx.x);
+        s_hi = __ldcg(P.bounds + 2 * blockIdx.x + 1);
     }
     __syncthreads();
     const int ilo = s_lo, ihi = s_hi;
@@ -186,9 +202,24 @@ per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
             return PER_ERR_CUDA;
         configured = true;
     }
-    sample_scan_kernel<THREADS, SPT><<<grid, THREADS, kWindowCap * sizeof(float), s>>>(P);
+    if (!P.bounds || static_cast<int>(grid) > P.bounds_n) return PER_ERR_STATE;
+    sample_bounds_kernel<<<(2 * grid + 7) / 8, 256, 0, s>>>(P, per_cta, static_cast<int>(grid));
     per_note_launch();
-    return cuda_status(cudaGetLastError());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = kWindowCap * sizeof(float);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, sample_scan_kernel<THREADS, SPT>, P);
+    per_note_launch();
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -229,6 +260,8 @@ SampleParams sample_params(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, 
     P.out = out;
     P.status = ctx->status;
     P.coarse = rank ? ctx->rank_coarse : ctx->coarse;
+    P.bounds = ctx->sample_bounds;
+    P.bounds_n = static_cast<int>(ctx->sample_bounds_n);
     return P;
 }
 
