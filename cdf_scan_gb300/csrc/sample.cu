@@ -48,7 +48,8 @@ __device__ int warp_lower_bound(const float* __restrict__ c, int n, float u, int
 // last (the thresholds and the searches the sampler would make itself, so
 // they are the same values).  The ends of all CTAs are searched at once,
 // instead of one CTA after another in front of each window copy.
-__global__ void __launch_bounds__(256) sample_bounds_kernel(SampleParams P, int per_cta, int ctas) {
+__global__ void __launch_bounds__(256) sample_bounds_kernel(SampleParams P, int* __restrict__ bounds, int per_cta,
+                                                             int ctas) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the sampler may be scheduled
     const int lane = threadIdx.x & 31;
     const int w = static_cast<int>((blockIdx.x * 256u + threadIdx.x) >> 5);
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(256) sample_bounds_kernel(SampleParams P, int 
     const int k = (w & 1) ? min(P.B, k0 + per_cta) - 1 : k0;
     const float u = stratified_threshold(k, draw_u(P, k), static_cast<float>(P.B), T);
     const int b = warp_lower_bound(P.cdf, P.n, u, lane);
-    if (lane == 0) P.bounds[w] = b;
+    if (lane == 0) bounds[w] = b;
 }
 
 // One CTA per THREADS x SPT consecutive strata: the thresholds, then (after
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(256) sample_bounds_kernel(SampleParams P, int 
 // window [lower_bound(first), lower_bound(last)] staged by one bulk copy and
 // searched in shared memory.
 template <int THREADS, int SPT>
-__global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
+__global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P, const int* __restrict__ bounds) {
     extern __shared__ __align__(128) float s_win[];
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ int s_lo, s_hi;
@@ -95,8 +96,8 @@ __global__ void __launch_bounds__(THREADS) sample_scan_kernel(SampleParams P) {
     // the window ends: from the bounds launch
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
-        s_lo = __ldcg(P.bounds + 2 * blockIdx.x);
-        s_hi = __ldcg(P.bounds + 2 * blockIdx.x + 1);
+        s_lo = __ldcg(bounds + 2 * blockIdx.x);
+        s_hi = __ldcg(bounds + 2 * blockIdx.x + 1);
     }
     __syncthreads();
     const int ilo = s_lo, ihi = s_hi;
@@ -190,7 +191,7 @@ per_status launch_coarse_cfg(const SampleParams& P, cudaStream_t s) {
 }
 
 template <int THREADS, int SPT>
-per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
+per_status launch_cfg(const SampleParams& P, int* bounds, int64_t bounds_n, cudaStream_t s) {
     const int per_cta = THREADS * SPT;
     const unsigned grid = static_cast<unsigned>((P.B + per_cta - 1) / per_cta);
     // the staging buffer plus the static barrier words exceed the default
@@ -202,8 +203,8 @@ per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
             return PER_ERR_CUDA;
         configured = true;
     }
-    if (!P.bounds || static_cast<int>(grid) > P.bounds_n) return PER_ERR_STATE;
-    sample_bounds_kernel<<<(2 * grid + 7) / 8, 256, 0, s>>>(P, per_cta, static_cast<int>(grid));
+    if (!bounds || static_cast<int64_t>(grid) > bounds_n) return PER_ERR_STATE;
+    sample_bounds_kernel<<<(2 * grid + 7) / 8, 256, 0, s>>>(P, bounds, per_cta, static_cast<int>(grid));
     per_note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
@@ -217,7 +218,7 @@ per_status launch_cfg(const SampleParams& P, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, sample_scan_kernel<THREADS, SPT>, P);
+    e = cudaLaunchKernelEx(&cfg, sample_scan_kernel<THREADS, SPT>, P, static_cast<const int*>(bounds));
     per_note_launch();
     return cuda_status(e);
 }
@@ -260,8 +261,6 @@ SampleParams sample_params(per_ctx* ctx, int B, uint64_t seed, uint64_t offset, 
     P.out = out;
     P.status = ctx->status;
     P.coarse = rank ? ctx->rank_coarse : ctx->coarse;
-    P.bounds = ctx->sample_bounds;
-    P.bounds_n = static_cast<int>(ctx->sample_bounds_n);
     return P;
 }
 
@@ -284,12 +283,12 @@ per_status launch_sample_scan(per_ctx* ctx, int B, uint64_t seed, uint64_t offse
     while (per_cta > 32 && ratio * per_cta > (2.0 * kWindowCap) / 3.0) per_cta >>= 1;
     while (per_cta > 32 && (B + per_cta - 1) / per_cta < 2 * ctx->num_sms) per_cta >>= 1;
     switch (per_cta) {
-        case 1024: return launch_cfg<256, 4>(P, s);
-        case 512: return launch_cfg<256, 2>(P, s);
-        case 256: return launch_cfg<256, 1>(P, s);
-        case 128: return launch_cfg<128, 1>(P, s);
-        case 64: return launch_cfg<64, 1>(P, s);
-        default: return launch_cfg<32, 1>(P, s);
+        case 1024: return launch_cfg<256, 4>(P, ctx->sample_bounds, ctx->sample_bounds_n, s);
+        case 512: return launch_cfg<256, 2>(P, ctx->sample_bounds, ctx->sample_bounds_n, s);
+        case 256: return launch_cfg<256, 1>(P, ctx->sample_bounds, ctx->sample_bounds_n, s);
+        case 128: return launch_cfg<128, 1>(P, ctx->sample_bounds, ctx->sample_bounds_n, s);
+        case 64: return launch_cfg<64, 1>(P, ctx->sample_bounds, ctx->sample_bounds_n, s);
+        default: return launch_cfg<32, 1>(P, ctx->sample_bounds, ctx->sample_bounds_n, s);
     }
 }
 

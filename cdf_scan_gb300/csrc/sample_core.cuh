@@ -34,9 +34,6 @@ struct SampleParams {
     unsigned* min_word;          // or one word every CTA atomicMin's (float bits; +inf on entry)
     // rank-based PER: the CDF is over ranks and out[k] = order[rank] (nullptr: out[k] = the index drawn)
     const int32_t* __restrict__ order;
-    // window ends [2 * cta] of the staged sampler, from its bounds launch
-    int* bounds;
-    int bounds_n;  // CTAs the buffer holds
 };
 
 __device__ __forceinline__ int32_t sample_item(const SampleParams& P, int r) { return P.order ? __ldg(P.order + r) : r; }
