@@ -126,7 +126,11 @@ __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long x
     return x;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) resample_kernel(ResampleParams R) {
+// STEP: the whole resample step (states copied, log-weights reset).  Its state
+// copy is memory-bound and gains from a third CTA per SM (40 registers, a few
+// spilled); the indices alone run faster at two (64 registers, no spills).
+template <bool STEP>
+__global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(ResampleParams R) {
     __shared__ float s_f[kWarps];
     __shared__ unsigned long long s_u[kWarps];
     __shared__ float s_cmax;                // this segment's maximum, read by the cluster
@@ -418,7 +422,8 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PER_ERR_CUDA;
-    const int64_t slots = 2 * static_cast<int64_t>(sms);  // resident CTAs (two per SM)
+    const bool step = state != nullptr;
+    const int64_t slots = (step ? 3 : 2) * static_cast<int64_t>(sms);  // resident CTAs per SM, as launch_bounds
     const int chunks = (P + kChunk - 1) / kChunk;
     int K = min(kMaxSplit, chunks);
     while (K > 1 && (chunks + K - 1) / K < kMinSegChunks && static_cast<int64_t>(rows) * K > slots) --K;
@@ -437,7 +442,8 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, resample_kernel, R);
+    const cudaError_t e = step ? cudaLaunchKernelEx(&cfg, resample_kernel<true>, R)
+                               : cudaLaunchKernelEx(&cfg, resample_kernel<false>, R);
     per_note_launch();
     return cuda_status(e);
 }
