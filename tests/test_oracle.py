@@ -195,25 +195,79 @@ def test_lower_bound_is_searchsorted_left_with_clamp():
     assert oracle.lower_bound_f32(np.array([1, 2, 3], np.float32), 3.5) == 2
 
 
-def test_brute_force_frequencies_small_n():
-    # enumerate U on a 2^-16 grid for B=1: the count landing on index i must
-    # equal 2^16 * pa_i / total up to the boundary rounding (a couple of grid
-    # points per boundary) -- this pins the CDF, the threshold and the search
-    # together.  A zero-priority item is never drawn.
-    p = np.array([0.5, 2.0, 0.0, 1.0, 3.0, 0.0, 0.25, 1.0, 4.0, 0.125, 1.5, 0.0, 2.5, 1.0, 0.75, 0.5],
-                 np.float32)
-    alpha = 0.7
+def _grid_count_at_or_below(c, T):
+    """Number of grid points x in [1, 2^24] whose B = 1 threshold
+    fl32(x 2^-24 * T) is <= c.  The product rounds monotonically in x, so the
+    set is a prefix [1, X]; X is found by bisection with each candidate's
+    threshold rounded by numpy's float32 multiply (an independent IEEE
+    implementation) and compared with c exactly (fp64 holds every fp32)."""
+    T32 = np.float32(T)
+    lo, hi = 0, 1 << 24  # invariant: thr(lo) <= c (thr(0) = 0), answer in [lo, hi]
+    if float(np.float32(np.float32(hi * 2.0 ** -24) * T32)) <= c:
+        return hi
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if float(np.float32(np.float32(mid * 2.0 ** -24) * T32)) <= c:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def _exact_grid_counts(C):
+    """Per index i, the exact number of the 2^24 grid points whose threshold
+    lies in (C[i-1], C[i]] -- the interval lower_bound maps to i -- with the
+    last index also taking every threshold above C[n-1] (the clamp)."""
+    T = np.float32(C[-1])
+    below = [_grid_count_at_or_below(float(c), T) for c in C[:-1]]
+    edges = np.array([0] + below + [1 << 24], np.int64)
+    return np.diff(edges)
+
+
+@pytest.mark.parametrize("case", ["dyadic_alpha1", "mixed_alpha07"])
+def test_brute_force_frequencies_small_n(case):
+    """All 2^24 values of U = m 2^-24 (m = 1 .. 2^24, the whole range of the
+    24-bit uniform in (0, 1]) for B = 1, enumerated in one oracle call: with
+    B = 2^24 and every U_k = 1 the stratified threshold is
+    fl32(fl32(k + 1) / 2^24 * T) = fl32((k + 1) 2^-24 T) -- exactly the B = 1
+    threshold of grid point k + 1, since k + 1 <= 2^24 and the division by a
+    power of two are exact.  Each index must be drawn exactly as often as the
+    number of grid points whose threshold falls in its CDF interval, counted
+    independently by a boundary search per index, and that count must be
+    2^24 * P_i within the boundary roundings.  A zero-priority item is never
+    drawn."""
+    if case == "dyadic_alpha1":
+        # dyadic priorities: every prefix sum is exact in fp64 and fp32, so
+        # the CDF is the rational cumsum and P_i is known exactly
+        p = np.array([0.5, 2.0, 0.0, 1.0, 3.0, 0.0, 0.25, 1.0, 4.0, 0.125, 1.5, 0.0, 2.5, 1.0, 0.75, 0.5],
+                     np.float32)
+        alpha = 1.0
+    else:
+        p = np.array([0.3, 2.0, 0.0, 1.7, 3.1, 0.0, 0.25, 1.0, 4.0, 0.01, 1.5, 0.0, 2.5, 1e-3, 0.75],
+                     np.float32)
+        alpha = 0.7
     C = oracle.cdf64(p, alpha)
-    M = 1 << 16
-    U = (np.arange(1, M + 1, dtype=np.float64) / M).astype(np.float32)
-    counts = np.zeros(p.size, np.int64)
-    for k in range(M):
-        idx, _ = oracle.sample_cdf_f64(C, 1, 0, 0, u01=U[k:k + 1])
-        counts[idx[0]] += 1
-    pa = p.astype(np.float64) ** alpha
-    want = M * pa / pa.sum()
+    if case == "dyadic_alpha1":
+        assert np.array_equal(C, np.cumsum([Fraction(float(x)) for x in p]).astype(np.float64))
+    M = 1 << 24
+    idx, u = oracle.sample_cdf_f64(C, M, 0, 0, u01=np.ones(M, np.float32))
+    # the thresholds are the B = 1 grid thresholds, in order
+    for m in (1, 2, 3, 12345, M // 2 + 7, M - 1, M):
+        assert u[m - 1] == np.float32(np.float32(m * 2.0 ** -24) * np.float32(C[-1]))
+    counts = np.bincount(idx, minlength=p.size)
+    want = _exact_grid_counts(C)
+    assert np.array_equal(counts, want)
     assert np.all(counts[p == 0] == 0)
-    assert np.all(np.abs(counts - want) <= 3)
+    pa = p.astype(np.float64) ** alpha
+    expect = M * pa / pa.sum()
+    # one grid step of U moves the threshold by T 2^-24; each boundary's fp32
+    # rounding of the threshold shifts at most a grid point or two
+    assert np.all(np.abs(counts - expect) <= 2.0)
+    if case == "dyadic_alpha1":
+        # total = 18.125 = 145/8: index i gets 2^24 p_i / 18.125 grid points
+        # up to the threshold rounding at its two boundaries
+        assert float(C[-1]) == 18.125
+        assert np.all(np.abs(counts - M * p.astype(np.float64) / 18.125) <= 2.0)
 
 
 def test_sampling_on_equal_priorities_hits_known_indices():
@@ -237,6 +291,50 @@ def test_apply_updates_last_duplicate_wins():
 
 
 # ------------------------------------------------------------ sum tree ------
+
+def test_tree_leaves_closed_forms_and_zero_padding():
+    """tree_leaves is leaf i = p_i^alpha for i < n and exactly 0 above n
+    (foxhunt "Tree Layout": the capacity is rounded up to a power of two and
+    the extra leaves hold nothing).  Pinned by values the mathematics fixes
+    without calling pow: alpha = 1 keeps p; alpha = 1/2 on perfect squares and
+    alpha = 1/4 on fourth powers give exact integer roots; alpha = 3/2 on
+    powers of four and alpha = 3/4 on powers of 16 give exact powers of two;
+    alpha = 0 gives 1 for every item below n, zeros included (C's
+    pow(0, 0) = 1), but still 0 in the padding."""
+    cap = 16
+    sq = np.array([0, 1, 4, 9, 16, 25, 36, 49, 64, 81, 100, 121], np.float32)
+    n = sq.size
+    for alpha, want_fn in [(1.0, lambda x: x), (0.5, lambda x: np.round(np.sqrt(x)))]:
+        lv = oracle.tree_leaves(sq, alpha, cap)
+        assert lv.dtype == np.float32 and lv.size == cap
+        assert np.array_equal(lv[:n], want_fn(sq.astype(np.float64)).astype(np.float32))
+        assert np.all(lv[n:] == 0.0) and not np.any(np.signbit(lv[n:]))
+    fourth = np.array([1, 16, 81, 256, 625], np.float32)
+    assert np.array_equal(oracle.tree_leaves(fourth, 0.25, 8), np.array([1, 2, 3, 4, 5, 0, 0, 0], np.float32))
+    pw4 = np.array([0.25, 1.0, 4.0, 16.0, 2.0 ** -20], np.float32)  # 4^k -> 8^k
+    assert np.array_equal(oracle.tree_leaves(pw4, 1.5, 8),
+                          np.array([0.125, 1, 8, 64, 2.0 ** -30, 0, 0, 0], np.float32))
+    pw16 = np.array([16.0, 256.0, 2.0 ** -8], np.float32)  # 16^k -> 8^k
+    assert np.array_equal(oracle.tree_leaves(pw16, 0.75, 4), np.array([8, 64, 2.0 ** -6, 0], np.float32))
+    # alpha = 0: ones below n (the zero item too), zeros above
+    z = np.array([0.0, 3.0, 0.0, 7.5, 1e-30], np.float32)
+    lv = oracle.tree_leaves(z, 0.0, 8)
+    assert np.array_equal(lv, np.array([1, 1, 1, 1, 1, 0, 0, 0], np.float32))
+    # n = cap (no padding) and n = 0 (all padding)
+    assert np.array_equal(oracle.tree_leaves(np.full(8, 9.0, np.float32), 0.5, 8), np.full(8, 3.0, np.float32))
+    assert np.array_equal(oracle.tree_leaves(np.zeros(0, np.float32), 0.0, 8), np.zeros(8, np.float32))
+    # a generic alpha: the leaf is the power rounded to fp32, so it lies
+    # within about half an fp32 ulp of the exact 2^(alpha e) (60-digit mpmath)
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 60
+    e = np.arange(-30, 31, 3)
+    x = (2.0 ** e).astype(np.float32)
+    lv = oracle.tree_leaves(x, 0.6, 32)
+    for k, v in zip(e, lv[:e.size]):
+        exact = mpmath.power(2, mpmath.mpf(0.6) * int(k))  # the fp64 alpha the oracle receives
+        assert abs(mpmath.mpf(float(v)) - exact) <= 0.5001 * float(np.spacing(v))
+    assert np.all(lv[e.size:] == 0.0)
+
 
 def _golden_layout():
     children, leaves, cap, root = {}, {}, None, None
