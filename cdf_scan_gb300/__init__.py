@@ -57,6 +57,7 @@ SIGNATURES = {
     "per_rank_order_ptr": (_vp, [_vp]),
     "per_rank_cdf_ptr": (_vp, [_vp]),
     "per_check": (ctypes.c_int, [_vp, _vp]),
+    "per_debug_drop_tile": (ctypes.c_int, [_vp, _i64]),
     "per_resample": (ctypes.c_int, [_vp, _i32, _i32, _u64, _u64, _vp, _vp, _vp, _vp]),
     "per_resample_step": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _u64, _u64, _vp, _vp, _vp, _vp, _vp]),
     "per_launch_count": (_u64, []),
@@ -260,6 +261,12 @@ def per_total_host(ctx: int, mode: int, stream=None) -> float:
 def per_check(ctx: int, stream=None) -> int:
     """Synchronise and return (and clear) the device status code (0 = OK)."""
     return int(lib().per_check(ctx, _stream(stream)))
+
+
+def per_debug_drop_tile(ctx: int, tile: int) -> None:
+    """Test-only fault injection: the next scan on ctx withholds tile
+    `tile`'s carry word, so waits for it run out (PER_ERR_TIMEOUT)."""
+    _check("per_debug_drop_tile", lib().per_debug_drop_tile(ctx, tile))
 
 
 def per_resample(logw: torch.Tensor, seed: int, offset: int, out_idx: torch.Tensor,

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/per.h"
 
 // Device status word bits (recorded by kernels, read by per_check).
@@ -56,6 +59,7 @@ struct per_ctx {
     unsigned* step_min;               // [3] per_step: call counter, then the batch minimum of p^alpha
                                       // (float bits) of even and odd calls
     unsigned long long* scan_xsum;    // [kScanXsumWords] chunk sums of the two-pass scan
+    int64_t drop_tile;                // per_debug_drop_tile: the tile or CTA whose message the next scan withholds (-1)
 
     // rank-based PER (PER_RANK): the radix sort's buffers, the order it
     // leaves, and the rank priorities with their CDF (which depend on the
@@ -106,6 +110,32 @@ constexpr int64_t kRankMaxN = int64_t(1) << 24;
 inline int64_t rank_count_words(int64_t cap) {
     const int64_t tiles = (cap + kRankSmallTile - 1) / kRankSmallTile;
     return kRadixDigits * (tiles > 64 ? tiles : 64);
+}
+
+// Launch set-up that is done once per device (a kernel's dynamic shared-memory
+// limit is a per-device function attribute, and occupancy is asked of the
+// current device): device_cached returns the value `init` computed the first
+// time this cache was used on the current device (init runs with that device
+// current, under the cache's lock), or 0 when init returned 0 or the device
+// ordinal is not below kMaxDevices.
+constexpr int kMaxDevices = 64;
+struct DeviceCache {
+    std::mutex mu;
+    std::atomic<int> value[kMaxDevices] = {};
+};
+template <class Init>
+int device_cached(DeviceCache& cache, Init init) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int v = cache.value[dev].load(std::memory_order_acquire);
+    if (v != 0) return v;
+    std::lock_guard<std::mutex> lock(cache.mu);
+    v = cache.value[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = init();
+        cache.value[dev].store(v, std::memory_order_release);
+    }
+    return v;
 }
 
 // Host-side launch accounting (per_launch_count).

@@ -102,6 +102,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     c->alpha = alpha;
     c->flags = flags;
     c->scan_desc_tiles = std::min<int64_t>((c->alloc_n + 1023) / 1024, kMaxWaveTiles);
+    c->drop_tile = -1;
     c->coarse_n = c->alloc_n / kCoarseStride + 1;
     // the sampler's CTAs: at most max(B / 1024, n / 4096) + 1 of them
     c->sample_bounds_n = std::max<int64_t>(int64_t(1) << 14, c->alloc_n / 4096) + 2;
@@ -362,6 +363,12 @@ per_status per_total_host(per_ctx* ctx, int mode, float* h_out, void* stream) {
     }
     if (cudaMemcpyAsync(h_out, src, sizeof(float), cudaMemcpyDeviceToHost, s) != cudaSuccess) return PER_ERR_CUDA;
     return cuda_status(cudaStreamSynchronize(s));
+}
+
+per_status per_debug_drop_tile(per_ctx* ctx, int64_t tile) {
+    if (!ctx || tile < -1) return PER_ERR_ARG;
+    ctx->drop_tile = tile;
+    return PER_OK;
 }
 
 per_status per_check(per_ctx* ctx, void* stream) {

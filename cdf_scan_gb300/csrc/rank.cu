@@ -457,13 +457,14 @@ per_status launch_rank_build(per_ctx* ctx, cudaStream_t s) {
     S.status = ctx->status;
     S.ticket = ctx->tickets + TK_RANK;
     S.n = n;
-    static int per_sm = 0;  // resident CTAs per SM of the cooperative kernel
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, radix_sort_small_kernel, kSortThreads, 0) !=
-            cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
-    }
+    static DeviceCache cache;  // resident CTAs per SM of the cooperative kernel
+    const int per_sm = device_cached(cache, []() {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, radix_sort_small_kernel, kSortThreads, 0) != cudaSuccess)
+            return 0;
+        return b < 1 ? 1 : b;
+    });
+    if (per_sm == 0) return PER_ERR_CUDA;
     const int small_tiles = (n + kRankSmallTile - 1) / kRankSmallTile;
     if (small_tiles <= kSmallMaxTiles && small_tiles <= per_sm * ctx->num_sms) {
         S.tiles = small_tiles;

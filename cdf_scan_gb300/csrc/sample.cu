@@ -155,15 +155,17 @@ per_status launch_coarse_cfg(const SampleParams& P, cudaStream_t s) {
     const int per_cta = THREADS * SPT;
     const unsigned grid = static_cast<unsigned>((P.B + per_cta - 1) / per_cta);
     const int smem = (kCoarseCap + kWindowCap) * static_cast<int>(sizeof(float));
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    static DeviceCache cache;
+    const int per_sm = device_cached(cache, [&]() {
+        int b = 0;
         if (cudaFuncSetAttribute(sample_coarse_kernel<THREADS, SPT, WEIGHTS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_coarse_kernel<THREADS, SPT, WEIGHTS>,
-                                                          THREADS, smem) != cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
-    }
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, sample_coarse_kernel<THREADS, SPT, WEIGHTS>, THREADS,
+                                                          smem) != cudaSuccess)
+            return 0;
+        return b < 1 ? 1 : b;
+    });
+    if (per_sm == 0) return PER_ERR_CUDA;
     if (!WEIGHTS) {
         sample_coarse_kernel<THREADS, SPT, WEIGHTS><<<grid, THREADS, smem, s>>>(P);
         per_note_launch();
@@ -195,14 +197,15 @@ per_status launch_cfg(const SampleParams& P, int* bounds, int64_t bounds_n, cuda
     const int per_cta = THREADS * SPT;
     const unsigned grid = static_cast<unsigned>((P.B + per_cta - 1) / per_cta);
     // the staging buffer plus the static barrier words exceed the default
-    // 48 KB dynamic limit: opt in once per instantiation
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(sample_scan_kernel<THREADS, SPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kWindowCap * sizeof(float))) != cudaSuccess)
-            return PER_ERR_CUDA;
-        configured = true;
-    }
+    // 48 KB dynamic limit: opt in once per instantiation and device
+    static DeviceCache cache;
+    if (!device_cached(cache, []() {
+            return cudaFuncSetAttribute(sample_scan_kernel<THREADS, SPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kWindowCap * sizeof(float))) == cudaSuccess
+                       ? 1
+                       : 0;
+        }))
+        return PER_ERR_CUDA;
     if (!bounds || static_cast<int64_t>(grid) > bounds_n) return PER_ERR_STATE;
     sample_bounds_kernel<<<(2 * grid + 7) / 8, 256, 0, s>>>(P, bounds, per_cta, static_cast<int>(grid));
     per_note_launch();

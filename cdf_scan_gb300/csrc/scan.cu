@@ -290,9 +290,12 @@ __device__ __forceinline__ void exchange_prefix(const ScanParams& P, int64_t sg,
     compute_sync<THREADS>();
     if (threadIdx.x == 0) {
         __threadfence();  // this CTA's slot before its arrival
-        const unsigned long long t = atomicAdd(P.ticket, 1ull);
+        // (a CTA chosen by per_debug_drop_tile only reads the ticket: its
+        // arrival is lost, so nobody is last and every wait for `ready`
+        // runs out)
+        const unsigned long long t = c == P.drop_tile ? ld_relaxed_u64(P.ticket) : atomicAdd(P.ticket, 1ull);
         s_gen = t / static_cast<unsigned long long>(G) + 1ull;
-        s_last = (t % static_cast<unsigned long long>(G)) == static_cast<unsigned long long>(G - 1);
+        s_last = c != P.drop_tile && (t % static_cast<unsigned long long>(G)) == static_cast<unsigned long long>(G - 1);
         if (s_last) __threadfence();  // every CTA's slot is visible from here on
     }
     compute_sync<THREADS>();
@@ -558,15 +561,17 @@ per_status launch_scan_2p(ScanParams P, int num_sms, cudaStream_t s) {
     constexpr int TILE = WARPS * 32 * ITEMS;
     const size_t smem = static_cast<size_t>(STAGES) * TILE * sizeof(float);
     if (!P.xsum || !P.ticket) return PER_ERR_STATE;
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    static DeviceCache cache;
+    const int per_sm = device_cached(cache, [&]() {
+        int b = 0;
         if (cudaFuncSetAttribute(build_cdf_2p_kernel<ITEMS, STAGES, WARPS, MINB>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_2p_kernel<ITEMS, STAGES, WARPS, MINB>,
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, build_cdf_2p_kernel<ITEMS, STAGES, WARPS, MINB>,
                                                           WARPS * 32 + 32, smem) != cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
-    }
+            return 0;
+        return b;  // 0: the kernel does not fit an SM (a launch error)
+    });
+    if (per_sm == 0) return PER_ERR_CUDA;
     const int64_t tiles = (P.n + TILE - 1) / TILE;
     if (tiles > 0xffffffffll) return PER_ERR_ARG;
     P.num_tiles = static_cast<unsigned>(tiles);
@@ -611,13 +616,15 @@ __global__ void __launch_bounds__(THREADS) build_cdf_wave_kernel(ScanParams P) {
 template <int THREADS>
 per_status launch_scan_wave(ScanParams P, int num_sms, cudaStream_t s) {
     constexpr int TILE = THREADS * 8;
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, build_cdf_wave_kernel<THREADS>, THREADS, 0) !=
+    static DeviceCache cache;
+    const int per_sm = device_cached(cache, []() {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, build_cdf_wave_kernel<THREADS>, THREADS, 0) !=
             cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
-    }
+            return 0;
+        return b < 1 ? 1 : b;
+    });
+    if (per_sm == 0) return PER_ERR_CUDA;
     const int64_t tiles = (P.n + TILE - 1) / TILE;
     if (tiles > static_cast<int64_t>(num_sms) * per_sm || tiles > P.desc_tiles) return PER_ERR_STATE;
     cudaLaunchConfig_t cfg = {};
@@ -673,6 +680,8 @@ per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* c
     P.xsum = ctx->scan_xsum;
     P.ticket = ctx->tickets + TK_SCAN;
     P.seg_tiles = 0;
+    P.drop_tile = ctx->drop_tile;  // a fault injected for one call only
+    ctx->drop_tile = -1;
     return scan_dispatch(P, ctx->num_sms, s);
 }
 
@@ -690,10 +699,12 @@ per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* c
 //
 // The array is part of the library image: every GPU that loads the library
 // holds it (about 160 KiB) until the process exits.  All calls on a device
-// share it and it keeps the previous call's contents (its counters are left
-// ready for the next call by the kernel itself), so two calls whose kernels
-// overlap on the GPU -- different streams without ordering between them --
-// race on it and give wrong results.  Serialise calls per device.
+// share it and it keeps the previous call's contents: the kernels leave their
+// counters, ticket and ready word at rest for the next call even after a
+// bounded wait ran out, and their tile words carry a per-call tag, so
+// nothing needs re-arming.  Two calls whose kernels overlap on the GPU --
+// different streams without ordering between them -- race on it and give
+// wrong results.  Serialise calls per device.
 // ====================================================================
 
 namespace {
@@ -701,7 +712,7 @@ namespace {
 constexpr int64_t kNoAllocMaxN = int64_t(1) << 24;  // 16,777,216 items
 constexpr int64_t kNoAllocMaxTiles = kMaxWaveTiles;  // tiles of a one-wave scan
 constexpr int kNoAllocCtrWords = 8;                 // 16 x u32 counters
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxDevices = kMaxDevices;
 
 }  // namespace
 
@@ -742,7 +753,9 @@ extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, floa
     {
         // One-time set-up per device, done by the first call on that device
         // (with it current): resolve the array's device address -- in host
-        // code the array's name is only a host-side stand-in -- and clear it.
+        // code the array's name is only a host-side stand-in -- clear it,
+        // and wait for the clearing, so that later calls on any stream find
+        // it ready.
         std::lock_guard<std::mutex> lock(g_noalloc_mu);
         if (!g_noalloc_ptr[dev]) {
             void* addr = nullptr;
@@ -753,7 +766,7 @@ extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, floa
             noalloc_init_kernel<<<16, 256, 0, s>>>(p);
             noalloc_epoch_kernel<<<1, 1, 0, s>>>(reinterpret_cast<unsigned*>(p + kNoAllocStateWords));
             per_note_launch(2);
-            if (cudaGetLastError() != cudaSuccess) return PER_ERR_CUDA;
+            if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return PER_ERR_CUDA;
             g_noalloc_sms[dev] = sms;
             g_noalloc_ptr[dev] = p;
         }
@@ -777,6 +790,10 @@ extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, floa
     P.xsum = scratch + kNoAllocXsumOff;
     P.ticket = scratch + kNoAllocTicketOff;
     P.seg_tiles = 0;
-    // same kernel and tile choice as per_build_cdf; at most 4096 tiles for n <= 2^24
+    P.drop_tile = -1;
+    // same kernels and tile choice as per_build_cdf: the one-wave kernels use
+    // at most kMaxWaveTiles tile words (launch_scan_wave checks), and larger
+    // inputs go to the two-pass kernel, whose exchange words do not depend
+    // on n
     return scan_dispatch(P, g_noalloc_sms[dev], s);
 }

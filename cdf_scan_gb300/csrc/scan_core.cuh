@@ -33,6 +33,10 @@ struct ScanParams {
     unsigned long long* xsum;    // exchange words of the two-pass kernel (kScanXsumWords)
     unsigned long long* ticket;  // grid-barrier ticket (0 between calls)
     int64_t seg_tiles;           // tiles per segment
+    // fault injection for tests (per_debug_drop_tile): the tile (one-wave
+    // kernels) or CTA (two-pass kernel) whose carry word or exchange arrival
+    // this call withholds, or -1
+    int64_t drop_tile;
 };
 
 // fp32 (>= 0) -> fixed point with kFracBits fractional bits, truncating below
@@ -272,7 +276,7 @@ __device__ __forceinline__ unsigned wave_scan_tile(const ScanParams& P, int64_t 
     float agg = 0.f;
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) agg = agg + s_wtot[w];
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && c != P.drop_tile)
         *reinterpret_cast<volatile unsigned long long*>(P.desc + c * kDescStride) =
             (static_cast<unsigned long long>(tag_agg) << 32) | __float_as_uint(agg);
     if (warp == 0) {

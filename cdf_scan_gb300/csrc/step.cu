@@ -249,12 +249,14 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
     if (tiles > ctx->scan_desc_tiles) return PER_ERR_STATE;
     // every index an update may name lies in some CTA's tile
     if (n_upd > 0 && ctx->capacity > tiles * TILE) return PER_ERR_STATE;
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, per_step_kernel, kStepThreads, 0) != cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
-    }
+    static DeviceCache cache;
+    const int per_sm = device_cached(cache, []() {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, per_step_kernel, kStepThreads, 0) != cudaSuccess)
+            return 0;
+        return b < 1 ? 1 : b;
+    });
+    if (per_sm == 0) return PER_ERR_CUDA;
     if (tiles > static_cast<int64_t>(per_sm) * ctx->num_sms) return PER_ERR_STATE;
     StepParams S = {};
     S.scan.p = ctx->prio;
@@ -271,6 +273,8 @@ per_status launch_step(per_ctx* ctx, const int32_t* upd_idx, const float* upd_p,
     S.scan.status = ctx->status;
     S.scan.num_tiles = static_cast<unsigned>(tiles);
     S.scan.coarse = ctx->coarse;
+    S.scan.drop_tile = ctx->drop_tile;  // a fault injected for one call only
+    ctx->drop_tile = -1;
     S.B = B;
     S.seed = seed;
     S.offset = offset;

@@ -606,16 +606,16 @@ per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n
     const bool has_tree = (ctx->flags & PER_TREE) != 0;
     if (has_tree && n <= kSmallN) {
         const size_t smem = sizeof(SmallSmem);
-        static int max_cluster = 0;  // largest schedulable cluster size (per process)
-        if (max_cluster == 0) {
+        static DeviceCache cache;  // largest schedulable cluster size, per device
+        const int max_cluster = device_cached(cache, [&]() {
             if (cudaFuncSetAttribute(small_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)) != cudaSuccess)
-                return PER_ERR_CUDA;
+                return 0;
             const bool nonportable = cudaFuncSetAttribute(small_update_kernel,
                                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                                      cudaSuccess;
             cudaGetLastError();
-            max_cluster = 1;
+            int best = 1;
             for (int c = nonportable ? 16 : 8; c > 1; c >>= 1) {
                 cudaLaunchConfig_t q = {};
                 q.gridDim = dim3(c);
@@ -630,12 +630,14 @@ per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n
                 q.numAttrs = 1;
                 int nc = 0;
                 if (cudaOccupancyMaxActiveClusters(&nc, small_update_kernel, &q) == cudaSuccess && nc > 0) {
-                    max_cluster = c;
+                    best = c;
                     break;
                 }
                 cudaGetLastError();
             }
-        }
+            return best;
+        });
+        if (max_cluster == 0) return PER_ERR_CUDA;
         int C = max_cluster;
         while (C > 1 && (ctx->cap_pow2 >> 6) < C) C >>= 1;  // at least 64 leaves per CTA
         cudaLaunchConfig_t cfg = {};
@@ -659,12 +661,13 @@ per_status launch_update(per_ctx* ctx, const int32_t* idx, const float* p, int n
         return cuda_status(e);
     }
     if (!has_tree) {
-        static int per_sm = 0;
-        if (per_sm == 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, update_scan_kernel, 256, 0) != cudaSuccess)
-                return PER_ERR_CUDA;
-            if (per_sm < 1) per_sm = 1;
-        }
+        static DeviceCache cache;
+        const int per_sm = device_cached(cache, []() {
+            int b = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, update_scan_kernel, 256, 0) != cudaSuccess) return 0;
+            return b < 1 ? 1 : b;
+        });
+        if (per_sm == 0) return PER_ERR_CUDA;
         int ctas = (n + 255) / 256;
         if (ctas > per_sm * ctx->num_sms) ctas = per_sm * ctx->num_sms;
         cudaLaunchConfig_t cfg = {};

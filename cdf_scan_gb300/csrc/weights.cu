@@ -84,12 +84,13 @@ __global__ void __launch_bounds__(kThreads) is_weights_kernel(IswParams P) {
 }  // namespace
 
 per_status launch_is_weights(per_ctx* ctx, const int32_t* idx, int B, float beta, float* out, cudaStream_t s) {
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, is_weights_kernel, kThreads, 0) != cudaSuccess)
-            return PER_ERR_CUDA;
-        if (per_sm < 1) per_sm = 1;
-    }
+    static DeviceCache cache;
+    const int per_sm = device_cached(cache, []() {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, is_weights_kernel, kThreads, 0) != cudaSuccess) return 0;
+        return b < 1 ? 1 : b;
+    });
+    if (per_sm == 0) return PER_ERR_CUDA;
     IswParams P;
     P.idx = idx;
     P.B = B;

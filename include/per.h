@@ -151,12 +151,14 @@ per_status per_build_cdf(per_ctx* ctx, void* stream);
  * until the process exits; hence n <= 16,777,216 (2^24), larger n returns
  * PER_ERR_ARG without launching.  The first call on each device performs a
  * one-time set-up with that device current (resolves the array's address,
- * clears it with two small kernels on `stream`); make that first call before
- * any stream capture.  All calls on a device share the array: calls whose
- * work overlaps on the GPU (different streams with no ordering between them)
- * race and give wrong results -- serialise them.  Device-side errors
- * (negative/NaN priority, range, timeout; the ST_* bits of per_check) are
- * OR-ed into *d_status when d_status is not NULL.
+ * clears it with two small kernels on `stream` and synchronises `stream`);
+ * make that first call before any stream capture.  All calls on a device
+ * share the array: calls whose work overlaps on the GPU (different streams
+ * with no ordering between them) race and give wrong results -- serialise
+ * them.  Device-side errors (negative/NaN priority, range, a bounded wait
+ * that ran out: 1 = timeout, 2 = range, 4 = value) are OR-ed into *d_status;
+ * d_status is the call's only error channel, so with d_status == NULL they
+ * go unreported.  The array needs no re-arming after an error.
  */
 per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, float* d_cdf, int* d_status,
                                  void* stream);
@@ -304,6 +306,24 @@ const float* per_rank_cdf_ptr(const per_ctx* ctx);
  * PER_ERR_RANGE, PER_ERR_VALUE, PER_ERR_EMPTY.
  */
 per_status per_check(per_ctx* ctx, void* stream);
+
+/*
+ * per_debug_drop_tile -- fault injection for tests of the failure path (no
+ * counterpart on the pages; the failure-detection plan of this library):
+ * the NEXT scan on this context -- per_build_cdf, or the scan inside
+ * per_step / per_rank_build -- loses one message, as if it had been dropped:
+ * in the one-wave scan (inputs that fit one wave of CTAs) tile `tile` does
+ * not publish its carry word; in the two-pass scan of larger inputs CTA
+ * `tile` does not arrive at the exchange of chunk sums.  Every wait for it
+ * then runs out after the bounded-wait limit (about 2 s): the kernels record
+ * PER_ERR_TIMEOUT (read by per_check), stop waiting, finish, and leave the
+ * context usable for the next call, whose result is correct again.  That
+ * call's CDF (and samples) are unspecified.  Tiles of the one-wave scan are
+ * 2048 items (n <= 2^19) or 4096 items; a tile or CTA the call does not have
+ * changes nothing.  tile = -1 cancels.  Host-side only; the injection
+ * applies to one call and is then cleared.  Never needed outside tests.
+ */
+per_status per_debug_drop_tile(per_ctx* ctx, int64_t tile);
 
 /*
  * per_resample -- row-batched systematic resampling (POPCORNBENCH particle

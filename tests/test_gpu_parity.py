@@ -132,7 +132,7 @@ def test_cdf_total_matches_per_total():
 
 @pytest.mark.parametrize("N,B", [(8192, 1024), (262144, 8192), (1000, 1), (1000, 777), (5000, 20000),
                                  (1 << 20, 65536), (33, 1024)])
-def test_sample_scan_bit_exact_on_gpu_cdf(N, B):
+def test_sample_scan_bit_exact_on_gpu_cdf(N, B, band_report):
     p = workloads.abs_normal(N, workloads.rng(103, N))
     ctx, c = gpu_cdf(p, 0.6)
     out = torch.empty(B, dtype=torch.int32, device="cuda")
@@ -145,6 +145,8 @@ def test_sample_scan_bit_exact_on_gpu_cdf(N, B):
     C = oracle.cdf64(p, 0.6)
     own, u64 = oracle.sample_cdf_f64(C, B, 7, 1000)
     n_band = band_check(C, got, own, u64, 2e-6 * C[-1])
+    name = "small workload (N=8192, B=1024), scan" if (N, B) == (8192, 1024) else f"scan N={N} B={B}"
+    band_report(name, n_band, B, "2e-6 total")
     # an fp32 CDF cannot resolve boundaries closer than ~1 ulp of the total:
     # expect about (N * 1e-7) of the samples to sit that close to one
     assert n_band <= B * (1e-7 * N + 1e-3) + 2

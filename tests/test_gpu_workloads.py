@@ -35,6 +35,19 @@ def new_ctx(p, alpha, flags, capacity=None):
     return ctx
 
 
+def band_check(C, idx_gpu, idx_ref, u, band):
+    """Indices may differ only where u lies within `band` of a CDF value
+    between them (C: the oracle's fp64 CDF); returns the number of such
+    differences."""
+    bad = np.nonzero(idx_gpu != idx_ref)[0]
+    for k in bad:
+        lo, hi = sorted((int(idx_gpu[k]), int(idx_ref[k])))
+        lo = max(lo - 1, 0)
+        gap = np.min(np.abs(C[lo:hi + 1] - float(u[k])))
+        assert gap <= band, f"sample {k}: gpu {idx_gpu[k]} oracle {idx_ref[k]} gap {gap} > {band}"
+    return len(bad)
+
+
 # ------------------------------------------------------------ scan update ---
 
 @pytest.mark.parametrize("n_upd", [1, 7, 8192, 8193, 50000])
@@ -61,7 +74,7 @@ def test_scan_update_last_writer_wins(n_upd):
 
 # ------------------------------------------------------- minibatch loop -----
 
-def test_minibatch_loop_matches_oracle():
+def test_minibatch_loop_matches_oracle(band_report):
     """The bench step itself: N=262144, 32 rounds of build_cdf, sample 8192
     with IS weights (beta 0.4, per_sample_weighted), update 8192 at the
     sampled indices."""
@@ -71,6 +84,7 @@ def test_minibatch_loop_matches_oracle():
     ctx = new_ctx(p, alpha, SCAN)
     idx = torch.empty(B, dtype=torch.int32, device="cuda")
     w = torch.empty(B, dtype=torch.float32, device="cuda")
+    n_band = 0
     for r in range(R):
         per.per_build_cdf(ctx.handle)
         per.per_sample_weighted(ctx.handle, B, seed, r * B, SCAN, beta, idx, w)
@@ -83,18 +97,21 @@ def test_minibatch_loop_matches_oracle():
         got = host(idx)
         want, _ = oracle.sample_cdf_f32(c, B, seed, r * B)
         assert np.array_equal(got, want), f"round {r}"
+        own, u64 = oracle.sample_cdf_f64(C, B, seed, r * B)
+        n_band += band_check(C, got, own, u64, 2e-6 * C[-1])
         ww = host(w)
         assert ww.max() == 1.0
         assert np.max(np.abs(ww / oracle.is_weights(p, N, alpha, got, beta) - 1.0)) <= 1e-6
         p = oracle.apply_updates(p, got, newp)
         assert np.array_equal(host(per.read_priorities(ctx.handle, N)), p), f"round {r}"
+    band_report(f"minibatch workload (N={N}, {R} rounds x B={B}), scan", n_band, R * B, "2e-6 total")
     assert per.per_check(ctx.handle) == 0
 
 
 # ------------------------------------------------------------- stress -------
 
 @pytest.mark.parametrize("alpha", [0.6, 1.0])
-def test_stress_scan_and_sample_full_size(alpha):
+def test_stress_scan_and_sample_full_size(alpha, band_report):
     """N = 16,777,216 uniform(0,1]; B = 1,048,576 stratified samples."""
     S = workloads.STRESS
     p = workloads.stress_priorities()
@@ -106,8 +123,14 @@ def test_stress_scan_and_sample_full_size(alpha):
     assert np.max(np.abs(c - C)) <= 1e-5 * C[-1]
     out = torch.empty(S["B"], dtype=torch.int32, device="cuda")
     per.per_sample(ctx.handle, S["B"], 1, 0, SCAN, out)
+    got = host(out)
     want, _ = oracle.sample_cdf_f32(c, S["B"], 1, 0)
-    assert np.array_equal(host(out), want)
+    assert np.array_equal(got, want)
+    # against the oracle's own fp64 CDF: differences only within the 1e-5
+    # band of the 16M CDF tolerance
+    own, u64 = oracle.sample_cdf_f64(C, S["B"], 1, 0)
+    n_band = band_check(C, got, own, u64, 1e-5 * C[-1])
+    band_report(f"stress workload (N={p.size}, B={S['B']}, alpha={alpha}), scan", n_band, S["B"], "1e-5 total")
     assert per.per_check(ctx.handle) == 0
 
 
@@ -119,7 +142,7 @@ def test_stress_all_ones_is_exact():
     assert np.array_equal(host(per.read_cdf(ctx.handle))[:n], np.arange(1, n + 1, dtype=np.float32))
 
 
-def test_resample_full_size():
+def test_resample_full_size(band_report):
     """256 rows x 65,536 log-weights N(0, 2^2)."""
     R = workloads.RESAMPLE
     lw = workloads.resample_logw()
@@ -127,17 +150,22 @@ def test_resample_full_size():
     cdf = torch.empty((R["rows"], R["P"]), dtype=torch.float32, device="cuda")
     per.per_resample(dev(lw), 6, 0, out, out_cdf=cdf)
     got, c = host(out), host(cdf)
+    n_band = n_checked = 0
     for b in range(0, R["rows"], 5):  # every fifth row against the fp64 oracle
         U = oracle.u01_closed_open(6, 0, b)
         assert np.array_equal(got[b], oracle.resample_row_on_cdf(c[b], U))
-        _, C, _ = oracle.resample_row(lw[b], U)
+        own, C, u = oracle.resample_row(lw[b], U)
         assert np.max(np.abs(c[b] - C)) <= 2e-6
+        n_band += band_check(C, got[b], own, u, 2e-6)
+        n_checked += R["P"]
+    band_report(f"resample workload ({R['rows']} x {R['P']}, every 5th row), row CDF", n_band, n_checked,
+                "2e-6 (row total 1)")
     assert np.all(np.diff(got, axis=1) >= 0)
 
 
 # ---------------------------------------------------------------- heavy -----
 
-def test_heavy_workload_scan_and_tree_with_beta_ramp():
+def test_heavy_workload_scan_and_tree_with_beta_ramp(band_report):
     """N = 1,048,576 lognormal(0, 2) with 1% zeros, alpha 0.7, B = 65,536,
     beta 0.4 .. 1.0; both sampling paths."""
     Hv = workloads.HEAVY
@@ -157,6 +185,15 @@ def test_heavy_workload_scan_and_tree_with_beta_ramp():
     tree = host(per.read_tree(ctx.handle))
     assert np.array_equal(ib, oracle.sample_tree(tree, B, Hv["seed"], 0)[0])
     assert np.all(p[ia] > 0) and np.all(p[ib] > 0)
+    # both paths against the oracle's own fp64 CDF (scan thresholds from the
+    # fp64 total; the tree's from its root)
+    own, u64 = oracle.sample_cdf_f64(C, B, Hv["seed"], 0)
+    band_report(f"heavy workload (N={N}, B={B}), scan", band_check(C, ia, own, u64, 2e-6 * C[-1]), B,
+                "2e-6 total")
+    _, ut = oracle.sample_tree(tree, B, Hv["seed"], 0)
+    own_t = np.minimum(np.searchsorted(C, ut.astype(np.float64), side="left"), N - 1)
+    band_report(f"heavy workload (N={N}, B={B}), tree", band_check(C, ib, own_t, ut, 2e-6 * C[-1]), B,
+                "2e-6 total")
     w = torch.empty(B, dtype=torch.float32, device="cuda")
     for beta in Hv["betas"]:
         for flags_idx in (a, b):
@@ -170,12 +207,14 @@ def test_heavy_workload_scan_and_tree_with_beta_ramp():
 
 # ----------------------------------------------------------------- tree -----
 
-def test_tree_workload_steps():
+def test_tree_workload_steps(band_report):
     """Capacity 500,000 (2^19 leaves): initial fill 131,072 lognormal(0,1),
-    then steps of insert 4096 at the ring head, sample 1024, update 1024 with
-    20% duplicate indices.  Every sampled index bit-exact against the oracle's
-    descent of the GPU tree; the whole tree bit-exact against the oracle's
-    pairwise rebuild of the oracle's own leaves at checkpoints."""
+    then the workload's 400 steps of insert 4096 at the ring head, sample
+    1024, update 1024 with 20% duplicate indices.  Every sampled index
+    bit-exact against the oracle's descent of the GPU tree, and within the
+    boundary band of a search of the oracle's fp64 CDF of its own leaves;
+    the whole tree bit-exact against the oracle's pairwise rebuild of the
+    oracle's own leaves at checkpoints."""
     T = workloads.TREE
     cap, B, alpha = T["capacity"], T["B"], T["alpha"]
     prio = np.zeros(cap, np.float32)
@@ -186,7 +225,8 @@ def test_tree_workload_steps():
     size, head = init.size, init.size % cap
     per.per_set_size(ctx.handle, size)
     out = torch.empty(B, dtype=torch.int32, device="cuda")
-    steps = 120  # fills the ring (after ~91 steps) and wraps
+    steps = T["steps"]  # 400: the ring fills after ~91 steps and wraps
+    n_band = 0
     for s in range(steps):
         ins = workloads.tree_insert(s)
         ins_idx = ((head + np.arange(ins.size)) % cap).astype(np.int32)
@@ -198,18 +238,25 @@ def test_tree_workload_steps():
         per.per_sample(ctx.handle, B, T["seed"], s * B, TREE, out)
         got = host(out)
         tree = host(per.read_tree(ctx.handle))
-        assert np.array_equal(got, oracle.sample_tree(tree, B, T["seed"], s * B)[0]), f"step {s}"
+        want, ut = oracle.sample_tree(tree, B, T["seed"], s * B)
+        assert np.array_equal(got, want), f"step {s}"
         assert np.all(got < size)
+        if s % 20 == 0:  # the fp64 search of the oracle's own leaves
+            C = np.cumsum(oracle.pow_alpha64(prio, alpha))
+            own = np.minimum(np.searchsorted(C, ut.astype(np.float64), side="left"), cap - 1)
+            n_band += band_check(C, got, own, ut, 2e-6 * C[-1])
         uidx, up = workloads.tree_update_batch(s, got)
         per.per_update(ctx.handle, dev(uidx), dev(up))
         prio = oracle.apply_updates(prio, uidx, up)
-        if s % 30 == 29 or s == steps - 1:
+        if s % 50 == 49 or s == steps - 1:
             tree = host(per.read_tree(ctx.handle))
             leaves = tree[tree.size // 2:]
             want_leaves = oracle.tree_leaves(prio, alpha, tree.size // 2)
             d = np.abs(leaves.view(np.int32).astype(np.int64) - want_leaves.view(np.int32).astype(np.int64))
             assert d.max() <= 4, f"step {s}: leaves differ from pow beyond 4 ulp"
             assert np.array_equal(tree[1:], oracle.tree_build(leaves)[1:]), f"step {s}"
+    band_report(f"tree workload (2^19 leaves, every 20th of {steps} steps x B={B}), tree", n_band,
+                (steps + 19) // 20 * B, "2e-6 total")
     assert per.per_check(ctx.handle) == 0
 
 
