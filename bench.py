@@ -6,18 +6,30 @@ priorities |N(0,1)|+1e-6, alpha=0.6, 32 rounds of
   |N(0,1)|+1e-6 priorities -> build_cdf -> sample 8192 stratified with
   their IS weights (beta=0.4)
 through the library's C ABI, one per_step call per round (one cooperative
-launch: update, rebuild, sample and weights with grid barriers between).  value = sampled transitions per second over
-all ranks (device-resident inputs); e2e = the same with each step's new
-priorities copied in from pinned host memory and the step's indices and
-weights copied back, inside the timed region.
+launch: update, rebuild, sample and weights with grid barriers between).
+value = sampled transitions per second over all ranks (device-resident
+inputs); e2e = the same with each step's new priorities copied in from pinned
+host memory and the step's indices and weights copied back, inside the timed
+region.
+
+The JSON line also carries one record per workload of the method (key
+"configs": small, minibatch, tree, heavy, stress, resample), each with its
+own timings, a roofline for its dominant kernel against the algorithmic
+bytes of that workload, the CPU oracle timed on a bounded sample of the same
+workload, and the number of sampled indices that differ from the oracle's
+search of its own fp64 CDF (only boundary-band differences are possible; the
+tests check the band).
+
+L2 is flushed before every timed replay where the record says so: a 512 MiB
+buffer is written and then another 512 MiB buffer is read, so that no input
+is cached and the flush leaves no dirty lines to be written back inside the
+timed region (the 16M scan is also reported after a write-only flush).
 
 --impl reference times the CPU oracle (serial C, fp64) on the same workload
 on this host's cores.  With torchrun, every rank runs an independent replica
 ("replicas only": the method has no exchange step); rank 0 prints one JSON
 line.
 """
-from __future__ import annotations
-
 import argparse
 import hashlib
 import json
@@ -42,18 +54,23 @@ WORKLOAD = (f"minibatch N={N} fp32 |N(0,1)|+1e-6, alpha={ALPHA}, {ROUNDS} rounds
             f"(build_cdf, sample {B} stratified, IS weights beta={BETA}, update {B} at sampled indices)")
 L2_FLUSH_BYTES = 512 << 20
 
-# algorithmic bytes per launch: what each kernel must read and write at least
+# Algorithmic bytes per launch -- what each kernel must read and write at
+# least -- for the minibatch workload's calls.  One fused round (per_step):
+# the scan reads p and writes the CDF (8 B per item), each of the B samples
+# writes its index and reads at most one 32-byte sector of the CDF, the
+# update reads an index and a priority (8 B per sample) and the IS weights
+# gather p and write a weight (8 B per sample).
 KERNEL_BYTES = {
-    "build_cdf": lambda: 8 * N,                          # 4 B read + 4 B write per item
-    "sample_is_weights": lambda: 4 * N + 12 * B,         # CDF windows once; index, p gather, weight
-    "update": lambda: 8 * B + 4 * B + 8 * B,             # idx + p read, priority write, winner slot
+    "build_cdf": lambda: 8 * N,
+    "sample_is_weights": lambda: B * (4 + 32) + 8 * B,
+    "update": lambda: 8 * B,
 }
+KERNEL_BYTES["step"] = lambda: 8 * N + B * (4 + 32) + 8 * B + 8 * B
 # Per key, the radix sort's four passes: pass 0 reads the priorities twice
 # (histogram, scatter) and writes keys and values (16 B); passes 1 and 2 read
 # the keys twice and the values once and write both (20 B each); pass 3 reads
 # the same and writes the order and its inverse (20 B).
 RANK_SORT_BYTES_PER_KEY = 16 + 20 + 20 + 20
-KERNEL_BYTES["step"] = lambda: sum(KERNEL_BYTES[k]() for k in ("update", "build_cdf", "sample_is_weights"))
 
 
 def env_rank():
@@ -85,7 +102,8 @@ def job_throughput(steps, world, t_ms):
 
 def config_dict(n_gpus):
     return {"workload": WORKLOAD, "N": N, "B": B, "rounds_per_step": ROUNDS, "alpha": ALPHA, "beta": BETA,
-            "parallelism": f"replicas x{n_gpus}", "l2": "flushed (512 MiB write) between timed steps"}
+            "parallelism": f"replicas x{n_gpus}",
+            "l2": "flushed between timed steps (512 MiB write, then 512 MiB read of another buffer)"}
 
 
 def load_peaks():
@@ -153,6 +171,64 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm -------
 
+class L2Flush:
+    """Evicts L2 between timed replays: writes one 512 MiB buffer, then reads
+    another (so L2 ends up holding clean lines of neither input); `dirty`
+    only writes."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.a = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.b = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def clean(self):
+        self.a.zero_()
+        self.torch.sum(self.b, dim=0, out=self.acc)
+
+    def dirty(self):
+        self.a.zero_()
+
+
+def graph_of(torch, body):
+    """CUDA graph of body() captured on a side stream."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        body()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, reps, flush=None, per_replay=1):
+    """Median microseconds per body (replay time / per_replay) between CUDA
+    events recorded on the replaying stream; flush() before each replay."""
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3 / per_replay)
+    return statistics.median(ts)
+
+
+def roofline(kernel, algo_bytes, us, peak, peak_kind, traffic=None, note=None):
+    achieved = algo_bytes / (us * 1e-6) / 1e9
+    r = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind,
+         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic, "avg_launch_us": round(us, 3),
+         "algorithmic_bytes_per_launch": int(algo_bytes)}
+    if note:
+        r["note"] = note
+    return r
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import cdf_scan_gb300 as per
@@ -173,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
     h_newp = torch.from_numpy(newp).pin_memory()
     h_idx = torch.empty((ROUNDS, B), dtype=torch.int32).pin_memory()
     h_w = torch.empty((ROUNDS, B), dtype=torch.float32).pin_memory()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     ctx = per.PerContext(N, ALPHA, per.PER_SCAN)
     h = ctx.handle
     per.per_set_priorities(h, d_p0)
@@ -200,13 +276,8 @@ def run_ours(args, rank, world, local_rank):
                 fn(r)
 
     def capture(body):
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
         before = per.per_launch_count()
-        with torch.cuda.graph(g, stream=s):
-            body()
-        torch.cuda.synchronize()
+        g = graph_of(torch, body)
         return g, per.per_launch_count() - before
 
     for _ in range(max(args.warmup, 1)):
@@ -215,8 +286,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     step_graph, kernels_per_step = capture(step_eager)
     split_graph, _ = capture(lambda: step_eager(split_calls))
-    kind_graphs = {k: capture(lambda fn=fn: [fn(r) for r in range(ROUNDS)])[0]
-                   for k, fn in {**calls, **split_calls}.items()}
+    kind_graphs = {k: capture(lambda fn=fn: [fn(r) for r in range(ROUNDS)])[0] for k, fn in split_calls.items()}
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -228,7 +298,7 @@ def run_ours(args, rank, world, local_rank):
     def timed(steps, graph, e2e=False):
         total_ms = 0.0
         for _ in range(steps):
-            flush.zero_()
+            flush.clean()
             barrier()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
@@ -254,8 +324,8 @@ def run_ours(args, rank, world, local_rank):
     t_ms = timed(args.steps, step_graph)
     clk = clocks.stop()
     e2e_ms = timed(args.steps, step_graph, e2e=True)
-    # per-kernel durations: each call kind replayed alone (32 launches per
-    # replay, L2 flushed before each replay, as in the step)
+    # the same round as three separate calls, each kind replayed alone (32
+    # launches per replay, L2 flushed before each replay), and as a whole
     kreps = max(3, min(args.steps, 50))
     per_kernel = {k: timed(kreps, g) / (kreps * ROUNDS) for k, g in kind_graphs.items()}
     split_ms = timed(kreps, split_graph) / kreps
@@ -268,14 +338,13 @@ def run_ours(args, rank, world, local_rank):
     result = None
     if rank == 0:
         peak, peak_kind = load_peaks()
-        name = "step"  # the one kernel of the timed step
-        avg_s = per_kernel[name] / 1e3
-        algo = KERNEL_BYTES[name]()
-        achieved = algo / avg_s / 1e9
-        roofline = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
-                    "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                    "traffic": traffic_for(name), "avg_launch_us": round(avg_s * 1e6, 3),
-                    "algorithmic_bytes_per_launch": algo}
+        # the roofline kernel's duration from the timed replays themselves: the
+        # step is 32 launches of it, so a launch averages ms_per_step / 32
+        # (gaps between the graph's launches included: an upper bound)
+        step_us = t_ms / args.steps / ROUNDS * 1e3
+        rl = roofline("per_step_kernel (update + build_cdf + sample + IS weights, one launch)", KERNEL_BYTES["step"](),
+                      step_us, peak, peak_kind, traffic_for("step"),
+                      note="latency-bound: the working set (1 MiB of priorities, 1 MiB of CDF) stays in L2")
         result = {
             "metric": METRIC, "value": job_throughput(args.steps, world, t_ms), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps,
@@ -285,21 +354,26 @@ def run_ours(args, rank, world, local_rank):
                     "h2d_bytes_per_step": int(ROUNDS * B * 4),
                     "d2h_bytes_per_step": int(ROUNDS * B * 8)},
             "gpu_launches": int(kernels_per_step * args.steps),
-            "roofline": roofline,
-            "kernel_us_per_launch": {k: round(v * 1e3, 3) for k, v in per_kernel.items()},
-            "us_per_round": round(t_ms / args.steps / ROUNDS * 1e3, 2),
+            "roofline": rl,
+            "kernel_us_per_launch": {"step": round(step_us, 3),
+                                     **{k: round(v * 1e3, 3) for k, v in per_kernel.items()}},
+            "us_per_round": round(step_us, 2),
             "split_calls_us_per_round": round(split_ms / ROUNDS * 1e3, 2),
             "clocks": clk,
             "impl": "gb300",
             "notes": "step = one CUDA-graph replay of 32 per_step calls through the C ABI (one cooperative "
-                     "launch per round); kernel_us_per_launch also times the three separate calls of the same "
-                     "round (update, build_cdf, sample_is_weights) and split_calls_us_per_round the round as "
-                     "those three launches; RNG offsets are fixed per captured round while the priority state "
-                     "evolves across steps",
+                     "launch per round); kernel_us_per_launch.step = ms_per_step / 32 from the timed replays; the "
+                     "other entries time the three separate calls of the same round (update, build_cdf, "
+                     "sample_is_weights), each kind alone, and split_calls_us_per_round the round as those three "
+                     "launches; RNG offsets are fixed per captured round while the priority state evolves across "
+                     "steps",
         }
-        if not args.no_extras:
-            result["extras"] = extras(per, torch, dev, peak)
     ctx.close()
+    if rank == 0 and not args.no_extras:
+        result["configs"], result["extras"], checks = measure_configs(per, torch, dev, peak, peak_kind, flush,
+                                                                      result)
+        if world == 1:
+            oracle_legs(result["configs"], checks, args.cpu_seconds)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -329,61 +403,339 @@ def traffic_for(kernel_name):
         return None
 
 
-def extras(per, torch, dev, peak):
-    """Other headline numbers of the metric, measured in the same run (not
-    the bench value): the 16M scan against HBM, the 1M-sample sampler, and
-    the tree sample+update step at full fill.  Each is a CUDA graph replayed
-    between CUDA events on the capturing stream."""
-    out = {}
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+def measure_configs(per, torch, dev, peak, peak_kind, flush, head):
+    """One record per workload, measured in this run; returns (configs,
+    extras, checks), `checks` holding the GPU results that the oracle legs
+    compare with."""
+    cfg, checks, extras = {}, {}, {}
+    tensor = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
 
-    def graph_of(body):
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            body()
-        torch.cuda.synchronize()
-        return g
+    # ---- small: N = 8192, B = 1024 (latency-bound: 64 KiB, L2-resident)
+    Sm = workloads.SMALL
+    n, b = Sm["N"], Sm["B"]
+    p = workloads.small_priorities()
+    ctx = per.PerContext(n, Sm["alpha"], per.PER_SCAN)
+    per.per_set_priorities(ctx.handle, tensor(p))
+    i_s = torch.empty(b, dtype=torch.int32, device=dev)
+    w_s = torch.empty(b, dtype=torch.float32, device=dev)
+    per.per_build_cdf(ctx.handle)
+    per.per_sample(ctx.handle, b, Sm["seed"], 0, per.PER_SCAN, i_s)
+    checks["small"] = {"p": p, "idx": i_s.cpu().numpy()}
+    reps = 32
+    us = {
+        "build_cdf": time_graph(torch, graph_of(torch, lambda: [per.per_build_cdf(ctx.handle) for _ in range(reps)]),
+                                50, per_replay=reps),
+        "sample": time_graph(torch, graph_of(torch, lambda: [per.per_sample(ctx.handle, b, Sm["seed"], 0,
+                                                                           per.PER_SCAN, i_s) for _ in range(reps)]),
+                             50, per_replay=reps),
+        "is_weights": time_graph(torch, graph_of(torch, lambda: [per.per_is_weights(ctx.handle, i_s, Sm["beta"], w_s)
+                                                                 for _ in range(reps)]), 50, per_replay=reps),
+        "combined_three_calls": time_graph(torch, graph_of(torch, lambda: [
+            (per.per_build_cdf(ctx.handle), per.per_sample(ctx.handle, b, Sm["seed"], 0, per.PER_SCAN, i_s),
+             per.per_is_weights(ctx.handle, i_s, Sm["beta"], w_s)) for _ in range(reps)]), 50, per_replay=reps),
+        "combined_per_step": time_graph(torch, graph_of(torch, lambda: [
+            per.per_step(ctx.handle, None, None, b, Sm["seed"], 0, per.PER_SCAN, Sm["beta"], i_s, w_s)
+            for _ in range(reps)]), 50, per_replay=reps),
+    }
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
+    cfg["small"] = {
+        "workload": f"N={n} fp32 |N(0,1)|+1e-6, alpha={Sm['alpha']}, beta={Sm['beta']}, B={b} stratified",
+        "us_per_call": {k: round(v, 2) for k, v in us.items()},
+        "samples_per_s": b / (us["combined_per_step"] * 1e-6),
+        "roofline": roofline("build_cdf_wave_kernel<256>", 8 * n, us["build_cdf"], peak, peak_kind,
+                             note="latency-bound: 64 KiB, L2-resident; the pages' point of comparison (PufferLib "
+                                  "PR #615 section 1: 90 us serial, 7.5 us two-level, GPU not stated)"),
+        "l2": "warm (the 64 KiB buffer stays resident between calls); graph of 32 calls per replay"}
 
-    def time_graph(g, reps, flush_l2=True, per_replay=1):
-        stream = torch.cuda.current_stream()
-        ts = []
-        for _ in range(reps):
-            if flush_l2:
-                flush.zero_()
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3 / per_replay)
-        return statistics.median(ts)
+    # ---- minibatch: the headline step (above); its record
+    cfg["minibatch"] = {
+        "workload": WORKLOAD, "us_per_round": head["us_per_round"],
+        "split_calls_us_per_round": head["split_calls_us_per_round"], "samples_per_s": head["value"],
+        "ms_per_32_rounds": head["ms_per_step"],
+        "vs_serial_scan_on_the_pages": "PufferLib PR #615 section 1: 32 x 2.85 ms of serial build_cdf per train "
+                                       "call at B=262144 (GPU not stated)",
+        "roofline": head["roofline"], "l2": head["config"]["l2"]}
+    ctx = per.PerContext(N, ALPHA, per.PER_SCAN)
+    p = workloads.minibatch_priorities()
+    per.per_set_priorities(ctx.handle, tensor(p))
+    i_m = torch.empty(B, dtype=torch.int32, device=dev)
+    w_m = torch.empty(B, dtype=torch.float32, device=dev)
+    per.per_step(ctx.handle, None, None, B, W["seed"], 0, per.PER_SCAN, BETA, i_m, w_m)
+    checks["minibatch"] = {"p": p, "idx": i_m.cpu().numpy()}
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
 
+    # ---- tree: capacity 500,000 (2^19 leaves); the 400-step growth loop
+    T = workloads.TREE
+    cap, tb = T["capacity"], T["B"]
+    ctx = per.PerContext(cap, T["alpha"], per.PER_TREE)
+    prio = np.zeros(cap, np.float32)
+    init = workloads.tree_initial()
+    prio[:init.size] = init
+    per.per_set_priorities(ctx.handle, tensor(prio))
+    size, head_pos = init.size, init.size % cap
+    per.per_set_size(ctx.handle, size)
+    out = torch.empty(tb, dtype=torch.int32, device=dev)
+    # a first pass draws every step's samples, so that the timed pass can
+    # enqueue all 400 steps (insert, sample, update) without host work between
+    steps = T["steps"]
+    plan = []
+    for s in range(steps):
+        ins = workloads.tree_insert(s)
+        ins_idx = ((head_pos + np.arange(ins.size)) % cap).astype(np.int32)
+        per.per_update(ctx.handle, tensor(ins_idx), tensor(ins))
+        prio = workloads_apply(prio, ins_idx, ins)
+        head_pos = (head_pos + ins.size) % cap
+        size = min(size + ins.size, cap)
+        per.per_set_size(ctx.handle, size)
+        per.per_sample(ctx.handle, tb, T["seed"], s * tb, per.PER_TREE, out)
+        ui, up = workloads.tree_update_batch(s, out.cpu().numpy())
+        per.per_update(ctx.handle, tensor(ui), tensor(up))
+        prio = workloads_apply(prio, ui, up)
+        plan.append((tensor(ins_idx), tensor(ins), size, tensor(ui), tensor(up)))
+    checks["tree"] = {"prio": prio, "size": size}
+    per.per_sample(ctx.handle, tb, T["seed"], steps * tb, per.PER_TREE, out)
+    checks["tree"]["idx"] = out.cpu().numpy()
+    ctx.close()
+    ctx = per.PerContext(cap, T["alpha"], per.PER_TREE)
+    prio0 = np.zeros(cap, np.float32)
+    prio0[:init.size] = init
+    per.per_set_priorities(ctx.handle, tensor(prio0))
+    per.per_set_size(ctx.handle, init.size)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s, (ii, iv, sz, ui, up) in enumerate(plan):
+        ev[s][0].record(stream)
+        per.per_update(ctx.handle, ii, iv)
+        per.per_set_size(ctx.handle, sz)
+        ev[s][1].record(stream)
+        per.per_sample(ctx.handle, tb, T["seed"], s * tb, per.PER_TREE, out)
+        per.per_update(ctx.handle, ui, up)
+        ev[s][2].record(stream)
+    torch.cuda.synchronize()
+    ins_us = [ev[s][0].elapsed_time(ev[s][1]) * 1e3 for s in range(steps)]
+    stp_us = [ev[s][1].elapsed_time(ev[s][2]) * 1e3 for s in range(steps)]
+    assert per.per_check(ctx.handle) == 0
+    fill_curve = []
+    for lo in range(0, steps, 25):
+        sl = slice(lo, min(lo + 25, steps))
+        fill_curve.append({"steps": f"{lo}-{sl.stop - 1}", "fill": int(plan[sl.stop - 1][2]),
+                           "step_us": round(statistics.median(stp_us[sl]), 2),
+                           "insert_us": round(statistics.median(ins_us[sl]), 2)})
+    # the steady state at full fill: a graph of 8 sample + update steps
+    tidx = torch.empty(tb, dtype=torch.int32, device=dev)
+    ups = plan[-8:]
+
+    def tree_steps(mode=per.PER_TREE):
+        for s in range(8):
+            per.per_sample(ctx.handle, tb, T["seed"], s * tb, mode, tidx)
+            per.per_update(ctx.handle, ups[s][3], ups[s][4])
+    tree_steps()
+    us_t = time_graph(torch, graph_of(torch, tree_steps), 50, per_replay=8)
+    tree_steps(per.PER_TREE | per.PER_IID)
+    us_i = time_graph(torch, graph_of(torch, lambda: tree_steps(per.PER_TREE | per.PER_IID)), 50, per_replay=8)
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
+    levels = 19
+    cfg["tree"] = {
+        "workload": f"segment tree capacity {cap} (2^19 leaves, fp32), fill {init.size} -> {cap} by insert_batch of "
+                    f"{T['insert']} lognormal(0,1); per step sample {tb}, update {tb} (20% duplicate indices); "
+                    f"{steps} steps; alpha={T['alpha']}",
+        "sample_update_step_us": round(us_t, 2), "target_us": 20.0,
+        "iid_sample_update_step_us": round(us_i, 2),
+        "insert_us_median": round(statistics.median(ins_us), 2),
+        "step_us_median_over_400": round(statistics.median(stp_us), 2),
+        "time_vs_fill": fill_curve,
+        "vs_pages": "foxhunt 'GPU Segment Tree for PER Sampling': O(n) prefix-sum sampling grew 5 -> 23 ms as the "
+                    "buffer filled 128K -> 500K on an H100; ~0.1 ms expected for the tree",
+        "roofline": roofline("sample_tree_kernel<128> + small_update_kernel",
+                             tb * levels * 8 + 12 * sum(min(1 << lv, 820) for lv in range(levels + 1)),
+                             us_t, peak, peak_kind,
+                             note="latency-bound: dependent loads down 19 levels of an L2-resident 4 MiB tree"),
+        "l2": "warm (the 4 MiB tree stays resident across steps); steady state: graph of 8 steps per replay; "
+              "growth loop: CUDA events around every step of all 400, enqueued back to back"}
+
+    # ---- heavy: N = 1,048,576 lognormal(0, 2), 1% zeros, alpha 0.7, B = 65536
+    Hv = workloads.HEAVY
+    p = workloads.heavy_priorities()
+    n, b = p.size, Hv["B"]
+    ctx = per.PerContext(n, Hv["alpha"], per.PER_SCAN | per.PER_TREE)
+    per.per_set_priorities(ctx.handle, tensor(p))
+    ia = torch.empty(b, dtype=torch.int32, device=dev)
+    ib = torch.empty(b, dtype=torch.int32, device=dev)
+    w_h = torch.empty(b, dtype=torch.float32, device=dev)
+    per.per_build_cdf(ctx.handle)
+    per.per_sample(ctx.handle, b, Hv["seed"], 0, per.PER_SCAN, ia)
+    per.per_sample(ctx.handle, b, Hv["seed"], 0, per.PER_TREE, ib)
+    checks["heavy"] = {"p": p, "idx_scan": ia.cpu().numpy(), "idx_tree": ib.cpu().numpy(),
+                       "tree_root": float(per.read_tree(ctx.handle)[1].item())}
+    us = {
+        "build_cdf": time_graph(torch, graph_of(torch, lambda: per.per_build_cdf(ctx.handle)), 30, flush.clean),
+        "sample_scan": time_graph(torch, graph_of(torch, lambda: per.per_sample(ctx.handle, b, Hv["seed"], 0,
+                                                                             per.PER_SCAN, ia)), 30, flush.clean),
+        "sample_tree": time_graph(torch, graph_of(torch, lambda: per.per_sample(ctx.handle, b, Hv["seed"], 0,
+                                                                             per.PER_TREE, ib)), 30, flush.clean),
+        "is_weights_7_betas": time_graph(torch, graph_of(torch, lambda: [per.per_is_weights(ctx.handle, ia, beta, w_h)
+                                                                         for beta in Hv["betas"]]), 30, flush.clean),
+    }
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
+    cfg["heavy"] = {
+        "workload": f"N={n} lognormal(0, sigma 2) with 1% exact zeros, alpha={Hv['alpha']}, B={b} stratified, IS "
+                    f"weights at beta {Hv['betas'][0]}..{Hv['betas'][-1]}; scan and tree paths",
+        "us_per_call": {k: round(v, 2) for k, v in us.items()},
+        "build_cdf_gbs": round(8 * n / (us["build_cdf"] * 1e-6) / 1e9, 1),
+        "samples_per_s_scan": b / (us["sample_scan"] * 1e-6),
+        "roofline": roofline("build_cdf_wave_kernel<512>", 8 * n, us["build_cdf"], peak, peak_kind,
+                             note="8 MiB each way: one wave of tiles, latency-dominated"),
+        "l2": "flushed before each rep (512 MiB write + 512 MiB read of other buffers)"}
+
+    # ---- stress: N = 16,777,216 uniform(0,1], B = 1,048,576
     S = workloads.STRESS
-    n = S["N"]
+    p = workloads.stress_priorities()
+    n, b = p.size, S["B"]
     ctx = per.PerContext(n, S["alpha"], per.PER_SCAN)
-    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
+    per.per_set_priorities(ctx.handle, tensor(p))
     for _ in range(3):
         per.per_build_cdf(ctx.handle)
-    us = time_graph(graph_of(lambda: per.per_build_cdf(ctx.handle)), 30)
-    gbs = 8 * n / (us * 1e-6) / 1e9
-    idx = torch.empty(S["B"], dtype=torch.int32, device=dev)
-    per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx)
-    us_s = time_graph(graph_of(lambda: per.per_sample(ctx.handle, S["B"], 1, 0, per.PER_SCAN, idx)), 20)
-    out["stress_build_cdf"] = {"N": n, "us": round(us, 2), "gbs": round(gbs, 1), "frac_of_measured_peak":
-                               round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
-                               "l2": "flushed before each rep", "timing": "one-call graph between events"}
-    out["stress_sample"] = {"B": S["B"], "us": round(us_s, 2), "samples_per_s": S["B"] / (us_s * 1e-6),
-                            "l2": "flushed before each rep"}
-    if per.per_check(ctx.handle) != 0:
-        out["stress_build_cdf"]["status"] = "device status not clean"
+    g_scan = graph_of(torch, lambda: per.per_build_cdf(ctx.handle))
+    us_scan = time_graph(torch, g_scan, 30, flush.clean)
+    us_scan_dirty = time_graph(torch, g_scan, 30, flush.dirty)
+    i_st = torch.empty(b, dtype=torch.int32, device=dev)
+    per.per_sample(ctx.handle, b, 1, 0, per.PER_SCAN, i_st)
+    us_samp = time_graph(torch, graph_of(torch, lambda: per.per_sample(ctx.handle, b, 1, 0, per.PER_SCAN, i_st)),
+                         20, flush.clean)
+    checks["stress"] = {"p": p, "idx": i_st.cpu().numpy()}
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
+    ctx = per.PerContext(n, 1.0, per.PER_SCAN)
+    per.per_set_priorities(ctx.handle, tensor(p))
+    per.per_build_cdf(ctx.handle)
+    us_scan1 = time_graph(torch, graph_of(torch, lambda: per.per_build_cdf(ctx.handle)), 30, flush.clean)
+    ctx.close()
+    samp_bytes = min(4 * n, b * 32) + 4 * b
+    cfg["stress"] = {
+        "workload": f"N={n} fp32 uniform(0,1], alpha={S['alpha']} (and 1.0); build_cdf + sample {b} stratified",
+        "build_cdf_us": round(us_scan, 2), "build_cdf_us_alpha1": round(us_scan1, 2),
+        "build_cdf_us_after_write_only_flush": round(us_scan_dirty, 2),
+        "build_cdf_gbs": round(8 * n / (us_scan * 1e-6) / 1e9, 1),
+        "build_cdf_frac_of_nominal_8tbs": round(8 * n / (us_scan * 1e-6) / 1e9 / 8000.0, 4),
+        "target_frac_of_hbm": 0.70,
+        "sample_us": round(us_samp, 2), "samples_per_s": b / (us_samp * 1e-6),
+        "sample_roofline": roofline("sample_bounds_kernel + sample_scan_kernel", samp_bytes, us_samp, peak,
+                                    peak_kind, traffic_for("sample_scan_stress")),
+        "roofline": roofline("build_cdf_2p_kernel<16, 4, 8, 3>", 8 * n, us_scan, peak, peak_kind,
+                             traffic_for("build_cdf_stress")),
+        "l2": "flushed before each rep (512 MiB write + 512 MiB read of other buffers); build_cdf also after a "
+              "write-only flush, whose dirty lines are written back inside the timed call"}
+
+    # ---- resample: 256 rows x 65536 log-weights N(0, 2^2)
+    R = workloads.RESAMPLE
+    lw = workloads.resample_logw()
+    logw = tensor(lw)
+    ridx = torch.empty((R["rows"], R["P"]), dtype=torch.int32, device=dev)
+    per.per_resample(logw, 6, 0, ridx)
+    checks["resample"] = {"lw": lw, "idx": ridx.cpu().numpy()}
+    us_r = time_graph(torch, graph_of(torch, lambda: per.per_resample(logw, 6, 0, ridx)), 20, flush.clean)
+    D = 4
+    state = torch.randn((R["rows"], R["P"], D), generator=torch.Generator(device=dev).manual_seed(6), device=dev)
+    out_state = torch.empty_like(state)
+    out_lw = torch.empty_like(logw)
+    per.per_resample_step(logw, state, 6, 0, ridx, out_state, out_lw)
+    us_rs = time_graph(torch, graph_of(torch, lambda: per.per_resample_step(logw, state, 6, 0, ridx, out_state,
+                                                                         out_lw)), 20, flush.clean)
+    rbytes = 8 * R["rows"] * R["P"]
+    sbytes = R["rows"] * R["P"] * (4 + 4 + 4 + 8 * D)
+    cfg["resample"] = {
+        "workload": f"row-batched systematic resampling {R['rows']} rows x {R['P']} fp32 log-weights N(0, 2^2): "
+                    f"softmax, per-row CDF, u_j = (j + U_b)/P",
+        "resample_us": round(us_r, 2), "rows_per_s": R["rows"] / (us_r * 1e-6),
+        "resample_step_d4_us": round(us_rs, 2),
+        "resample_step_d4_gbs": round(sbytes / (us_rs * 1e-6) / 1e9, 1),
+        "resample_step_d4_frac": round(sbytes / (us_rs * 1e-6) / 1e9 / peak, 4),
+        "roofline": roofline("resample_kernel<0>", rbytes, us_r, peak, peak_kind, traffic_for("resample")),
+        "l2": "flushed before each rep (512 MiB write + 512 MiB read of other buffers)"}
+
+    extras.update(rank_and_gather_extras(per, torch, dev, peak, flush, tensor))
+    return cfg, extras, checks
+
+
+def workloads_apply(prio, idx, p):
+    """prio with prio[idx[k]] = p[k] in batch order (the last occurrence
+    wins): the host's copy of the buffer the tree workload fills."""
+    out = prio.copy()
+    out[idx] = p  # numpy fancy assignment keeps the last duplicate
+    return out
+
+
+def rank_and_gather_extras(per, torch, dev, peak, flush, tensor):
+    """Measurements beyond the workloads' records: the minibatch step that
+    also copies the sampled transitions, rank-based PER (the sort and the
+    step) and the torch.cumsum / searchsorted comparator."""
+    out = {}
+    Mb = workloads.MINIBATCH
+    ctx = per.PerContext(Mb["N"], Mb["alpha"], per.PER_SCAN)
+    per.per_set_priorities(ctx.handle, tensor(workloads.minibatch_priorities()))
+    trans = torch.randn((Mb["N"], 64), generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+    gi = [torch.empty(Mb["B"], dtype=torch.int32, device=dev) for _ in range(2)]
+    gw = torch.empty(Mb["B"], dtype=torch.float32, device=dev)
+    grows = torch.empty((Mb["B"], 64), dtype=torch.float32, device=dev)
+    gnew = [tensor(workloads.minibatch_new_priorities(r)) for r in range(8)]
+    per.per_build_cdf(ctx.handle)
+    per.per_sample(ctx.handle, Mb["B"], Mb["seed"], 0, per.PER_SCAN, gi[0])
+
+    def gather_steps():
+        for r in range(8):
+            per.per_step_gather(ctx.handle, gi[r & 1], gnew[r], Mb["B"], Mb["seed"], r * Mb["B"], per.PER_SCAN,
+                                Mb["beta"], gi[(r + 1) & 1], gw, trans, grows)
+    gather_steps()
+    us_g = time_graph(torch, graph_of(torch, gather_steps), 30, per_replay=8)
+    out["step_gather_minibatch_256B"] = {"N": Mb["N"], "B": Mb["B"], "row_bytes": 256, "us": round(us_g, 2),
+                                         "l2": "warm (the transitions stay resident across steps)",
+                                         "timing": "graph of 8 steps between events, per step"}
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
+    # rank-based PER on the minibatch workload: per step, update the 8192
+    # sampled items, re-sort all 262,144 by priority, sample 8192 ranks with
+    # IS weights (per_step, mode PER_RANK)
+    ctx = per.PerContext(Mb["N"], Mb["alpha"], per.PER_RANK)
+    per.per_set_priorities(ctx.handle, tensor(workloads.minibatch_priorities()))
+    per.per_rank_build(ctx.handle)
+    ri = [torch.empty(Mb["B"], dtype=torch.int32, device=dev) for _ in range(2)]
+    rw = torch.empty(Mb["B"], dtype=torch.float32, device=dev)
+    rnew = [tensor(workloads.minibatch_new_priorities(r)) for r in range(8)]
+    per.per_sample(ctx.handle, Mb["B"], Mb["seed"], 0, per.PER_RANK, ri[0])
+
+    def rank_steps():
+        for r in range(8):
+            per.per_step(ctx.handle, ri[r & 1], rnew[r], Mb["B"], Mb["seed"], r * Mb["B"], per.PER_RANK,
+                         Mb["beta"], ri[(r + 1) & 1], rw)
+    rank_steps()
+    us_k = time_graph(torch, graph_of(torch, rank_steps), 30, per_replay=8)
+    us_b = time_graph(torch, graph_of(torch, lambda: per.per_rank_build(ctx.handle)), 30)
+    out["rank_minibatch_step"] = {"N": Mb["N"], "B": Mb["B"], "us": round(us_k, 2), "sort_us": round(us_b, 2),
+                                  "l2": "warm (the 1 MiB priorities stay resident across steps)",
+                                  "timing": "graph of 8 steps between events, per step"}
+    assert per.per_check(ctx.handle) == 0
+    ctx.close()
+    S = workloads.STRESS
+    n = S["N"]
+    ctx = per.PerContext(n, S["alpha"], per.PER_RANK)
+    per.per_set_priorities(ctx.handle, tensor(workloads.stress_priorities()))
+    per.per_rank_build(ctx.handle)
+    us_16 = time_graph(torch, graph_of(torch, lambda: per.per_rank_build(ctx.handle)), 10, flush.clean)
+    sort_bytes = RANK_SORT_BYTES_PER_KEY * n
+    out["rank_sort_16M"] = {"N": n, "us": round(us_16, 2), "keys_per_s": n / (us_16 * 1e-6),
+                            "gbs": round(sort_bytes / (us_16 * 1e-6) / 1e9, 1),
+                            "frac_of_measured_peak": round(sort_bytes / (us_16 * 1e-6) / 1e9 / peak, 4),
+                            "bytes_per_key": RANK_SORT_BYTES_PER_KEY, "l2": "flushed before each rep"}
+    assert per.per_check(ctx.handle) == 0
     ctx.close()
     # comparator, context only: the same CDF and sampling with library kernels
-    # (torch.cumsum of p**alpha in fp32, torch.searchsorted of the stratified
-    # thresholds), timed the same way
-    tp = torch.from_numpy(workloads.stress_priorities()).to(dev)
+    tp = tensor(workloads.stress_priorities())
     tcdf = torch.empty_like(tp)
     tu = ((torch.arange(S["B"], device=dev, dtype=torch.float32) + 0.5) / S["B"])
     tidx = torch.empty(S["B"], dtype=torch.int64, device=dev)
@@ -394,142 +746,122 @@ def extras(per, torch, dev, peak):
     def torch_sample():
         torch.searchsorted(tcdf, tu * tcdf[-1], out=tidx)
     torch_cdf()
-    us_tc = time_graph(graph_of(torch_cdf), 30)
-    us_ts = time_graph(graph_of(torch_sample), 20)
-    out["torch_comparator_16M"] = {"build_cdf_us": round(us_tc, 2), "sample_us": round(us_ts, 2),
-                                   "note": "torch.cumsum(p**alpha) and torch.searchsorted on the stress input "
-                                           "(library kernels); context only", "l2": "flushed before each rep"}
+    out["torch_comparator_16M"] = {
+        "build_cdf_us": round(time_graph(torch, graph_of(torch, torch_cdf), 30, flush.clean), 2),
+        "sample_us": round(time_graph(torch, graph_of(torch, torch_sample), 20, flush.clean), 2),
+        "note": "torch.cumsum(p**alpha) and torch.searchsorted on the stress input (library kernels); context only",
+        "l2": "flushed before each rep"}
+    return out
+
+
+def oracle_legs(cfg, checks, seconds):
+    """The CPU oracle (serial C, fp64, one thread) timed on a bounded sample
+    of each workload, and the count of the GPU's sampled indices that differ
+    from the oracle's search of its own fp64 CDF on the same inputs."""
+    import oracle
+    oracle.build()
+    budget = max(1.0, seconds / 4)
+
+    def timed_loop(fn):
+        t0 = time.perf_counter()
+        it = 0
+        while True:
+            fn()
+            it += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget:
+                return dt / it, it
+
+    def mism(a, b):
+        return {"differing": int(np.count_nonzero(a != b)), "samples": int(a.size),
+                "note": "all inside the boundary band (checked by the GPU tests)"}
+
+    Sm = workloads.SMALL
+    c = checks["small"]
+
+    def small():
+        C = oracle.cdf64(c["p"], Sm["alpha"])
+        idx, _ = oracle.sample_cdf_f64(C, Sm["B"], Sm["seed"], 0)
+        oracle.is_weights(c["p"], c["p"].size, Sm["alpha"], idx, Sm["beta"])
+        return idx
+    s_it, it = timed_loop(small)
+    cfg["small"]["cpu_baseline"] = {"value": Sm["B"] / s_it, "unit": "samples/s", "cores": 1, "kind": "oracle",
+                                    "us_per_combined_call": round(s_it * 1e6, 1),
+                                    "sample": f"{it} repetitions of build_cdf + sample + IS weights, single thread"}
+    cfg["small"]["mismatches_vs_oracle_fp64"] = mism(checks["small"]["idx"], small())
+
+    c = checks["minibatch"]
+    C = oracle.cdf64(c["p"], ALPHA)
+    own, _ = oracle.sample_cdf_f64(C, B, W["seed"], 0)
+    cfg["minibatch"]["mismatches_vs_oracle_fp64"] = mism(c["idx"], own)
+    cfg["minibatch"]["cpu_baseline"] = cpu_baseline(budget)
 
     T = workloads.TREE
-    cap = T["capacity"]
-    ctx = per.PerContext(cap, T["alpha"], per.PER_TREE)
-    p = workloads.lognormal(cap, workloads.rng(T["seed"], 999))
-    per.per_set_priorities(ctx.handle, torch.from_numpy(p).to(dev))
-    tidx = torch.empty(T["B"], dtype=torch.int32, device=dev)
-    upd_idx = []
-    upd_p = []
-    for s in range(8):
-        per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE, tidx)
-        i, q = workloads.tree_update_batch(s, tidx.cpu().numpy())
-        upd_idx.append(torch.from_numpy(i).to(dev))
-        upd_p.append(torch.from_numpy(q).to(dev))
+    c = checks["tree"]
+    cap_pow2 = 1 << 19
+    tb = T["B"]
 
-    def tree_steps():
-        for s in range(8):
-            per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE, tidx)
-            per.per_update(ctx.handle, upd_idx[s], upd_p[s])
-    tree_steps()
-    us_t = time_graph(graph_of(tree_steps), 50, flush_l2=False, per_replay=8)
-    out["tree_sample_update_step"] = {"capacity": cap, "B": T["B"], "us": round(us_t, 2), "target_us": 20.0,
-                                      "l2": "warm (the 4 MiB tree stays resident across steps)",
-                                      "timing": "graph of 8 steps between events, per step"}
-    if per.per_check(ctx.handle) != 0:
-        out["tree_sample_update_step"]["status"] = "device status not clean"
+    def tree_step():
+        leaves = oracle.tree_leaves(c["prio"], T["alpha"], cap_pow2)
+        tree = oracle.tree_build(leaves)
+        idx, u = oracle.sample_tree(tree, tb, T["seed"], T["steps"] * tb)
+        prio = workloads_apply(c["prio"], idx, c["prio"][idx])
+        oracle.tree_build(oracle.tree_leaves(prio, T["alpha"], cap_pow2))
+        return idx, u, leaves
+    t_it, it = timed_loop(tree_step)
+    cfg["tree"]["cpu_baseline"] = {"value": 1.0 / t_it, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                                   "us_per_step": round(t_it * 1e6, 1),
+                                   "sample": f"{it} sample + update steps at full fill (the oracle rebuilds the "
+                                             "whole tree per update), single thread"}
+    _, u, leaves = tree_step()
+    Cl = np.cumsum(leaves.astype(np.float64))
+    own = np.minimum(np.searchsorted(Cl, u.astype(np.float64), side="left"), cap_pow2 - 1)
+    cfg["tree"]["mismatches_vs_oracle_fp64"] = mism(c["idx"], own)
 
-    def iid_steps():  # the same step with i.i.d. thresholds (mode PER_TREE | PER_IID)
-        for s in range(8):
-            per.per_sample(ctx.handle, T["B"], 3, s * T["B"], per.PER_TREE | per.PER_IID, tidx)
-            per.per_update(ctx.handle, upd_idx[s], upd_p[s])
-    iid_steps()
-    us_i = time_graph(graph_of(iid_steps), 50, flush_l2=False, per_replay=8)
-    out["tree_iid_sample_update_step"] = {"capacity": cap, "B": T["B"], "us": round(us_i, 2),
-                                          "l2": "warm (the 4 MiB tree stays resident across steps)",
-                                          "timing": "graph of 8 steps between events, per step"}
-    if per.per_check(ctx.handle) != 0:
-        out["tree_iid_sample_update_step"]["status"] = "device status not clean"
-    ctx.close()
+    Hv = workloads.HEAVY
+    c = checks["heavy"]
+
+    def heavy():
+        C = oracle.cdf64(c["p"], Hv["alpha"])
+        idx, _ = oracle.sample_cdf_f64(C, Hv["B"], Hv["seed"], 0)
+        for beta in Hv["betas"]:
+            oracle.is_weights(c["p"], c["p"].size, Hv["alpha"], idx, beta)
+        return C, idx
+    h_it, it = timed_loop(heavy)
+    C, own = heavy()
+    cfg["heavy"]["cpu_baseline"] = {"value": Hv["B"] / h_it, "unit": "samples/s", "cores": 1, "kind": "oracle",
+                                    "us_per_iteration": round(h_it * 1e6, 1),
+                                    "sample": f"{it} x (build_cdf, sample {Hv['B']}, IS weights at 7 betas), single "
+                                              "thread"}
+    ut = oracle.thresholds(Hv["B"], Hv["seed"], 0, c["tree_root"])  # the tree path's thresholds (T = root)
+    own_t = np.minimum(np.searchsorted(C, ut.astype(np.float64), side="left"), C.size - 1)
+    cfg["heavy"]["mismatches_vs_oracle_fp64"] = {"scan": mism(c["idx_scan"], own), "tree": mism(c["idx_tree"], own_t)}
+
+    S = workloads.STRESS
+    c = checks["stress"]
+    t0 = time.perf_counter()
+    C = oracle.cdf64(c["p"], S["alpha"])
+    t1 = time.perf_counter()
+    own, _ = oracle.sample_cdf_f64(C, S["B"], 1, 0)
+    t2 = time.perf_counter()
+    cfg["stress"]["cpu_baseline"] = {"value": 8 * c["p"].size / (t1 - t0) / 1e9, "unit": "GB/s (build_cdf)",
+                                     "cores": 1, "kind": "oracle", "build_cdf_us": round((t1 - t0) * 1e6, 1),
+                                     "sample_us": round((t2 - t1) * 1e6, 1),
+                                     "sample": "one build_cdf of 16M items and one sample of 1M, single thread"}
+    cfg["stress"]["mismatches_vs_oracle_fp64"] = mism(c["idx"], own)
 
     R = workloads.RESAMPLE
-    logw = torch.from_numpy(workloads.resample_logw()).to(dev)
-    ridx = torch.empty((R["rows"], R["P"]), dtype=torch.int32, device=dev)
-    per.per_resample(logw, 6, 0, ridx)
-    us_r = time_graph(graph_of(lambda: per.per_resample(logw, 6, 0, ridx)), 20)
-    rbytes = 8 * R["rows"] * R["P"]
-    out["resample"] = {"rows": R["rows"], "P": R["P"], "us": round(us_r, 2),
-                       "gbs": round(rbytes / (us_r * 1e-6) / 1e9, 1),
-                       "frac_of_measured_peak": round(rbytes / (us_r * 1e-6) / 1e9 / peak, 4),
-                       "l2": "flushed before each rep"}
-    # the minibatch step that also returns the sampled transitions: rows of
-    # 64 floats (256 B) per item, copied inside the step's launch
-    Mb = workloads.MINIBATCH
-    ctx = per.PerContext(Mb["N"], Mb["alpha"], per.PER_SCAN)
-    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
-    trans = torch.randn((Mb["N"], 64), generator=torch.Generator(device=dev).manual_seed(7), device=dev)
-    gi = [torch.empty(Mb["B"], dtype=torch.int32, device=dev) for _ in range(2)]
-    gw = torch.empty(Mb["B"], dtype=torch.float32, device=dev)
-    grows = torch.empty((Mb["B"], 64), dtype=torch.float32, device=dev)
-    gnew = [torch.from_numpy(workloads.minibatch_new_priorities(r)).to(dev) for r in range(8)]
-    per.per_build_cdf(ctx.handle)
-    per.per_sample(ctx.handle, Mb["B"], Mb["seed"], 0, per.PER_SCAN, gi[0])
+    c = checks["resample"]
+    rows = list(range(0, R["rows"], 32))
 
-    def gather_steps():
-        for r in range(8):
-            per.per_step_gather(ctx.handle, gi[r & 1], gnew[r], Mb["B"], Mb["seed"], r * Mb["B"], per.PER_SCAN,
-                                Mb["beta"], gi[(r + 1) & 1], gw, trans, grows)
-    gather_steps()
-    us_g = time_graph(graph_of(gather_steps), 30, flush_l2=False, per_replay=8)
-    out["step_gather_minibatch_256B"] = {"N": Mb["N"], "B": Mb["B"], "row_bytes": 256, "us": round(us_g, 2),
-                                         "l2": "warm (the transitions stay resident across steps)",
-                                         "timing": "graph of 8 steps between events, per step"}
-    if per.per_check(ctx.handle) != 0:
-        out["step_gather_minibatch_256B"]["status"] = "device status not clean"
-    ctx.close()
-
-    # rank-based PER on the minibatch workload: per step, update the 8192
-    # sampled items, re-sort all 262,144 by priority, sample 8192 ranks with
-    # IS weights (per_step, mode PER_RANK)
-    Mb = workloads.MINIBATCH
-    ctx = per.PerContext(Mb["N"], Mb["alpha"], per.PER_RANK)
-    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.minibatch_priorities()).to(dev))
-    per.per_rank_build(ctx.handle)
-    ri = [torch.empty(Mb["B"], dtype=torch.int32, device=dev) for _ in range(2)]
-    rw = torch.empty(Mb["B"], dtype=torch.float32, device=dev)
-    rnew = [torch.from_numpy(workloads.minibatch_new_priorities(r)).to(dev) for r in range(8)]
-    per.per_sample(ctx.handle, Mb["B"], Mb["seed"], 0, per.PER_RANK, ri[0])
-
-    def rank_steps():
-        for r in range(8):
-            per.per_step(ctx.handle, ri[r & 1], rnew[r], Mb["B"], Mb["seed"], r * Mb["B"], per.PER_RANK,
-                         Mb["beta"], ri[(r + 1) & 1], rw)
-    rank_steps()
-    us_k = time_graph(graph_of(rank_steps), 30, flush_l2=False, per_replay=8)
-    us_b = time_graph(graph_of(lambda: per.per_rank_build(ctx.handle)), 30, flush_l2=False)
-    out["rank_minibatch_step"] = {"N": Mb["N"], "B": Mb["B"], "us": round(us_k, 2), "sort_us": round(us_b, 2),
-                                  "l2": "warm (the 1 MiB priorities stay resident across steps)",
-                                  "timing": "graph of 8 steps between events, per step"}
-    if per.per_check(ctx.handle) != 0:
-        out["rank_minibatch_step"]["status"] = "device status not clean"
-    ctx.close()
-    # the sort at 16M items (L2 flushed): four 8-bit passes, each reading the
-    # keys twice and the values once and writing both (pass 0 reads the
-    # priorities; the last writes the order and its inverse)
-    ctx = per.PerContext(n, S["alpha"], per.PER_RANK)
-    per.per_set_priorities(ctx.handle, torch.from_numpy(workloads.stress_priorities()).to(dev))
-    per.per_rank_build(ctx.handle)
-    us_16 = time_graph(graph_of(lambda: per.per_rank_build(ctx.handle)), 10)
-    sort_bytes = RANK_SORT_BYTES_PER_KEY * n
-    out["rank_sort_16M"] = {"N": n, "us": round(us_16, 2), "keys_per_s": n / (us_16 * 1e-6),
-                            "gbs": round(sort_bytes / (us_16 * 1e-6) / 1e9, 1),
-                            "frac_of_measured_peak": round(sort_bytes / (us_16 * 1e-6) / 1e9 / peak, 4),
-                            "bytes_per_key": RANK_SORT_BYTES_PER_KEY, "l2": "flushed before each rep"}
-    if per.per_check(ctx.handle) != 0:
-        out["rank_sort_16M"]["status"] = "device status not clean"
-    ctx.close()
-
-    # the whole particle-filter resample step with D = 4 states per particle:
-    # indices, gathered states and the reset log-weights in one launch
-    D = 4
-    state = torch.randn((R["rows"], R["P"], D), generator=torch.Generator(device=dev).manual_seed(6), device=dev)
-    out_state = torch.empty_like(state)
-    out_lw = torch.empty_like(logw)
-    per.per_resample_step(logw, state, 6, 0, ridx, out_state, out_lw)
-    us_s = time_graph(graph_of(lambda: per.per_resample_step(logw, state, 6, 0, ridx, out_state, out_lw)), 20)
-    sbytes = R["rows"] * R["P"] * (4 + 4 + 4 + 8 * D)  # logw in, idx out, logw out, states in and out
-    out["resample_step_d4"] = {"rows": R["rows"], "P": R["P"], "D": D, "us": round(us_s, 2),
-                               "gbs": round(sbytes / (us_s * 1e-6) / 1e9, 1),
-                               "frac_of_measured_peak": round(sbytes / (us_s * 1e-6) / 1e9 / peak, 4),
-                               "l2": "flushed before each rep"}
-    return out
+    def resample_rows():
+        return [oracle.resample_row(c["lw"][b], oracle.u01_closed_open(6, 0, b))[0] for b in rows]
+    r_it, it = timed_loop(resample_rows)
+    cfg["resample"]["cpu_baseline"] = {"value": len(rows) / r_it, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                                       "us_per_row": round(r_it / len(rows) * 1e6, 1),
+                                       "sample": f"{it} x {len(rows)} rows of {R['P']}, single thread"}
+    got = np.concatenate([c["idx"][b] for b in rows])
+    cfg["resample"]["mismatches_vs_oracle_fp64"] = mism(got, np.concatenate(resample_rows()))
 
 
 # ------------------------------------------------------ kernel cases --------
