@@ -627,7 +627,7 @@ def measure_configs(per, torch, dev, peak, peak_kind, flush, head):
         "sample_us": round(us_samp, 2), "samples_per_s": b / (us_samp * 1e-6),
         "sample_roofline": roofline("sample_bounds_kernel + sample_scan_kernel", samp_bytes, us_samp, peak,
                                     peak_kind, traffic_for("sample_scan_stress")),
-        "roofline": roofline("build_cdf_2p_kernel<16, 4, 8, 3>", 8 * n, us_scan, peak, peak_kind,
+        "roofline": roofline("build_cdf_stream_kernel", 8 * n, us_scan, peak, peak_kind,
                              traffic_for("build_cdf_stress")),
         "l2": "flushed before each rep (512 MiB write + 512 MiB read of other buffers); build_cdf also after a "
               "write-only flush, whose dirty lines are written back inside the timed call"}

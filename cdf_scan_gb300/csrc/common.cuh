@@ -23,6 +23,20 @@ __device__ __forceinline__ void st_relaxed_v2(unsigned long long* p, unsigned lo
     asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
 
+// 32-byte relaxed accesses (sm_100+): each 64-bit word is single-copy atomic
+// on its own, the four together are not (readers check a tag in every word).
+__device__ __forceinline__ void ld_relaxed_v4(const unsigned long long* p, unsigned long long& a,
+                                              unsigned long long& b, unsigned long long& c, unsigned long long& d) {
+    asm volatile("ld.relaxed.gpu.global.v4.u64 {%0, %1, %2, %3}, [%4];"
+                 : "=l"(a), "=l"(b), "=l"(c), "=l"(d)
+                 : "l"(p)
+                 : "memory");
+}
+__device__ __forceinline__ void st_relaxed_v4(unsigned long long* p, unsigned long long a, unsigned long long b,
+                                              unsigned long long c, unsigned long long d) {
+    asm volatile("st.relaxed.gpu.global.v4.u64 [%0], {%1, %2, %3, %4};" ::"l"(p), "l"(a), "l"(b), "l"(c), "l"(d)
+                 : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

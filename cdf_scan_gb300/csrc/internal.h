@@ -58,7 +58,8 @@ struct per_ctx {
     int slot_n;
     unsigned* step_min;               // [3] per_step: call counter, then the batch minimum of p^alpha
                                       // (float bits) of even and odd calls
-    unsigned long long* scan_xsum;    // [kScanXsumWords] chunk sums of the two-pass scan
+    unsigned long long* scan_rec;     // [scan_rec_tiles * kRecStride] tile records of the streaming scan
+    int64_t scan_rec_tiles;
     int64_t drop_tile;                // per_debug_drop_tile: the tile or CTA whose message the next scan withholds (-1)
 
     // rank-based PER (PER_RANK): the radix sort's buffers, the order it
@@ -79,15 +80,20 @@ struct per_ctx {
 };
 
 // Grid-barrier ticket words (per_ctx::tickets).
-enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_SCAN = 3, TK_STEP = 4, TK_RANK = 5, NUM_TICKETS = 8 };
+enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_STEP = 4, TK_RANK = 5, NUM_TICKETS = 8 };
 
 // Items per entry of the coarse CDF index: coarse[j] = cdf[min(64j+63, n-1)].
 constexpr int kCoarseStride = 64;
 
-// Exchange words of the two-pass scan: 2 parities x kScanMaxGrid CTAs x one
-// 128-bit exact sum, 2 parities x a 128-bit total, a ready word, padding.
+// Streaming scan (inputs larger than one wave): at most kScanMaxGrid CTAs,
+// 8192-item tiles, and per tile one record of kRecWords 64-bit words (an
+// exact 128-bit sum as four tagged 32-bit pieces) alone in a 128-byte line
+// (kRecStride words), for up to scan_rec_tiles(n) tiles.
 constexpr int kScanMaxGrid = 1024;
-constexpr int64_t kScanXsumWords = 4 * kScanMaxGrid + 8;
+constexpr int kStreamTile = 8192;
+constexpr int kRecWords = 4;
+constexpr int kRecStride = 16;
+inline int64_t scan_rec_tiles(int64_t n) { return (n + kStreamTile - 1) / kStreamTile + 1; }
 
 // 64-bit words of scan state for up to `tiles` tiles: one tagged aggregate
 // word per tile, each alone in a 128-byte line (kDescStride words apart) so

@@ -41,7 +41,7 @@ void free_ctx(per_ctx* c) {
     cudaFree(c->sample_bounds);
     cudaFree(c->tickets);
     cudaFree(c->slots);
-    cudaFree(c->scan_xsum);
+    cudaFree(c->scan_rec);
     cudaFree(c->step_min);
     cudaFree(c->rank_keys0);
     cudaFree(c->rank_keys1);
@@ -103,6 +103,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
     c->flags = flags;
     c->scan_desc_tiles = std::min<int64_t>((c->alloc_n + 1023) / 1024, kMaxWaveTiles);
     c->drop_tile = -1;
+    c->scan_rec_tiles = scan_rec_tiles(c->alloc_n);
     c->coarse_n = c->alloc_n / kCoarseStride + 1;
     // the sampler's CTAs: at most max(B / 1024, n / 4096) + 1 of them
     c->sample_bounds_n = std::max<int64_t>(int64_t(1) << 14, c->alloc_n / 4096) + 2;
@@ -118,7 +119,7 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
              alloc_zero(&c->coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
              alloc_zero(&c->sample_bounds, 2 * static_cast<size_t>(c->sample_bounds_n), s) == cudaSuccess &&
              alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
-             alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess &&
+             alloc_zero(&c->scan_rec, static_cast<size_t>(c->scan_rec_tiles * kRecStride), s) == cudaSuccess &&
              alloc_zero(&c->step_min, 3, s) == cudaSuccess;
     if (ok && (flags & PER_TREE)) ok = alloc_zero(&c->tree, 2 * static_cast<size_t>(c->cap_pow2) + 16, s) == cudaSuccess;
     if (ok && (flags & PER_RANK)) {
@@ -132,8 +133,8 @@ per_status per_create(per_ctx** out, int64_t capacity, float alpha, uint32_t fla
              alloc_zero(&c->rank_cdf, c->alloc_n, s) == cudaSuccess &&
              alloc_zero(&c->rank_coarse, static_cast<size_t>(c->coarse_n), s) == cudaSuccess &&
              (c->sample_bounds || alloc_zero(&c->sample_bounds, 2 * static_cast<size_t>(c->sample_bounds_n), s) == cudaSuccess) &&
-             alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess &&
-             alloc_zero(&c->scan_xsum, static_cast<size_t>(kScanXsumWords), s) == cudaSuccess;
+             (c->scan_desc || alloc_zero(&c->scan_desc, static_cast<size_t>(scan_state_words(c->scan_desc_tiles)), s) == cudaSuccess) &&
+             (c->scan_rec || alloc_zero(&c->scan_rec, static_cast<size_t>(c->scan_rec_tiles * kRecStride), s) == cudaSuccess);
     }
     if (ok) {
         // epochs start at 1 (0 marks "never written"); the IS-weight minimum

@@ -9,10 +9,12 @@
 //  * Inputs that fit one wave of co-resident CTAs: build_cdf_wave_kernel,
 //    one tile per CTA scanned in registers, carries by an exact lookback
 //    over tagged tile-sum words (scan_core.cuh).
-//  * Larger inputs: build_cdf_2p_kernel, two passes per L2-sized segment --
-//    slice sums from HBM, one exact exchange of chunk sums per segment, then
-//    slice scans re-read from L2 -- with a producer warp streaming tiles
-//    through a ring of 1-D bulk copies (TMA) on mbarriers.
+//  * Larger inputs: build_cdf_stream_kernel, one pass over the input by
+//    persistent CTAs -- a producer warp streams tiles through a ring of 1-D
+//    bulk copies (TMA) on mbarriers, compute warps scan them locally and park
+//    the result in tensor memory, and each tile is written out a few tiles
+//    later, once its exact carry has been collected from the tagged records
+//    of the tiles before it (a decoupled lookback).
 //
 // Carries are 128-bit fixed-point integers (60 fractional bits), so they do
 // not depend on the order in which partial sums arrive; each unit (tile or
@@ -38,38 +40,40 @@ __device__ __forceinline__ void load_tile(const ScanParams& P, unsigned t, float
     if (bytes) bulk_copy_g2s(buf, P.p + base, bytes, bar);
 }
 
-// ---- two passes per segment: reduce, exchange, scan from L2 ----------------
+// ---- the streaming scan: one pass by persistent CTAs ------------------------
 //
-// For inputs larger than one wave.  The tiles are cut into segments of at most
-// kSegMaxTiles tiles (64 MiB of fp32 at 4096-item tiles), small enough that a
-// segment read from HBM is still in L2 when it is read a second time.  Inside
-// segment s, CTA c owns a contiguous chunk of the segment's tiles and makes
-// two passes over it.  A tile is WARPS slices of 32 x ITEMS items, one per
-// compute warp, and the slice is the unit of the exact carries:
-//   pass 1: p^alpha and a fixed-order sum per slice (fp32);
-//   exchange: the chunk's exact sum (128-bit fixed point) goes to a slot; after
-//     a grid barrier every CTA adds the slots up (its exclusive prefix and the
-//     segment total) and turns E = prefix + the chunk's earlier slice sums
-//     into the carries (hi, lo, fl32(E), fl32(E')) of its slices, E' being
-//     the next slice's E;
-//   pass 2: re-reads the chunk (from L2), scans each slice with the monotone
-//     per-warp scan of the kernels above, and writes
-//     clamp(hi + (lo + local), fl32(E), fl32(E')) from registers.
-// The clamp bounds come from the exact pass-1 sums, so the CDF is
-// non-decreasing across slices, tiles and chunks, and no carry depends on
-// timing: the result is bit-reproducible.  Compute warps never wait for each
-// other inside a pass; a producer warp refills each stage of the ring of
-// bulk copies once all compute warps have released it (mbarriers), and the
-// one cross-CTA dependency is the grid barrier per segment.
-
-constexpr int64_t kSegMaxTiles = 4096;  // tiles per segment (64 MiB at 4096 items)
-constexpr int kChunkMax = 32;           // tiles per CTA per segment (one lane per tile)
-
-// Barrier among the compute warps only (the producer warp never joins it).
-template <int N>
-__device__ __forceinline__ void compute_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
-}
+// For inputs larger than one wave of tiles.  One CTA per SM (co-resident,
+// cooperative launch) takes 8192-item tiles (kStreamTile: sixteen 512-item
+// slices, one per compute warp) in ticket order from a global counter, so an
+// SM that gets less memory bandwidth simply takes fewer tiles.  The slice is
+// the unit of the exact carries.  Four roles per CTA, all on the CTA's own
+// sequence of tiles k = 0, 1, ...:
+//   producer warp: draws tile t_k = ticket++ and streams it into stage
+//     k mod STAGES of a ring of 1-D bulk copies (TMA) on mbarriers; once the
+//     tickets run out it records how many tiles the CTA got;
+//   16 compute warps, one slice each: the local phase of tile k -- the
+//     slice's p^alpha (the stage goes back to the producer as soon as it has
+//     been read), its fp32 sum (a fixed order), then its local inclusive
+//     scan, which waits in tensor memory (TMEM, 256 KB per SM, otherwise
+//     unused here: room for NX tiles) -- and then the emit phase of tile
+//     k - LAG, whose exclusive prefix has been found meanwhile: the local
+//     scan back from TMEM, written out once with the slice's carry
+//     (hi, lo, fl32(E), fl32(E')) added;
+//   publisher warp: the exact 128-bit fixed-point sums of the tile's slices,
+//     their exclusive prefixes within the tile, and the tile's total in its
+//     record, tagged "aggregate";
+//   four lookback warps, taking the CTA's tiles in turn: the tile's exclusive
+//     prefix E from the records of the tiles before it -- the nearest one
+//     tagged "inclusive" plus the aggregates after it (a decoupled
+//     lookback) -- then E + the tile's total into its record, tagged
+//     "inclusive", and the sixteen slice carries.
+// A record is four 64-bit words, 32 payload bits each under a 32-bit tag
+// (call epoch << 1 | inclusive), one 32-byte store, alone in a 128-byte line;
+// a reader takes it only when all four tags agree.  All sums are exact
+// integers, so E does not depend on where a lookback stopped: the CDF is
+// bit-reproducible, and the arithmetic of a slice -- its sum, local scan,
+// carry and clamped write -- is the same whichever CTA handles it, and the
+// same as in the one-pass-per-slice formulation: sum, scan, add the carry.
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -104,37 +108,69 @@ __device__ __forceinline__ void run_values(const ScanParams& P, const float* buf
     }
 }
 
-// Inclusive scan of one run (8 consecutive items per lane, lanes in order)
-// continuing from `carry`, the last value of the slice so far: thread-serial
-// over the lane's items, shuffles across the lanes, and an exact max-scan
-// that removes the dips fp32 reassociation can leave between lanes.  On
-// return `carry` is the run's last value.
-__device__ __forceinline__ void scan_run(float (&v)[8], float& carry, int lane) {
-    float r[8];
-    r[0] = v[0];
+// Local inclusive scan of a slice's two runs a and b (8 consecutive items
+// per lane, lanes in order; b continues from a's last value, a from 0).  Per
+// run: the lane-serial sums of its 8 items, a shuffle scan of the lane
+// totals, the run's base (carry + the lanes before) added to each item, and
+// an exact max-scan that removes the dips fp32 reassociation can leave
+// between lanes; the run's last value is the carry into the next.  The
+// lane-serial sums and the shuffle scans of the two runs interleave, and a
+// run whose values already ascend across the lanes (no NaN, every lane's
+// first value at or above the previous lane's last one, or the carry for
+// lane 0) skips the max-scan, which would leave it unchanged.
+__device__ __forceinline__ void scan_pair(float (&a)[8], float (&b)[8], int lane) {
+    float ra[8], rb[8];
+    ra[0] = a[0];
+    rb[0] = b[0];
 #pragma unroll
-    for (int e = 1; e < 8; ++e) r[e] = r[e - 1] + v[e];
-    float x = r[7];
+    for (int e = 1; e < 8; ++e) {
+        ra[e] = ra[e - 1] + a[e];
+        rb[e] = rb[e - 1] + b[e];
+    }
+    float xa = ra[7], xb = rb[7];
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_up_sync(PER_FULL_MASK, x, d);
-        if (lane >= d) x += y;
+        const float ya = __shfl_up_sync(PER_FULL_MASK, xa, d);
+        const float yb = __shfl_up_sync(PER_FULL_MASK, xb, d);
+        if (lane >= d) {
+            xa += ya;
+            xb += yb;
+        }
     }
-    float ex = __shfl_up_sync(PER_FULL_MASK, x, 1);
-    if (lane == 0) ex = 0.f;
-    const float base = carry + ex;
-    add_each<8>(base, r);
-    float mx = r[7];
+    float exa = __shfl_up_sync(PER_FULL_MASK, xa, 1);
+    float exb = __shfl_up_sync(PER_FULL_MASK, xb, 1);
+    if (lane == 0) exa = exb = 0.f;
+    float carry = 0.f;
+    // run a, then run b from a's last value
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_up_sync(PER_FULL_MASK, mx, d);
-        if (lane >= d) mx = fmaxf(mx, y);
+    for (int h = 0; h < 2; ++h) {
+        float(&r)[8] = h == 0 ? ra : rb;
+        float(&v)[8] = h == 0 ? a : b;
+        const float base = carry + (h == 0 ? exa : exb);
+        add_each<8>(base, r);
+        float prev = __shfl_up_sync(PER_FULL_MASK, r[7], 1);
+        if (lane == 0) prev = carry;
+        bool ordered = prev <= r[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) ordered = ordered && r[e - 1] <= r[e];
+        if (__all_sync(PER_FULL_MASK, ordered)) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = r[e];
+            carry = __shfl_sync(PER_FULL_MASK, r[7], 31);
+        } else {
+            float mx = r[7];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const float y = __shfl_up_sync(PER_FULL_MASK, mx, d);
+                if (lane >= d) mx = fmaxf(mx, y);
+            }
+            float pm = __shfl_up_sync(PER_FULL_MASK, mx, 1);
+            if (lane == 0) pm = carry;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = fmaxf(r[e], pm);
+            carry = __shfl_sync(PER_FULL_MASK, mx, 31);
+        }
     }
-    float pm = __shfl_up_sync(PER_FULL_MASK, mx, 1);
-    if (lane == 0) pm = carry;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = fmaxf(r[e], pm);
-    carry = __shfl_sync(PER_FULL_MASK, mx, 31);
 }
 
 // p^alpha of this lane's items of its warp's slice of a full tile (runs of 8
@@ -161,21 +197,18 @@ __device__ __forceinline__ void slice_values(const ScanParams& P, const float* b
 }
 
 // Writes one run of a slice: hi + (lo + local) with the slice's carry
-// cy = (hi, lo, fl32(E), fl32(E')), clamped to [fl32(E), fl32(E')] when the
-// run's first or last value falls outside (the values are monotone along the
-// run), and its coarse-index entries; item n-1 gets fl32(E') itself, the
-// correctly rounded exact total.  FAST: full tile, 32-byte aligned cdf.
+// cy = (hi, lo, fl32(E), fl32(E')), clamped to [fl32(E), fl32(E')], and its
+// coarse-index entries; item n-1 gets fl32(E') itself, the correctly rounded
+// exact total.  (The values are monotone along the run, so the clamp changes
+// only a run whose first or last value falls outside.)  FAST: full tile,
+// 32-byte aligned cdf.
 template <bool FAST, int TILE>
 __device__ __forceinline__ void emit_run(const ScanParams& P, float (&v)[8], float4 cy, int64_t tile_base, int i0,
                                          int valid, int lane) {
     add_each<8>(cy.y, v);
     add_each<8>(cy.x, v);
-    const float first = __shfl_sync(PER_FULL_MASK, v[0], 0);
-    const float last = __shfl_sync(PER_FULL_MASK, v[7], 31);
-    if (!(first >= cy.z && last <= cy.w)) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = fminf(fmaxf(v[e], cy.z), cy.w);
-    }
+    for (int e = 0; e < 8; ++e) v[e] = fminf(fmaxf(v[e], cy.z), cy.w);
     if (tile_base + i0 <= P.n - 1 && P.n - 1 < tile_base + i0 + 8) {  // the last value is fl32(E_total) exactly
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -222,368 +255,443 @@ __device__ __forceinline__ u128 warp_scan_u128(u128 v, int lane) {
     return v;
 }
 
-// The chunks of a CTA of the two-pass kernel and the sequence of bulk copies
-// it consumes: for each segment its chunk's tiles twice (pass 1, then pass 2).
-struct TwoPassLoads {
-    int64_t T, S, nseg;
-    int G, c;
-    int64_t s = 0, j = 0, lo = 0, len = 0;
-    int pass = 0;
-    bool done = false;
 
-    __device__ int64_t seg_count(int64_t sg) const { return T - sg * S < S ? T - sg * S : S; }
-    __device__ int64_t chunk_lo(int64_t sg) const { return sg * S + c * seg_count(sg) / G; }
-    __device__ int64_t chunk_len(int64_t sg) const { return sg * S + (c + 1) * seg_count(sg) / G - chunk_lo(sg); }
-    __device__ void start() {
-        lo = chunk_lo(0);
-        len = chunk_len(0);
-    }
-    // the tile of the next copy; false once the sequence is exhausted
-    __device__ bool next(int64_t& tile) {
-        while (!done && j >= len) {
-            j = 0;
-            if (pass == 0) {
-                pass = 1;
-            } else {
-                pass = 0;
-                if (++s >= nseg) {
-                    done = true;
-                } else {
-                    lo = chunk_lo(s);
-                    len = chunk_len(s);
+// Ring stages, the lag (tiles) between a tile's local phase and its emit
+// phase, and the ring of per-tile exchange state and TMEM slots (more than
+// LAG) of the streaming kernel.  The lag covers the latency of a lookback
+// (the records of the tiles before it appear over a few microseconds), four
+// lookback warps its throughput.
+constexpr int kStreamStages = 4;
+constexpr int kStreamLag = 6;
+constexpr int kStreamXring = 8;
+constexpr int kStreamWarps = kStreamTile / 512;  // compute warps, one slice each
+constexpr int kStreamLookback = 4;               // lookback warps
+constexpr int kStreamThreads = (kStreamWarps + 2 + kStreamLookback) * 32;
+// Records per lane per poll of a lookback: a window of 160 tiles, which
+// reaches the CTA's previous tile (about one tile per CTA back).
+constexpr int kLookbackQ = 5;
+
+// Record tags of the current call: "aggregate" (the tile's own sum) and
+// "inclusive" (the exact prefix through the tile).
+__device__ __forceinline__ unsigned tag_aggregate(unsigned epoch) { return epoch << 1; }
+__device__ __forceinline__ unsigned tag_inclusive(unsigned epoch) { return (epoch << 1) | 1u; }
+
+__device__ __forceinline__ void publish_record(const ScanParams& P, int64_t t, unsigned tag, u128 v) {
+    const unsigned long long tg = static_cast<unsigned long long>(tag) << 32;
+    const uint64_t lo = static_cast<uint64_t>(v), hi = static_cast<uint64_t>(v >> 64);
+    st_relaxed_v4(P.rec + t * kRecStride, tg | (lo & 0xffffffffull), tg | (lo >> 32), tg | (hi & 0xffffffffull),
+                  tg | (hi >> 32));
+}
+
+// Exclusive prefix of tile t (t >= 1) by decoupled lookback, one warp.  Lane
+// l reads the records of tiles hi - 1 - l - 32q (q < kLookbackQ) of a
+// window below hi.  The window is resolved once every record above its
+// highest "inclusive" one is present: the answer is that inclusive value
+// plus the aggregates above it.  A window without an inclusive record but
+// complete adds all of its aggregates and moves down.  Polls until then,
+// at most kWaitLimitNs (ST_TIMEOUT, *abort set).
+__device__ __forceinline__ u128 lookback(const ScanParams& P, int64_t t, unsigned epoch, int lane,
+                                         volatile int* abort) {
+    const unsigned tg_a = tag_aggregate(epoch), tg_i = tag_inclusive(epoch);
+    u128 acc = 0;
+    int64_t hi = t;
+    uint64_t t0 = 0;
+    while (hi > 0 && !__any_sync(PER_FULL_MASK, *abort != 0)) {
+        const int64_t lo = hi > 32 * kLookbackQ ? hi - 32 * kLookbackQ : 0;
+        for (;;) {
+            unsigned long long w[kLookbackQ][kRecWords];
+#pragma unroll
+            for (int q = 0; q < kLookbackQ; ++q) {
+                const int64_t i = hi - 1 - lane - 32 * q;
+                if (i >= lo) ld_relaxed_v4(P.rec + i * kRecStride, w[q][0], w[q][1], w[q][2], w[q][3]);
+            }
+            // per record: 0 missing, 1 aggregate, 2 inclusive; the lane's
+            // highest inclusive record (its smallest q)
+            int64_t best = -1;
+            unsigned present = 0, incl = 0;
+#pragma unroll
+            for (int q = 0; q < kLookbackQ; ++q) {
+                const int64_t i = hi - 1 - lane - 32 * q;
+                if (i < lo) continue;
+                const unsigned g = static_cast<unsigned>(w[q][0] >> 32);
+                bool same = true;
+#pragma unroll
+                for (int k = 1; k < kRecWords; ++k) same = same && static_cast<unsigned>(w[q][k] >> 32) == g;
+                if (same && (g == tg_a || g == tg_i)) {
+                    present |= 1u << q;
+                    if (g == tg_i) {
+                        incl |= 1u << q;
+                        if (best < 0) best = i;
+                    }
                 }
             }
-        }
-        if (done) return false;
-        tile = lo + j++;
-        return true;
-    }
-};
-
-// Layout of the two-pass kernel's exchange words (ScanParams::xsum):
-// slots[2][kScanMaxGrid][2] | totals[2][2] | ready.  Parity = segment & 1.
-constexpr int64_t kXsumTotals = 4 * kScanMaxGrid;
-constexpr int64_t kXsumReady = kXsumTotals + 4;
-
-// Exchange of the two-pass kernel, run by the compute warps of every CTA of
-// the co-resident grid once per segment, after each CTA has written its
-// chunk's exact sum to slots[c].  The CTA that arrives last at `ticket`
-// turns the slots into exclusive prefixes in place with one block-wide scan
-// (O(G) reads in all, instead of every CTA reading every slot), writes the
-// segment total and publishes `ready`; every CTA waits for `ready`
-// (bounded: ST_TIMEOUT) and reads its own prefix and the total into
-// ex / tot (all compute threads).
-template <int WARPS>
-__device__ __forceinline__ void exchange_prefix(const ScanParams& P, int64_t sg, int c, int G, u128& ex, u128& tot) {
-    constexpr int THREADS = WARPS * 32;
-    constexpr int Q = kScanMaxGrid / THREADS;
-    static_assert(kScanMaxGrid % THREADS == 0, "slots per thread");
-    __shared__ unsigned long long s_gen;
-    __shared__ int s_last;
-    __shared__ unsigned long long s_part[WARPS][2];
-    __shared__ unsigned long long s_res[4];
-    unsigned long long* slots = P.xsum + (sg & 1) * kScanMaxGrid * 2;
-    unsigned long long* total = P.xsum + kXsumTotals + (sg & 1) * 2;
-    unsigned long long* ready = P.xsum + kXsumReady;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-    compute_sync<THREADS>();
-    if (threadIdx.x == 0) {
-        __threadfence();  // this CTA's slot before its arrival
-        // (a CTA chosen by per_debug_drop_tile only reads the ticket: its
-        // arrival is lost, so nobody is last and every wait for `ready`
-        // runs out)
-        const unsigned long long t = c == P.drop_tile ? ld_relaxed_u64(P.ticket) : atomicAdd(P.ticket, 1ull);
-        s_gen = t / static_cast<unsigned long long>(G) + 1ull;
-        s_last = c != P.drop_tile && (t % static_cast<unsigned long long>(G)) == static_cast<unsigned long long>(G - 1);
-        if (s_last) __threadfence();  // every CTA's slot is visible from here on
-    }
-    compute_sync<THREADS>();
-    const unsigned long long gen = s_gen;
-    if (s_last) {
-        u128 x[Q];
-        u128 run = 0;
+            // the highest inclusive record of the window
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int k = threadIdx.x * Q + q;
-            unsigned long long a = 0ull, b = 0ull;
-            if (k < G) ld_relaxed_v2(slots + 2 * k, a, b);
-            x[q] = (static_cast<u128>(b) << 64) | a;
-        }
+            for (int o = 16; o > 0; o >>= 1) {
+                const int64_t ob = __shfl_xor_sync(PER_FULL_MASK, best, o);
+                best = ob > best ? ob : best;
+            }
+            bool missing = false;  // a record above `best` not yet there
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {  // thread-local exclusive prefixes
-            const u128 v = x[q];
-            x[q] = run;
-            run += v;
-        }
-        const u128 incl = warp_scan_u128(run, lane);
-        if (lane == 31) {
-            s_part[warp][0] = static_cast<unsigned long long>(incl);
-            s_part[warp][1] = static_cast<unsigned long long>(incl >> 64);
-        }
-        compute_sync<THREADS>();
-        u128 off = incl - run, all = 0;
+            for (int q = 0; q < kLookbackQ; ++q) {
+                const int64_t i = hi - 1 - lane - 32 * q;
+                if (i >= lo && i > best && !((present >> q) & 1u)) missing = true;
+            }
+            if (!__any_sync(PER_FULL_MASK, missing)) {
+                u128 part = 0;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
-            const u128 pw = (static_cast<u128>(s_part[w][1]) << 64) | s_part[w][0];
-            if (w < warp) off += pw;
-            all += pw;
-        }
+                for (int q = 0; q < kLookbackQ; ++q) {
+                    const int64_t i = hi - 1 - lane - 32 * q;
+                    if (i >= lo && i >= best) {
+                        u128 v = 0;
 #pragma unroll
-        for (int q = 0; q < Q; ++q) {
-            const int k = threadIdx.x * Q + q;
-            const u128 e = off + x[q];
-            if (k < G) st_relaxed_v2(slots + 2 * k, static_cast<unsigned long long>(e), static_cast<unsigned long long>(e >> 64));
-        }
-        if (threadIdx.x == 0)
-            st_relaxed_v2(total, static_cast<unsigned long long>(all), static_cast<unsigned long long>(all >> 64));
-        compute_sync<THREADS>();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            st_release_u64(ready, gen);
-        }
-    }
-    if (threadIdx.x == 0) {
-        uint64_t t0 = 0;
-        while (ld_acquire_u64(ready) < gen) {
-            const uint64_t now = global_ns();
+                        for (int k = 0; k < kRecWords; ++k)
+                            v |= static_cast<u128>(static_cast<unsigned>(w[q][k])) << (32 * k);
+                        part += v;
+                    }
+                }
+                acc += warp_sum_u128(part);
+                if (best >= 0) return acc;
+                hi = lo;
+                break;
+            }
+            // lane 0's clock for the whole warp, so every lane takes the same branch
+            const uint64_t now = __shfl_sync(PER_FULL_MASK, global_ns(), 0);
             if (t0 == 0) {
                 t0 = now;
             } else if (now - t0 > kWaitLimitNs) {
-                atomicOr(P.status, ST_TIMEOUT);
-                break;
+                if (lane == 0) {
+                    atomicOr(P.status, ST_TIMEOUT);
+                    *abort = 1;
+                }
+                __syncwarp();
+                return acc;
             }
-            __nanosleep(32);
+            __nanosleep(128);
         }
-        ld_relaxed_v2(slots + 2 * c, s_res[0], s_res[1]);
-        ld_relaxed_v2(total, s_res[2], s_res[3]);
     }
-    compute_sync<THREADS>();
-    ex = (static_cast<u128>(s_res[1]) << 64) | s_res[0];
-    tot = (static_cast<u128>(s_res[3]) << 64) | s_res[2];
+    return acc;
 }
 
-template <int ITEMS, int STAGES, int WARPS, int MINB>
-__global__ void __launch_bounds__(WARPS * 32 + 32, MINB) build_cdf_2p_kernel(ScanParams P) {
-    constexpr int THREADS = WARPS * 32;  // compute threads; one more warp produces
-    constexpr int TILE = THREADS * ITEMS;
-    constexpr int RUNS = ITEMS / 8;
-    static_assert(ITEMS % 8 == 0, "runs of 8 consecutive items per lane");
+// ---- tensor memory (TMEM) as the lag buffer ----------------------------------
+// TMEM is 128 lanes x 512 columns of 32 bits per SM; a warp reaches only the
+// 32 lanes of its quarter (warp index mod 4).  Compute warp w keeps the 16
+// p^alpha values of each of its lanes of tile k in columns
+// (k mod NX) * 64 + (w / 4) * 16 .. + 15 of lanes 32 (w mod 4) + lane:
+// 16 warps x 16 columns per tile, NX = 8 tiles = all 512 columns.
+constexpr unsigned kTmemCols = 512;
+
+__device__ __forceinline__ void tmem_alloc(unsigned* s_addr) {  // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(s_addr)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(unsigned taddr) {  // whole warp, the allocating one
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 consecutive columns of this lane: store, then wait for the store.
+__device__ __forceinline__ void tmem_store16(unsigned taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+        "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+        "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 16 consecutive columns of this lane: load, then wait for the load.
+__device__ __forceinline__ void tmem_load16(unsigned taddr, float (&v)[16]) {
+    unsigned r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+// 24 warps: six per SM sub-partition, whose register file (16,384) holds six
+// warps of 80 registers.
+__global__ void __maxnreg__(80) build_cdf_stream_kernel(ScanParams P) {
+    constexpr int STAGES = kStreamStages, LAG = kStreamLag, NX = kStreamXring;
+    constexpr int WARPS = kStreamWarps;  // compute warps, one 512-item slice each
+    constexpr int TILE = kStreamTile;    // WARPS slices x 32 lanes x 16 items
+    constexpr int PRODUCER = WARPS, PUBLISHER = WARPS + 1, LOOKBACK0 = WARPS + 2;
+    static_assert(TILE == WARPS * 32 * 16 && WARPS <= 32, "16 items per lane, a slice per lane of the publisher");
+    static_assert(NX > LAG, "exchange / TMEM slots for the lagged tiles, plus the one in its sum phase");
+    static_assert(NX * WARPS * 16 == 4 * kTmemCols, "TMEM: 16 columns per warp per tile, 4 warps per lane quarter");
     extern __shared__ __align__(128) float s_buf[];  // STAGES x TILE
-    __shared__ __align__(8) uint64_t s_full[STAGES], s_empty[STAGES];
-    __shared__ float s_agg[kChunkMax * WARPS];              // slice sums of the chunk
-    __shared__ float4 s_carry[kChunkMax * WARPS];           // slice carries
-    __shared__ volatile int s_abort;                        // a wait ran out: stop waiting
+    __shared__ __align__(8) uint64_t s_full[STAGES], s_empty[STAGES], s_sums[NX], s_pub[NX], s_carried[NX];
+    __shared__ int64_t s_tile[STAGES];          // tile of each stage
+    __shared__ int64_t s_xtile[NX];             // tile of each exchange slot (CTA tile k: slot k % NX),
+                                                // for the publisher and lookback warps
+    __shared__ float s_sum[NX * WARPS];         // slice sums
+    __shared__ ulonglong2 s_pre[NX * WARPS];    // their exact exclusive prefixes within the tile
+    __shared__ ulonglong2 s_agg[NX];            // the tile's exact total
+    __shared__ float4 s_carry[NX * WARPS];      // slice carries (hi, lo, fl32(E), fl32(E'))
+    __shared__ unsigned s_tmem;                 // TMEM base address
+    __shared__ volatile int s_abort;            // a wait ran out: nobody waits any more
+    __shared__ volatile int s_count;            // tiles this CTA got (known once the tickets run out)
+    __shared__ unsigned s_epoch;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    TwoPassLoads L;
-    L.T = P.num_tiles;
-    L.S = P.seg_tiles;
-    L.nseg = (L.T + L.S - 1) / L.S;
-    L.G = G;
-    L.c = c;
-    L.start();
+    const int64_t T = P.num_tiles;
     if (threadIdx.x == 0) {
         for (int st = 0; st < STAGES; ++st) {
             mbar_init(&s_full[st], 1);
             mbar_init(&s_empty[st], WARPS);
         }
+        for (int x = 0; x < NX; ++x) {
+            mbar_init(&s_sums[x], WARPS);
+            mbar_init(&s_pub[x], 1);
+            mbar_init(&s_carried[x], 1);
+        }
         s_abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_count = 0x7fffffff;
+        s_epoch = ld_relaxed_u32(P.ctrs + CTR_SCAN_EPOCH);
     }
+    if (warp == 0) tmem_alloc(&s_tmem);  // all 512 columns (one CTA per SM)
+    tmem_fence_before();
     __syncthreads();
-    // bounded wait; after the first expiry in the CTA nobody waits any more
-    auto wait = [&](uint64_t* bar, unsigned parity) {
-        if (s_abort) return;
-        if (!mbar_wait_bounded(bar, parity)) {
-            s_abort = 1;
-            atomicOr(P.status, ST_TIMEOUT);
+    tmem_fence_after();
+    const unsigned epoch = s_epoch;
+    // Bounded wait for phase `parity` of `bar`, which belongs to the CTA's
+    // tile k: false when the CTA got fewer than k + 1 tiles (nothing will
+    // arrive) or after an expired wait.
+    auto wait_k = [&](uint64_t* bar, unsigned parity, int k) -> bool {
+        if (s_abort) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = global_ns();
+        for (;;) {
+            if (k >= s_count || s_abort) return false;
+            if (mbar_try_wait_for(bar, parity, 1000u)) return true;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                s_abort = 1;
+                atomicOr(P.status, ST_TIMEOUT);
+                return false;
+            }
         }
     };
+    // the same, decided for the whole warp (every lane waits, and the warp
+    // proceeds only if all saw the phase complete), so that the warp stays
+    // converged for its shuffles and tcgen05 instructions
+    auto wait_w = [&](uint64_t* bar, unsigned parity, int k) -> bool {
+        return __all_sync(PER_FULL_MASK, wait_k(bar, parity, k));
+    };
+    auto aborted_w = [&]() -> bool { return __any_sync(PER_FULL_MASK, s_abort != 0); };
+    int issued = 0;  // copies issued (producer thread)
 
-    if (warp == WARPS) {
-        // ======================= producer warp ================================
+    if (warp == PRODUCER) {
         if (lane == 0) {
-            for (uint64_t q = 0;; ++q) {
-                int64_t t;
-                if (!L.next(t)) break;
-                const int st = static_cast<int>(q % STAGES);
-                if (q >= STAGES) wait(&s_empty[st], static_cast<unsigned>(q / STAGES - 1) & 1u);
-                if (s_abort) break;
+            for (int k = 0;; ++k) {
+                const int st = k % STAGES;
+                if (k >= STAGES && !wait_k(&s_empty[st], static_cast<unsigned>(k / STAGES - 1) & 1u, k - STAGES)) break;
+                const int64_t t = atomicAdd(P.ctrs + CTR_SCAN_TICKET, 1u);
+                if (t >= T || s_abort) {
+                    s_count = k;
+                    break;
+                }
+                s_tile[st] = t;
                 load_tile<TILE>(P, static_cast<unsigned>(t), s_buf + st * TILE, &s_full[st]);
+                issued = k + 1;
             }
+        }
+    } else if (warp == PUBLISHER) {
+        for (int k = 0;; ++k) {
+            const int st = k % NX;
+            if (!wait_w(&s_sums[st], static_cast<unsigned>(k / NX) & 1u, k)) break;
+            bool range_err = false;
+            const u128 f = lane < WARPS ? to_fixed(s_sum[st * WARPS + lane], range_err) : 0;
+            if (range_err) atomicOr(P.status, ST_RANGE);
+            const u128 incl = warp_scan_u128(f, lane);
+            if (lane < WARPS) {
+                const u128 ex = incl - f;
+                s_pre[st * WARPS + lane] = make_ulonglong2(static_cast<unsigned long long>(ex),
+                                                           static_cast<unsigned long long>(ex >> 64));
+            }
+            const uint64_t tlo = __shfl_sync(PER_FULL_MASK, static_cast<uint64_t>(incl), WARPS - 1);
+            const uint64_t thi = __shfl_sync(PER_FULL_MASK, static_cast<uint64_t>(incl >> 64), WARPS - 1);
+            const u128 agg = (static_cast<u128>(thi) << 64) | tlo;
+            const int64_t t = s_xtile[st];
+            __syncwarp();
+            if (lane == 0) {
+                s_agg[st] = make_ulonglong2(tlo, thi);
+                // tile 0's aggregate is already its inclusive prefix
+                if (t != P.drop_tile) publish_record(P, t, t == 0 ? tag_inclusive(epoch) : tag_aggregate(epoch), agg);
+                mbar_arrive(&s_pub[st]);
+            }
+        }
+    } else if (warp >= LOOKBACK0) {
+        for (int k = warp - LOOKBACK0;; k += kStreamLookback) {
+            const int st = k % NX;
+            if (!wait_w(&s_pub[st], static_cast<unsigned>(k / NX) & 1u, k)) break;
+            const int64_t t = s_xtile[st];
+            const ulonglong2 a = s_agg[st];
+            const u128 E = t > 0 ? lookback(P, t, epoch, lane, &s_abort) : 0;
+            if (lane == 0 && t > 0 && t != P.drop_tile)
+                publish_record(P, t, tag_inclusive(epoch), E + ((static_cast<u128>(a.y) << 64) | a.x));
+            // carries of the sixteen slices, lane w for slice w: E_w = E + the
+            // slices before w; E_w' = E_w + slice w's sum
+            if (lane < WARPS) {
+                const ulonglong2 ep = s_pre[st * WARPS + lane];
+                const u128 Ew = E + ((static_cast<u128>(ep.y) << 64) | ep.x);
+                bool unused = false;
+                const u128 En = Ew + to_fixed(s_sum[st * WARPS + lane], unused);
+                float hi, lo;
+                fixed_to_float2(Ew, hi, lo);
+                s_carry[st * WARPS + lane] = make_float4(hi, lo, hi, fixed_to_float(En));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_carried[st]);
         }
     } else {
         // ======================= compute warps ================================
-        u128 base = 0;   // exact total of the earlier segments
-        uint64_t q = 0;  // copies consumed
-        const int ibase = warp * 32 * ITEMS + lane * 8;  // this lane's first item of run 0
+        const int ibase = warp * 512 + lane * 8;  // this lane's first item of run 0
+        // this warp's TMEM columns of slot 0 (lanes of its quarter)
+        const unsigned tbase = s_tmem + (static_cast<unsigned>(32 * (warp & 3)) << 16) + static_cast<unsigned>((warp >> 2) * 16);
         bool bad = false;
-        for (int64_t sg = 0; sg < L.nseg; ++sg) {
-            const int64_t lo = L.chunk_lo(sg);
-            const int m = static_cast<int>(L.chunk_len(sg));
-
-            // ---- pass 1: slice sums ---------------------------------------
-            for (int j = 0; j < m; ++j, ++q) {
-                const int st = static_cast<int>(q % STAGES);
-                wait(&s_full[st], static_cast<unsigned>(q / STAGES) & 1u);
-                const int64_t tile_base = (lo + j) * TILE;
-                const int valid = static_cast<int>(P.n - tile_base < TILE ? P.n - tile_base : TILE);
-                const float* buf = s_buf + st * TILE;
-                float sum = 0.f;
-                if (valid == TILE && P.pow_mode != 2) {
-                    // full tile: the slice's values at once, one range test
-                    float v[ITEMS];
-                    slice_values<ITEMS>(P, buf, ibase, v, bad);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_empty[st]);
-                    unsigned long long acc = f2_pack(v[0], v[1]);
-#pragma unroll
-                    for (int e = 2; e < ITEMS; e += 2) acc = f2_add(acc, f2_pack(v[e], v[e + 1]));
-                    float a0, a1;
-                    f2_unpack(acc, a0, a1);
-                    sum = a0 + a1;
+        int k_end = 0x7fffffff;  // the CTA's tile count, once its local phases ran out
+        // tile of exchange slot x in lane x (slot k % NX holds CTA tile k until
+        // this warp has written it)
+        int64_t ring_tile = 0;
+        for (int k = 0; k - LAG < k_end && !aborted_w(); ++k) {
+            // ---- local phase of tile k: p^alpha, the slice's sum, its local scan to TMEM
+            if (k < k_end) {
+                const int st = k % STAGES, x = k % NX;
+                if (!wait_w(&s_full[st], static_cast<unsigned>(k / STAGES) & 1u, k)) {
+                    k_end = aborted_w() ? 0 : k;
                 } else {
+                    const int64_t t = s_tile[st];
+                    const int64_t tile_base = t * TILE;
+                    const int valid = static_cast<int>(P.n - tile_base < TILE ? P.n - tile_base : TILE);
+                    const float* buf = s_buf + st * TILE;
+                    float v[16];
+                    float sum = 0.f;
+                    if (valid == TILE && P.pow_mode != 2) {
+                        // full tile: the slice's values at once, one range test;
+                        // the sum in two interleaved chains, then their sum
+                        slice_values<16>(P, buf, ibase, v, bad);
+                        unsigned long long acc = f2_pack(v[0], v[1]);
 #pragma unroll
-                    for (int r = 0; r < RUNS; ++r) {
-                        float v[8];
-                        run_values<TILE>(P, buf, tile_base, valid, ibase + r * 256, v, bad);
+                        for (int e = 2; e < 16; e += 2) acc = f2_add(acc, f2_pack(v[e], v[e + 1]));
+                        float a0, a1;
+                        f2_unpack(acc, a0, a1);
+                        sum = a0 + a1;
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) sum += v[e];
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_empty[st]);
-                }
+                        for (int r = 0; r < 2; ++r) {
+                            float(&u)[8] = *reinterpret_cast<float(*)[8]>(v + 8 * r);
+                            run_values<TILE>(P, buf, tile_base, valid, ibase + r * 256, u, bad);
 #pragma unroll
-                for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(PER_FULL_MASK, sum, d);
-                if (lane == 0) s_agg[j * WARPS + warp] = sum;
-            }
-
-            // ---- exchange: chunk sums -> prefixes -> carries of the slices ---
-            // Before the barrier, from this CTA's sums alone: lane j of warp w
-            // holds the exact prefix of slice (j, w) within the chunk and the
-            // next slice's (kChunkMax == 32: one lane per tile).
-            static_assert(kChunkMax == 32, "one lane per tile of the chunk");
-            compute_sync<THREADS>();  // s_agg complete
-            u128 loc = 0, loc_next = 0;
-            {
-                u128 tsum = 0, before = 0;  // tile j's sum; its slices before this warp's
-                bool range_err = false;
-                if (lane < m) {
-#pragma unroll
-                    for (int w = 0; w < WARPS; ++w) {
-                        const u128 f = to_fixed(s_agg[lane * WARPS + w], range_err);
-                        if (w < warp) before += f;
-                        if (w == warp) loc_next = f;
-                        tsum += f;
-                    }
-                }
-                if (range_err && warp == 0) atomicOr(P.status, ST_RANGE);
-                const u128 incl = warp_scan_u128(tsum, lane);
-                loc = incl - tsum + before;
-                loc_next += loc;
-                if (warp == 0 && lane == 31)  // the chunk's exact sum
-                    st_relaxed_v2(P.xsum + (sg & 1) * kScanMaxGrid * 2 + 2 * c,
-                                  static_cast<unsigned long long>(incl), static_cast<unsigned long long>(incl >> 64));
-            }
-            {
-                u128 ex, tot;
-                exchange_prefix<WARPS>(P, sg, c, G, ex, tot);
-                if (lane < m) {  // carry of this warp's slice of tile `lane`
-                    float hi, lo2;
-                    fixed_to_float2(base + ex + loc, hi, lo2);
-                    s_carry[lane * WARPS + warp] = make_float4(hi, lo2, hi, fixed_to_float(base + ex + loc_next));
-                }
-                base += tot;
-            }
-            compute_sync<THREADS>();  // s_agg is free for the next segment
-
-            // ---- pass 2: slice scans, written with their carries -------------
-            for (int j = 0; j < m; ++j, ++q) {
-                const int st = static_cast<int>(q % STAGES);
-                wait(&s_full[st], static_cast<unsigned>(q / STAGES) & 1u);
-                const int64_t tile_base = (lo + j) * TILE;
-                const int valid = static_cast<int>(P.n - tile_base < TILE ? P.n - tile_base : TILE);
-                const bool full = valid == TILE;
-                const float* buf = s_buf + st * TILE;
-                const float4 cy = s_carry[j * WARPS + warp];
-                float carry = 0.f;
-                if (full && P.pow_mode != 2 && P.cdf_v8) {
-                    // full tile: the slice's values at once, then run by run
-                    float v[ITEMS];
-                    bool unused = false;
-                    slice_values<ITEMS>(P, buf, ibase, v, unused);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_empty[st]);
-#pragma unroll
-                    for (int r = 0; r < RUNS; ++r) {
-                        float(&u)[8] = *reinterpret_cast<float(*)[8]>(v + 8 * r);
-                        scan_run(u, carry, lane);
-                        emit_run<true, TILE>(P, u, cy, tile_base, ibase + r * 256, TILE, lane);
-                    }
-                } else {
-#pragma unroll
-                    for (int r = 0; r < RUNS; ++r) {
-                        float v[8];
-                        bool unused = false;
-                        run_values<TILE>(P, buf, tile_base, valid, ibase + r * 256, v, unused);
-                        if (r == RUNS - 1) {  // the stage has been read
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&s_empty[st]);
+                            for (int e = 0; e < 8; ++e) sum += u[e];
                         }
-                        scan_run(v, carry, lane);
-                        emit_run<false, TILE>(P, v, cy, tile_base, ibase + r * 256, valid, lane);
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_empty[st]);  // the stage has been read
+#pragma unroll
+                    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(PER_FULL_MASK, sum, d);
+                    if (lane == 0) {
+                        s_sum[x * WARPS + warp] = sum;
+                        if (warp == 0) s_xtile[x] = t;
+                    }
+                    if (lane == x) ring_tile = t;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_sums[x]);
+                    // the slice's local scan while its carry is being found
+                    scan_pair(*reinterpret_cast<float(*)[8]>(v), *reinterpret_cast<float(*)[8]>(v + 8), lane);
+                    tmem_store16(tbase + static_cast<unsigned>(x * 64), v);
+                }
+            }
+            // ---- emit phase of tile k - LAG: the carry added, clamped, written once
+            const int ks = k - LAG;
+            if (ks >= 0 && ks < k_end) {
+                const int x = ks % NX;
+                if (!wait_w(&s_carried[x], static_cast<unsigned>(ks / NX) & 1u, ks)) break;
+                const int64_t tile_base = __shfl_sync(PER_FULL_MASK, ring_tile, x) * TILE;
+                const int valid = static_cast<int>(P.n - tile_base < TILE ? P.n - tile_base : TILE);
+                const float4 cy = s_carry[x * WARPS + warp];
+                float u[16];
+                tmem_load16(tbase + static_cast<unsigned>(x * 64), u);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float(&ur)[8] = *reinterpret_cast<float(*)[8]>(u + 8 * r);
+                    if (valid == TILE && P.cdf_v8)
+                        emit_run<true, TILE>(P, ur, cy, tile_base, ibase + r * 256, TILE, lane);
+                    else
+                        emit_run<false, TILE>(P, ur, cy, tile_base, ibase + r * 256, valid, lane);
                 }
             }
         }
         if (__any_sync(PER_FULL_MASK, bad) && lane == 0) atomicOr(P.status, ST_VALUE);
     }
 
-    // ---- the last CTA to finish rearms the barrier ticket for the next call --
+    tmem_fence_before();
     __syncthreads();
+    tmem_fence_after();
+    if (warp == 0) tmem_dealloc(s_tmem);  // every TMEM access above has completed (waited)
+    if (warp == PRODUCER && lane == 0) {
+        // after an expired wait some copies may not have been consumed: wait
+        // (bounded) for the last copy issued into each stage before exiting
+        for (int st = 0; st < STAGES && st < issued; ++st) {
+            const int uses = (issued - st + STAGES - 1) / STAGES;
+            mbar_wait_bounded(&s_full[st], static_cast<unsigned>(uses - 1) & 1u);
+        }
+    }
+    // the last CTA to finish re-arms the ticket and advances the epoch for
+    // the next call
     if (threadIdx.x == 0) {
         const unsigned done = atomicAdd(P.ctrs + CTR_SCAN_DONE, 1u);
         if (done == gridDim.x - 1u) {
             P.ctrs[CTR_SCAN_DONE] = 0u;
-            *P.ticket = 0ull;
-            P.xsum[kXsumReady] = 0ull;
+            P.ctrs[CTR_SCAN_TICKET] = 0u;
+            advance_scan_epoch(P, epoch);
         }
     }
 }
 
-// Launch of the two-pass kernel: one co-resident wave (cooperative) of at most
-// kScanMaxGrid CTAs; segments of equal size, at most kSegMaxTiles tiles and at
-// most kChunkMax tiles per CTA.
-template <int ITEMS, int STAGES, int WARPS, int MINB>
-per_status launch_scan_2p(ScanParams P, int num_sms, cudaStream_t s) {
-    constexpr int TILE = WARPS * 32 * ITEMS;
-    const size_t smem = static_cast<size_t>(STAGES) * TILE * sizeof(float);
-    if (!P.xsum || !P.ticket) return PER_ERR_STATE;
+// Launch of the streaming kernel: one co-resident wave (cooperative) of at
+// most one CTA per SM, which take tiles by ticket.  Each CTA allocates all
+// 512 TMEM columns of its SM, so a second CTA on the same SM would wait in
+// its allocation for the first one to finish: the grid never exceeds the SM
+// count (the kernel's shared memory and registers also fit only one).
+per_status launch_scan_stream(ScanParams P, int num_sms, cudaStream_t s) {
+    constexpr int TILE = kStreamTile;
+    const size_t smem = static_cast<size_t>(kStreamStages) * TILE * sizeof(float);
+    if (!P.rec) return PER_ERR_STATE;
     static DeviceCache cache;
     const int per_sm = device_cached(cache, [&]() {
         int b = 0;
-        if (cudaFuncSetAttribute(build_cdf_2p_kernel<ITEMS, STAGES, WARPS, MINB>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, build_cdf_2p_kernel<ITEMS, STAGES, WARPS, MINB>,
-                                                          WARPS * 32 + 32, smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(build_cdf_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, build_cdf_stream_kernel, kStreamThreads, smem) !=
+                cudaSuccess)
             return 0;
         return b;  // 0: the kernel does not fit an SM (a launch error)
     });
     if (per_sm == 0) return PER_ERR_CUDA;
     const int64_t tiles = (P.n + TILE - 1) / TILE;
-    if (tiles > 0xffffffffll) return PER_ERR_ARG;
+    if (tiles > 0x7fffffffll || tiles > P.rec_tiles) return PER_ERR_ARG;
     P.num_tiles = static_cast<unsigned>(tiles);
-    int64_t grid = static_cast<int64_t>(num_sms) * per_sm;
+    int64_t grid = num_sms;
     if (grid > tiles) grid = tiles;
     if (grid > kScanMaxGrid) grid = kScanMaxGrid;
-    const int64_t seg_max = kSegMaxTiles < kChunkMax * grid ? kSegMaxTiles : kChunkMax * grid;
-    const int64_t nseg = (tiles + seg_max - 1) / seg_max;
-    P.seg_tiles = (tiles + nseg - 1) / nseg;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(WARPS * 32 + 32);
+    cfg.blockDim = dim3(kStreamThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -591,7 +699,7 @@ per_status launch_scan_2p(ScanParams P, int num_sms, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_2p_kernel<ITEMS, STAGES, WARPS, MINB>, P);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, build_cdf_stream_kernel, P);
     per_note_launch();
     return cuda_status(e);
 }
@@ -642,7 +750,7 @@ per_status launch_scan_wave(ScanParams P, int num_sms, cudaStream_t s) {
 }
 
 // One wave of 2048-item tiles for small inputs, of 4096-item tiles up to what
-// the GPU holds at once, then the two-pass kernel.
+// the GPU holds at once, then the streaming kernel.
 per_status scan_dispatch(ScanParams P, int num_sms, cudaStream_t s) {
     if (P.n <= int64_t(1) << 19) {
         const per_status st = launch_scan_wave<256>(P, num_sms, s);
@@ -652,7 +760,7 @@ per_status scan_dispatch(ScanParams P, int num_sms, cudaStream_t s) {
         const per_status st = launch_scan_wave<512>(P, num_sms, s);
         if (st != PER_ERR_STATE) return st;
     }
-    return launch_scan_2p<16, 4, 8, 3>(P, num_sms, s);
+    return launch_scan_stream(P, num_sms, s);
 }
 
 }  // namespace
@@ -677,9 +785,8 @@ per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* c
     P.status = ctx->status;
     P.num_tiles = 0;
     P.coarse = coarse;
-    P.xsum = ctx->scan_xsum;
-    P.ticket = ctx->tickets + TK_SCAN;
-    P.seg_tiles = 0;
+    P.rec = ctx->scan_rec;
+    P.rec_tiles = ctx->scan_rec_tiles;
     P.drop_tile = ctx->drop_tile;  // a fault injected for one call only
     ctx->drop_tile = -1;
     return scan_dispatch(P, ctx->num_sms, s);
@@ -692,17 +799,17 @@ per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* c
 // framework's operator or callback, where the host application owns every
 // byte of device memory through its own pool, or a latency-critical loop in
 // which cudaMalloc's implicit device synchronisation is not acceptable.  This
-// entry point runs the same scan kernel as per_build_cdf, but keeps its
-// lookback words, chunk sums, barrier ticket and counters in the file-scope
-// array below instead of in a context, so the caller only passes the
-// priorities and the output CDF and nothing is ever allocated.
+// entry point runs the same scan kernels as per_build_cdf, but keeps their
+// lookback words, tile records and counters in the file-scope array below
+// instead of in a context, so the caller only passes the priorities and the
+// output CDF and nothing is ever allocated.
 //
 // The array is part of the library image: every GPU that loads the library
-// holds it (about 160 KiB) until the process exits.  All calls on a device
+// holds it (about 400 KiB) until the process exits.  All calls on a device
 // share it and it keeps the previous call's contents: the kernels leave their
-// counters, ticket and ready word at rest for the next call even after a
-// bounded wait ran out, and their tile words carry a per-call tag, so
-// nothing needs re-arming.  Two calls whose kernels overlap on the GPU --
+// counters and ticket at rest for the next call even after a bounded wait
+// ran out, and their tile words and records carry a per-call tag, so nothing
+// needs re-arming.  Two calls whose kernels overlap on the GPU --
 // different streams without ordering between them -- race on it and give
 // wrong results.  Serialise calls per device.
 // ====================================================================
@@ -717,11 +824,11 @@ constexpr int kNoAllocMaxDevices = kMaxDevices;
 }  // namespace
 
 constexpr int64_t kNoAllocStateWords = kNoAllocMaxTiles * kDescStride + 1;  // == scan_state_words(kMaxWaveTiles)
-// layout (64-bit words): lookback words | counters | status | chunk sums
-// (16-byte aligned) | barrier ticket
-constexpr int64_t kNoAllocXsumOff = (kNoAllocStateWords + kNoAllocCtrWords + 8 + 1) & ~int64_t(1);
-constexpr int64_t kNoAllocTicketOff = kNoAllocXsumOff + kScanXsumWords;
-constexpr int64_t kNoAllocWords = kNoAllocTicketOff + 2;
+// layout (64-bit words): lookback words | counters | status | tile records
+// of the streaming kernel (128-byte aligned)
+constexpr int64_t kNoAllocRecOff = (kNoAllocStateWords + kNoAllocCtrWords + 8 + 15) & ~int64_t(15);
+constexpr int64_t kNoAllocRecTiles = (kNoAllocMaxN + kStreamTile - 1) / kStreamTile + 1;  // == scan_rec_tiles(max n)
+constexpr int64_t kNoAllocWords = kNoAllocRecOff + kNoAllocRecTiles * kRecStride;
 static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocWords];
 
 namespace {
@@ -787,13 +894,12 @@ extern "C" per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, floa
     P.status = d_status ? d_status : reinterpret_cast<int*>(scratch + kNoAllocStateWords + kNoAllocCtrWords);
     P.num_tiles = 0;
     P.coarse = nullptr;
-    P.xsum = scratch + kNoAllocXsumOff;
-    P.ticket = scratch + kNoAllocTicketOff;
-    P.seg_tiles = 0;
+    P.rec = scratch + kNoAllocRecOff;
+    P.rec_tiles = kNoAllocRecTiles;
     P.drop_tile = -1;
     // same kernels and tile choice as per_build_cdf: the one-wave kernels use
     // at most kMaxWaveTiles tile words (launch_scan_wave checks), and larger
-    // inputs go to the two-pass kernel, whose exchange words do not depend
-    // on n
+    // inputs go to the streaming kernel, whose records cover n <= kNoAllocMaxN
+    // (launch_scan_stream checks)
     return scan_dispatch(P, g_noalloc_sms[dev], s);
 }

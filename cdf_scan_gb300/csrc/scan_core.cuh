@@ -29,14 +29,14 @@ struct ScanParams {
     int* status;
     unsigned num_tiles;
     float* coarse;  // every kCoarseStride-th CDF value (or nullptr)
-    // two-pass kernel only
-    unsigned long long* xsum;    // exchange words of the two-pass kernel (kScanXsumWords)
-    unsigned long long* ticket;  // grid-barrier ticket (0 between calls)
-    int64_t seg_tiles;           // tiles per segment
-    // fault injection for tests (per_debug_drop_tile): the tile (one-wave
-    // kernels) or CTA (two-pass kernel) whose carry word or exchange arrival
-    // this call withholds, or -1
-    int64_t drop_tile;
+    // streaming kernel only: one tagged record per tile, kRecStride words
+    // apart (rec_tiles of them)
+    unsigned long long* rec = nullptr;
+    int64_t rec_tiles = 0;
+    // fault injection for tests (per_debug_drop_tile): the tile whose carry
+    // word (one-wave kernels) or record (streaming kernel) this call
+    // withholds, or -1
+    int64_t drop_tile = -1;
 };
 
 // fp32 (>= 0) -> fixed point with kFracBits fractional bits, truncating below
@@ -177,6 +177,7 @@ __device__ __forceinline__ void advance_scan_epoch(const ScanParams& P, unsigned
     unsigned next = epoch + 1u;
     if (next >= (1u << 30)) {
         for (int64_t i = 0; i < P.desc_tiles; ++i) P.desc[i * kDescStride] = 0ull;
+        for (int64_t i = 0; i < P.rec_tiles * kRecStride; ++i) P.rec[i] = 0ull;
         next = 1u;
     }
     P.ctrs[CTR_SCAN_EPOCH] = next;

@@ -143,11 +143,12 @@ per_status per_build_cdf(per_ctx* ctx, void* stream);
  * a latency-critical loop where cudaMalloc's implicit device synchronisation
  * is not acceptable.  This call needs no context: it reads d_prio[0..n)
  * (float32, >= 0, 16-byte aligned), writes d_cdf[0..n) (16-byte aligned) =
- * the inclusive prefix sum of d_prio^alpha, with the same kernel and the same
- * bit-exact result as per_build_cdf, and allocates nothing.
+ * the inclusive prefix sum of d_prio^alpha, with the same kernels and the
+ * same bit-exact result as per_build_cdf, and allocates nothing.
  *
- * Its scratch (tile aggregates for the lookback, chunk sums and a few counters) is a fixed ~160 KiB
- * array compiled into the library, held by every GPU that loads the library
+ * Its scratch (tile sums and tile records for the lookbacks and a few
+ * counters) is a fixed ~400 KiB array compiled into the library, held by
+ * every GPU that loads the library
  * until the process exits; hence n <= 16,777,216 (2^24), larger n returns
  * PER_ERR_ARG without launching.  The first call on each device performs a
  * one-time set-up with that device current (resolves the array's address,
@@ -313,14 +314,15 @@ per_status per_check(per_ctx* ctx, void* stream);
  * the NEXT scan on this context -- per_build_cdf, or the scan inside
  * per_step / per_rank_build -- loses one message, as if it had been dropped:
  * in the one-wave scan (inputs that fit one wave of CTAs) tile `tile` does
- * not publish its carry word; in the two-pass scan of larger inputs CTA
- * `tile` does not arrive at the exchange of chunk sums.  Every wait for it
- * then runs out after the bounded-wait limit (about 2 s): the kernels record
- * PER_ERR_TIMEOUT (read by per_check), stop waiting, finish, and leave the
- * context usable for the next call, whose result is correct again.  That
- * call's CDF (and samples) are unspecified.  Tiles of the one-wave scan are
- * 2048 items (n <= 2^19) or 4096 items; a tile or CTA the call does not have
- * changes nothing.  tile = -1 cancels.  Host-side only; the injection
+ * not publish its carry word; in the streaming scan of larger inputs tile
+ * `tile` does not publish its record (neither its sum nor its inclusive
+ * prefix).  Every wait for it then runs out after the bounded-wait limit
+ * (about 2 s): the kernels record PER_ERR_TIMEOUT (read by per_check), stop
+ * waiting, finish, and leave the context usable for the next call, whose
+ * result is correct again.  That call's CDF (and samples) are unspecified.
+ * Tiles of the one-wave scan are 2048 items (n <= 2^19) or 4096 items, of
+ * the streaming scan 8192 items; a tile the call does not have changes
+ * nothing.  tile = -1 cancels.  Host-side only; the injection
  * applies to one call and is then cleared.  Never needed outside tests.
  */
 per_status per_debug_drop_tile(per_ctx* ctx, int64_t tile);

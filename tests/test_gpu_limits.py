@@ -1,7 +1,7 @@
 """GPU parity at the entry points' largest sizes, against the oracle.
 
-  * build_cdf at n = 2^28 (1 GiB of priorities: 16 L2-sized segments of the
-    two-pass scan): within 1e-5 of the total of the fp64 prefix sums,
+  * build_cdf at n = 2^28 (1 GiB of priorities: 32,768 tiles of the
+    streaming scan): within 1e-5 of the total of the fp64 prefix sums,
     monotone, last value = per_total; 2^20 samples bit-exact when the oracle
     searches the GPU's CDF;
   * the sampler at its largest batch, B = 2^24, bit-exact the same way;

@@ -6,8 +6,8 @@
   GPU's leaves, after a bulk load and after updates.
 * An update index outside [0, capacity) records PER_ERR_VALUE and writes
   nothing for that entry (the valid entries of the batch still apply).
-* A lost message (per_debug_drop_tile: a carry word or an exchange arrival
-  that is never published) makes the waits for it run out: the call records
+* A lost message (per_debug_drop_tile: a carry word or a tile record that is
+  never published) makes the waits for it run out: the call records
   PER_ERR_TIMEOUT, the kernels finish, and the next call on the same context
   is correct again against the oracle.  The waits are bounded (about 2 s); no
   GPU is faulted, trapped or hung.
@@ -116,10 +116,10 @@ def check_cdf(ctx, p, alpha):
 
 
 @pytest.mark.parametrize("n,drop", [(100_000, 5), (1_000_000, 40), (3 * (1 << 20) + 11, 3)],
-                         ids=["one-wave-2048", "one-wave-4096", "two-pass"])
+                         ids=["one-wave-2048", "one-wave-4096", "streaming"])
 def test_lost_scan_message_times_out_and_the_context_recovers(n, drop):
-    """one-wave scans: tile `drop` never publishes its carry word; two-pass
-    scan: CTA `drop` never arrives at the exchange of chunk sums."""
+    """one-wave scans: tile `drop` never publishes its carry word; streaming
+    scan: tile `drop` never publishes its record (sum or inclusive prefix)."""
     alpha = 0.6
     p = workloads.abs_normal(n, workloads.rng(402, n))
     ctx = new_ctx(p, alpha, SCAN)

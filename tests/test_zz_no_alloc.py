@@ -5,7 +5,7 @@ owns all device memory, or in a loop that cannot afford cudaMalloc's implicit
 device synchronisation).  For them the library offers a context-free
 build_cdf whose scratch is a fixed array compiled into the library.  This test
 calls it through the C ABI several times in a row, on different inputs and
-sizes -- one item, the one-wave and two-pass kernels, and the largest size the
+sizes -- one item, the one-wave and streaming kernels, and the largest size the
 array allows, with and without a status word -- and checks each result
 against the CPU oracle's fp64 CDF (2e-6 of the total up to 2^20 items, 1e-5
 above, the tolerances of the other tests) and against the context-based
