@@ -26,7 +26,9 @@
 //      max fills every output with the particle whose run covers it (16-byte
 //      stores; no per-output search).
 // exp is the hardware ex2 of (lw - m) * log2(e): its relative error (~2^-22)
-// stays far inside the CDF tolerance.  For a power-of-two P the threshold
+// stays far inside the CDF tolerance.  Segments of up to 16,384 particles
+// (the usual case) are staged in shared memory, so the row is read once and
+// exp runs once per particle; longer segments read the row in each pass.  For a power-of-two P the threshold
 // division is an exact multiplication by 2^-k.
 #include <cooperative_groups.h>
 
@@ -42,9 +44,19 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kLane = 8;                   // consecutive particles per lane per chunk
 constexpr int kBatch = 8;                  // float4 loads in flight per thread in passes 1 and 2
 constexpr int kChunk = kThreads * kLane;   // 4096
+constexpr int kWarpBlock = 32 * kLane;     // outputs per warp per output block (256)
+static_assert(kWarps * kWarpBlock == kChunk, "the warps' staging rows tile one block of kChunk");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxSplit = 8;      // CTAs per row at most (one cluster, the portable size limit)
 constexpr int kMinSegChunks = 4;  // chunks per CTA below which splitting needs a spare wave
+// Segments of at most kStageMax particles are staged in shared memory (64 KiB,
+// two CTAs per SM): pass 1 copies the log-weights there, pass 2 replaces
+// them by w = exp(x - m), and pass 3 reads w back, so the row is read from
+// global memory once and exp runs once per particle.  Longer segments (and
+// the resample step, which runs three CTAs per SM) read the row in every
+// pass and compute exp twice.
+constexpr int kStageMax = 4 * kChunk;
+static_assert(kStageMax == kThreads * 4 * kBatch, "one pass-1 iteration covers a staged segment");
 
 struct ResampleParams {
     const float* logw;  // may also be out_logw
@@ -61,6 +73,7 @@ struct ResampleParams {
     float* out_logw;                  // [rows][P] (may be logw itself)
     float reset;                      // fl32(-log P)
     int seg;                          // particles per CTA of a row's cluster (a multiple of kChunk)
+    bool staged;                      // the segment lives in shared memory (seg <= kStageMax)
 };
 
 // Threshold u_j = fl32(fl32(j + U) / P); for a power of two P the division is
@@ -88,19 +101,27 @@ __device__ __forceinline__ int count_le(float c, float U, int P, float fP, float
 // is exact below 2^24 and U < 1); every j >= f + 1 does not, since
 // fl32(j + U) >= j > C.  So two exact tests, at j = f - 1 and j = f, settle
 // the count (the test is monotone in j, so the two indicators add up).
+//
+// In floats: F = floor(C) and F - 1 are exact, so the tests are
+// fl32((F - 1) + U) <= C and fl32(F + U) <= C.  For F = 0 the first test
+// (j = -1) always holds and stands in for the missing j <= -2 term; for
+// F >= P the count is clamped to P (the tests are monotone in j, so the
+// second cannot hold without the first).  NaN gives 0.
 __device__ __forceinline__ int count_le_pow2(float c, float U, int P, float fP) {
     const float C = __fmul_rn(c, fP);
-    const int f = __float2int_rd(C);  // C >= 0 (NaN gives some f; the result stays in [0, P])
-    int n = min(max(f - 1, 0), P);
-    if (f - 1 >= 0 && f - 1 < P && __fadd_rn(__int2float_rn(f - 1), U) <= C) ++n;
-    if (f >= 0 && f < P && __fadd_rn(__int2float_rn(f), U) <= C) ++n;
-    return n;
+    const float F = floorf(C);
+    int n = __float2int_rz(F) - 1;
+    if (__fadd_rn(__fsub_rn(F, 1.0f), U) <= C) ++n;
+    if (__fadd_rn(F, U) <= C) ++n;
+    return min(max(n, 0), P);
 }
 
-// floor(w * 2^40) for w = exp(x - m) in [0, 1], from the float's exponent and
-// mantissa with integer shifts (no 64-bit conversion); -inf weights give 0.
-__device__ __forceinline__ unsigned long long fix40(float x, float m) {
-    const float w = hw_ex2(__fmul_rn(__fsub_rn(x, m), kLog2e));
+// w = exp(x - m) as the hardware ex2 of (x - m) * log2(e); -inf gives 0.
+__device__ __forceinline__ float exp_rel(float x, float m) { return hw_ex2(__fmul_rn(__fsub_rn(x, m), kLog2e)); }
+
+// floor(w * 2^40) for w in [0, 1], from the float's exponent and mantissa
+// with integer shifts (no 64-bit conversion).
+__device__ __forceinline__ unsigned long long fix40w(float w) {
     const unsigned bits = __float_as_uint(w);
     const int sh = static_cast<int>(bits >> 23) - 110;  // w * 2^40 = mant * 2^(e - 150 + 40)
     const unsigned long long mant = (bits & 0x7fffffu) | 0x800000u;
@@ -138,9 +159,10 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
     __shared__ float s_rmax;
     __shared__ unsigned long long s_rq[2];  // the row's total; the segments' before this one
     __shared__ unsigned long long s_off[kWarps + 1];
-    __shared__ __align__(16) int s_stage[kChunk];  // one block of outputs: run starts, then filled
-    __shared__ int s_wmax[kWarps];
-    __shared__ int s_range[2];                      // the chunk's outputs [j_lo, j_hi)
+    __shared__ __align__(16) int s_stage[kChunk];  // one block of outputs (per warp: kWarpBlock of them): run starts, then filled
+    __shared__ int s_wmax[kWarps];                  // resample step only: the block-wide max-scan
+    __shared__ int s_range[2];                      // resample step only: the chunk's outputs [j_lo, j_hi)
+    extern __shared__ __align__(16) float s_seg[];  // the staged segment (kStageMax floats when R.staged)
     cg::cluster_group cluster = cg::this_cluster();
     const int K = static_cast<int>(cluster.num_blocks()), k = static_cast<int>(cluster.block_rank());
     const int b = blockIdx.x / K;
@@ -158,6 +180,11 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
         for (int u = 0; u < kBatch; ++u) {
             const int i = i0 + u * kThreads * 4;
             q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+        if (R.staged) {  // the whole segment, -inf past its end (one iteration)
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                *reinterpret_cast<float4*>(s_seg + (i0 - s0) + u * kThreads * 4) = q[u];
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) m = fmaxf(m, fmaxf(fmaxf(q[u].x, q[u].y), fmaxf(q[u].z, q[u].w)));
@@ -188,11 +215,18 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int i = i0 + u * kThreads * 4;
-            q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (R.staged)  // this thread's own pass-1 stores
+                q[u] = *reinterpret_cast<const float4*>(s_seg + (i0 - s0) + u * kThreads * 4);
+            else
+                q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            acc += fix40(q[u].x, rmax) + fix40(q[u].y, rmax) + fix40(q[u].z, rmax) + fix40(q[u].w, rmax);
+        for (int u = 0; u < kBatch; ++u) {
+            const float4 w = make_float4(exp_rel(q[u].x, rmax), exp_rel(q[u].y, rmax), exp_rel(q[u].z, rmax),
+                                         exp_rel(q[u].w, rmax));
+            if (R.staged) *reinterpret_cast<float4*>(s_seg + (i0 - s0) + u * kThreads * 4) = w;
+            acc += fix40w(w.x) + fix40w(w.y) + fix40w(w.z) + fix40w(w.w);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(PER_FULL_MASK, acc, o);
@@ -227,34 +261,43 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
     const float U = R.u_rows ? R.u_rows[b] : u01_closed_open(R.seed, R.offset + static_cast<uint64_t>(b));
 
     // ---- 3: scan, then the outputs of each chunk ----------------------------------
-    // the next chunk's loads are issued before the current chunk is processed
+    // unstaged: the next chunk's loads are issued before the current chunk is
+    // processed; staged: w comes from shared memory (written before the
+    // barriers above)
     float4 nxt[kLane / 4];
 #pragma unroll
     for (int h = 0; h < kLane / 4; ++h) {
         const int i = s0 + threadIdx.x * kLane + 4 * h;
-        nxt[h] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        nxt[h] = !R.staged && i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
     unsigned long long carry = s_rq[1];  // the exact total of the segments before this one
     for (int c0 = s0; c0 < s1; c0 += kChunk) {
         const int i0 = c0 + threadIdx.x * kLane;
         float4 cur[kLane / 4];
+        if (R.staged) {
 #pragma unroll
-        for (int h = 0; h < kLane / 4; ++h) {
-            cur[h] = nxt[h];
-            const int i = i0 + kChunk + 4 * h;
-            nxt[h] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            for (int h = 0; h < kLane / 4; ++h)
+                cur[h] = *reinterpret_cast<const float4*>(s_seg + (i0 - s0) + 4 * h);
+        } else {
+#pragma unroll
+            for (int h = 0; h < kLane / 4; ++h) {
+                const float4 x = nxt[h];
+                cur[h] = make_float4(exp_rel(x.x, rmax), exp_rel(x.y, rmax), exp_rel(x.z, rmax), exp_rel(x.w, rmax));
+                const int i = i0 + kChunk + 4 * h;
+                nxt[h] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
         }
         unsigned long long r[kLane];
         unsigned long long run = 0ull;
 #pragma unroll
         for (int h = 0; h < kLane / 4; ++h) {
-            run += fix40(cur[h].x, rmax);
+            run += fix40w(cur[h].x);
             r[4 * h] = run;
-            run += fix40(cur[h].y, rmax);
+            run += fix40w(cur[h].y);
             r[4 * h + 1] = run;
-            run += fix40(cur[h].z, rmax);
+            run += fix40w(cur[h].z);
             r[4 * h + 2] = run;
-            run += fix40(cur[h].w, rmax);
+            run += fix40w(cur[h].w);
             r[4 * h + 3] = run;
         }
         const unsigned long long x = warp_incl_u64(run, lane);
@@ -293,98 +336,181 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
             nend[e] = n;
             prev = n;
         }
-        // the chunk's outputs [j_lo, j_hi): from its first particle's run start
-        // to its last particle's run end
-        if (threadIdx.x == 0) s_range[0] = start;
-        if (threadIdx.x == kThreads - 1) s_range[1] = c0 + kChunk >= P ? P : nend[kLane - 1];
-        __syncthreads();
-        const int j_lo = s_range[0], j_hi = s_range[1];
-        // outputs in blocks of kChunk from the chunk's first output (rounded
-        // down to 8, so that a thread's 8 outputs start 32-byte aligned): a
-        // chunk of about kChunk outputs mostly needs one block.  Each
-        // non-empty run writes its particle at its first output, and a
-        // prefix max fills every output with the particle whose run covers it
-        int started = -1;  // the last particle started in earlier blocks
-        for (int b0 = j_lo & ~(kLane - 1); b0 < j_hi; b0 += kChunk) {
-            const int t0 = threadIdx.x * kLane;  // this thread's outputs in the block: b0 + t0 .. + 7
-            *reinterpret_cast<int4*>(s_stage + t0) = make_int4(-1, -1, -1, -1);
-            *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(-1, -1, -1, -1);
+        if constexpr (STEP) {
+            // The resample step copies a state row per output, which gains
+            // from all warps copying at once: the chunk's outputs [j_lo, j_hi)
+            // -- from its first particle's run start to its last particle's
+            // run end -- go out in block-wide blocks of kChunk.
+            if (threadIdx.x == 0) s_range[0] = start;
+            if (threadIdx.x == kThreads - 1) s_range[1] = c0 + kChunk >= P ? P : nend[kLane - 1];
             __syncthreads();
-            int a = start;
-#pragma unroll
-            for (int e = 0; e < kLane; ++e) {
-                if (nend[e] > a && a >= b0 && a < b0 + kChunk) s_stage[a - b0] = i0 + e;
-                a = nend[e];
-            }
-            __syncthreads();
-            const int4 v0 = *reinterpret_cast<const int4*>(s_stage + t0);
-            const int4 v1 = *reinterpret_cast<const int4*>(s_stage + t0 + 4);
-            int v[kLane] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int e = 1; e < kLane; ++e) v[e] = max(v[e], v[e - 1]);
-            int x = v[kLane - 1];
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int y = __shfl_up_sync(PER_FULL_MASK, x, d);
-                if (lane >= d) x = max(x, y);
-            }
-            if (lane == 31) s_wmax[warp] = x;
-            int before = __shfl_up_sync(PER_FULL_MASK, x, 1);
-            if (lane == 0) before = -1;
-            __syncthreads();
-            // the maxima of the warps before this one and of all warps: one
-            // max-scan over the kWarps warp maxima (lane w holds warp w's)
-            int wm = lane < kWarps ? s_wmax[lane] : -1;
-#pragma unroll
-            for (int d = 1; d < kWarps; d <<= 1) {
-                const int y = __shfl_up_sync(PER_FULL_MASK, wm, d);
-                if (lane >= d) wm = max(wm, y);
-            }
-            const int wb_in = __shfl_sync(PER_FULL_MASK, wm, warp > 0 ? warp - 1 : 0);
-            const int wb = max(started, warp > 0 ? wb_in : -1);
-            const int all = max(started, __shfl_sync(PER_FULL_MASK, wm, kWarps - 1));
-            before = max(before, wb);
-#pragma unroll
-            for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
-            const int j0 = b0 + t0;
-            if (j0 >= j_lo && j0 + kLane <= j_hi) {  // written once: evict-first stores
-                __stcs(reinterpret_cast<int4*>(orow + j0), make_int4(v[0], v[1], v[2], v[3]));
-                __stcs(reinterpret_cast<int4*>(orow + j0 + 4), make_int4(v[4], v[5], v[6], v[7]));
-            } else {
-#pragma unroll
-                for (int e = 0; e < kLane; ++e)
-                    if (j0 + e >= j_lo && j0 + e < j_hi) orow[j0 + e] = v[e];
-            }
-            if (R.out_state) {
-                // the block's particles in shared memory, then their states
-                // copied by consecutive threads for consecutive outputs
-                // (coalesced: neighbouring outputs hold neighbouring particles).
-                // States are read and written once: evict-first loads and
-                // stores, so that they do not push the rows' log-weights,
-                // which the row's later passes read again, out of L2.
-                __syncthreads();  // every thread has read s_stage
-                *reinterpret_cast<int4*>(s_stage + t0) = make_int4(v[0], v[1], v[2], v[3]);
-                *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
+            const int j_lo = s_range[0], j_hi = s_range[1];
+            // outputs in blocks of kChunk from the chunk's first output (rounded
+            // down to 8, so that a thread's 8 outputs start 32-byte aligned): a
+            // chunk of about kChunk outputs mostly needs one block.  Each
+            // non-empty run writes its particle at its first output, and a
+            // prefix max fills every output with the particle whose run covers it
+            int started = -1;  // the last particle started in earlier blocks
+            for (int b0 = j_lo & ~(kLane - 1); b0 < j_hi; b0 += kChunk) {
+                const int t0 = threadIdx.x * kLane;  // this thread's outputs in the block: b0 + t0 .. + 7
+                *reinterpret_cast<int4*>(s_stage + t0) = make_int4(-1, -1, -1, -1);
+                *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(-1, -1, -1, -1);
                 __syncthreads();
-                const int D = R.D;
-                const float* srow = R.state + static_cast<size_t>(b) * P * D;
-                float* drow = R.out_state + static_cast<size_t>(b) * P * D;
-                for (int t = threadIdx.x; t < kChunk; t += kThreads) {
-                    const int j = b0 + t;
-                    if (j < j_lo || j >= j_hi) continue;
-                    const int i = s_stage[t];
-                    if ((D & 3) == 0) {
-                        for (int d = 0; d < D; d += 4)
-                            __stcs(reinterpret_cast<float4*>(drow + static_cast<size_t>(j) * D + d),
-                                   __ldcs(reinterpret_cast<const float4*>(srow + static_cast<size_t>(i) * D + d)));
-                    } else {
-                        for (int d = 0; d < D; ++d)
-                            __stcs(drow + static_cast<size_t>(j) * D + d, __ldcs(srow + static_cast<size_t>(i) * D + d));
+                int a = start;
+    #pragma unroll
+                for (int e = 0; e < kLane; ++e) {
+                    if (nend[e] > a && a >= b0 && a < b0 + kChunk) s_stage[a - b0] = i0 + e;
+                    a = nend[e];
+                }
+                __syncthreads();
+                const int4 v0 = *reinterpret_cast<const int4*>(s_stage + t0);
+                const int4 v1 = *reinterpret_cast<const int4*>(s_stage + t0 + 4);
+                int v[kLane] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    #pragma unroll
+                for (int e = 1; e < kLane; ++e) v[e] = max(v[e], v[e - 1]);
+                int x = v[kLane - 1];
+    #pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(PER_FULL_MASK, x, d);
+                    if (lane >= d) x = max(x, y);
+                }
+                if (lane == 31) s_wmax[warp] = x;
+                int before = __shfl_up_sync(PER_FULL_MASK, x, 1);
+                if (lane == 0) before = -1;
+                __syncthreads();
+                // the maxima of the warps before this one and of all warps: one
+                // max-scan over the kWarps warp maxima (lane w holds warp w's)
+                int wm = lane < kWarps ? s_wmax[lane] : -1;
+    #pragma unroll
+                for (int d = 1; d < kWarps; d <<= 1) {
+                    const int y = __shfl_up_sync(PER_FULL_MASK, wm, d);
+                    if (lane >= d) wm = max(wm, y);
+                }
+                const int wb_in = __shfl_sync(PER_FULL_MASK, wm, warp > 0 ? warp - 1 : 0);
+                const int wb = max(started, warp > 0 ? wb_in : -1);
+                const int all = max(started, __shfl_sync(PER_FULL_MASK, wm, kWarps - 1));
+                before = max(before, wb);
+    #pragma unroll
+                for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
+                const int j0 = b0 + t0;
+                if (j0 >= j_lo && j0 + kLane <= j_hi) {  // written once: evict-first stores
+                    __stcs(reinterpret_cast<int4*>(orow + j0), make_int4(v[0], v[1], v[2], v[3]));
+                    __stcs(reinterpret_cast<int4*>(orow + j0 + 4), make_int4(v[4], v[5], v[6], v[7]));
+                } else {
+    #pragma unroll
+                    for (int e = 0; e < kLane; ++e)
+                        if (j0 + e >= j_lo && j0 + e < j_hi) orow[j0 + e] = v[e];
+                }
+                if (R.out_state) {
+                    // the block's particles in shared memory, then their states
+                    // copied by consecutive threads for consecutive outputs
+                    // (coalesced: neighbouring outputs hold neighbouring particles).
+                    // States are read and written once: evict-first loads and
+                    // stores, so that they do not push the rows' log-weights,
+                    // which the row's later passes read again, out of L2.
+                    __syncthreads();  // every thread has read s_stage
+                    *reinterpret_cast<int4*>(s_stage + t0) = make_int4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
+                    __syncthreads();
+                    const int D = R.D;
+                    const float* srow = R.state + static_cast<size_t>(b) * P * D;
+                    float* drow = R.out_state + static_cast<size_t>(b) * P * D;
+                    for (int t = threadIdx.x; t < kChunk; t += kThreads) {
+                        const int j = b0 + t;
+                        if (j < j_lo || j >= j_hi) continue;
+                        const int i = s_stage[t];
+                        if ((D & 3) == 0) {
+                            for (int d = 0; d < D; d += 4)
+                                __stcs(reinterpret_cast<float4*>(drow + static_cast<size_t>(j) * D + d),
+                                       __ldcs(reinterpret_cast<const float4*>(srow + static_cast<size_t>(i) * D + d)));
+                        } else {
+                            for (int d = 0; d < D; ++d)
+                                __stcs(drow + static_cast<size_t>(j) * D + d, __ldcs(srow + static_cast<size_t>(i) * D + d));
+                        }
                     }
                 }
+                started = all;
+                __syncthreads();  // s_stage and s_wmax are reused by the next block
             }
-            started = all;
-            __syncthreads();  // s_stage and s_wmax are reused by the next block
+        } else {
+            // the warp's outputs [w_lo, w_hi): from its first particle's run start
+            // to its last particle's run end.  They are written in blocks of 256
+            // from w_lo rounded down to 8 (so that a lane's 8 outputs start
+            // 32-byte aligned; a warp's ~256 outputs mostly need one block): each
+            // non-empty run puts its particle at its first output in the warp's
+            // staging row, and a warp prefix max fills every output with the
+            // particle whose run covers it.  Only the warp synchronises.
+            const int w_lo = __shfl_sync(PER_FULL_MASK, start, 0);
+            const int w_hi = __shfl_sync(PER_FULL_MASK, nend[kLane - 1], 31);
+            int* stage = s_stage + warp * kWarpBlock;
+            const int t0 = lane * kLane;  // this lane's outputs in a block: b0 + t0 .. + 7
+            int started = -1;             // the last particle started in earlier blocks
+            for (int b0 = w_lo & ~(kLane - 1); b0 < w_hi; b0 += kWarpBlock) {
+                *reinterpret_cast<int4*>(stage + t0) = make_int4(-1, -1, -1, -1);
+                *reinterpret_cast<int4*>(stage + t0 + 4) = make_int4(-1, -1, -1, -1);
+                __syncwarp();
+                int a = start;
+    #pragma unroll
+                for (int e = 0; e < kLane; ++e) {
+                    if (nend[e] > a && a >= b0 && a < b0 + kWarpBlock) stage[a - b0] = i0 + e;
+                    a = nend[e];
+                }
+                __syncwarp();
+                const int4 v0 = *reinterpret_cast<const int4*>(stage + t0);
+                const int4 v1 = *reinterpret_cast<const int4*>(stage + t0 + 4);
+                int v[kLane] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    #pragma unroll
+                for (int e = 1; e < kLane; ++e) v[e] = max(v[e], v[e - 1]);
+                int x = v[kLane - 1];
+    #pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(PER_FULL_MASK, x, d);
+                    if (lane >= d) x = max(x, y);
+                }
+                int before = __shfl_up_sync(PER_FULL_MASK, x, 1);
+                if (lane == 0) before = -1;
+                before = max(before, started);
+                started = max(started, __shfl_sync(PER_FULL_MASK, x, 31));
+    #pragma unroll
+                for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
+                const int j0 = b0 + t0;
+                if (j0 >= w_lo && j0 + kLane <= w_hi) {  // written once: evict-first stores
+                    __stcs(reinterpret_cast<int4*>(orow + j0), make_int4(v[0], v[1], v[2], v[3]));
+                    __stcs(reinterpret_cast<int4*>(orow + j0 + 4), make_int4(v[4], v[5], v[6], v[7]));
+                } else {
+    #pragma unroll
+                    for (int e = 0; e < kLane; ++e)
+                        if (j0 + e >= w_lo && j0 + e < w_hi) orow[j0 + e] = v[e];
+                }
+                if (R.out_state) {
+                    // the block's particles in the staging row, then their states
+                    // copied by consecutive lanes for consecutive outputs
+                    // (coalesced: neighbouring outputs hold neighbouring particles).
+                    // States are read and written once: evict-first loads and
+                    // stores, so that they do not push the rows' log-weights,
+                    // which the row's later passes read again, out of L2.
+                    __syncwarp();  // every lane has read the staging row
+                    *reinterpret_cast<int4*>(stage + t0) = make_int4(v[0], v[1], v[2], v[3]);
+                    *reinterpret_cast<int4*>(stage + t0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
+                    __syncwarp();
+                    const int D = R.D;
+                    const float* srow = R.state + static_cast<size_t>(b) * P * D;
+                    float* drow = R.out_state + static_cast<size_t>(b) * P * D;
+                    const int j_end = min(b0 + kWarpBlock, w_hi);
+                    for (int j = max(b0, w_lo) + lane; j < j_end; j += 32) {
+                        const int i = stage[j - b0];
+                        if ((D & 3) == 0) {
+                            for (int d = 0; d < D; d += 4)
+                                __stcs(reinterpret_cast<float4*>(drow + static_cast<size_t>(j) * D + d),
+                                       __ldcs(reinterpret_cast<const float4*>(srow + static_cast<size_t>(i) * D + d)));
+                        } else {
+                            for (int d = 0; d < D; ++d)
+                                __stcs(drow + static_cast<size_t>(j) * D + d, __ldcs(srow + static_cast<size_t>(i) * D + d));
+                        }
+                    }
+                }
+                __syncwarp();  // the staging row is reused by the next block
+            }
         }
     }
     if (R.out_logw) {  // every read of the segment's log-weights is done: the reset may overwrite them
@@ -430,10 +556,21 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     const int seg_chunks = (chunks + K - 1) / K;
     K = (chunks + seg_chunks - 1) / seg_chunks;
     R.seg = seg_chunks * kChunk;
+    R.staged = !step && R.seg <= kStageMax;
+    const size_t smem = R.staged ? kStageMax * sizeof(float) : 0;
+    if (R.staged) {
+        static DeviceCache cache;
+        const int ok = device_cached(cache, [&]() {
+            return cudaFuncSetAttribute(resample_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem)) == cudaSuccess ? 1 : 2;
+        });
+        if (ok != 1) return PER_ERR_CUDA;
+    }
     if (static_cast<int64_t>(rows) * K > 0x7fffffffll) return PER_ERR_ARG;  // grid limit
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows) * static_cast<unsigned>(K));
     cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
