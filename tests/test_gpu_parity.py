@@ -79,8 +79,49 @@ def test_cdf_matches_oracle_ragged_sizes(n):
     assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
 
 
+# Inputs beyond one wave of tiles take the streaming kernel (8192-item tiles
+# by ticket, one CTA per SM): fewer tiles than CTAs, a last tile that ends
+# exactly at n (item n-1 in a full tile), last tiles of 1 item (no bulk copy)
+# and of 7 items (4 copied, 3 read directly), and several tiles per CTA.
+STREAM_SIZES = [1_400_000, 1 << 21, (1 << 21) + 1, (1 << 21) + 7, 2 * 152 * 8192 + 5, 5_000_000]
+
+
+@pytest.mark.parametrize("n", STREAM_SIZES)
+def test_cdf_streaming_path_ragged(n):
+    p = workloads.abs_normal(n, workloads.rng(104, n))
+    ctx, c = gpu_cdf(p, 0.6)
+    C = oracle.cdf64(p, 0.6)
+    assert np.all(np.diff(c) >= 0)
+    assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
+    assert per.per_total_host(ctx.handle, SCAN) == c[-1]
+
+
+@pytest.mark.parametrize("alpha", [0.0, 1.0])
+def test_cdf_streaming_path_exact_modes(alpha):
+    # alpha = 0 counts items (0^0 = 1); alpha = 1 on small integers is exact
+    n = (1 << 21) + 3
+    p = workloads.rng(105).integers(0, 5, size=n).astype(np.float32)  # total < 2^24
+    _, c = gpu_cdf(p, alpha)
+    want = np.arange(1, n + 1) if alpha == 0.0 else np.cumsum(p.astype(np.int64))
+    assert np.array_equal(c, want.astype(np.float32))
+
+
+def test_cdf_streaming_path_reports_negative_priority():
+    # alpha = 1: the slice sums stay finite, so only PER_ERR_VALUE is recorded
+    # (with a fractional alpha the power of -1 is NaN and the range check
+    # fires first)
+    p = np.ones((1 << 21) + 5, np.float32)
+    p[1_234_567] = -1.0
+    ctx = make_ctx(p, 1.0, SCAN)
+    per.per_build_cdf(ctx.handle)
+    assert per.per_check(ctx.handle) == 8  # PER_ERR_VALUE
+    per.per_set_priorities(ctx.handle, dev(np.abs(p)))
+    per.per_build_cdf(ctx.handle)
+    assert per.per_check(ctx.handle) == 0
+
+
 def test_cdf_large_tile_path_ragged():
-    # above ~2.5M items the 4096-item tile variant runs; ragged tail included
+    # lognormal priorities through the streaming kernel; ragged tail included
     n = 3 * 1024 * 1024 + 12345
     p = workloads.lognormal(n, workloads.rng(101), 1.0)
     _, c = gpu_cdf(p, 0.7)
