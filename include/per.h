@@ -127,9 +127,13 @@ per_status per_update(per_ctx* ctx, const int32_t* d_idx, const float* d_prio, i
  * per_build_cdf -- PR #615 "Parallel build_cdf": cdf[i] = sum_{j<=i} p_j^alpha
  * over the n valid items, as one single-pass decoupled-lookback scan with
  * p^alpha fused into the load.  The result is monotone non-decreasing and
- * bit-reproducible (tile carries are summed exactly in 128-bit fixed point;
- * each tile's sum of p^alpha must stay below 2^44, else PER_ERR_RANGE is
- * recorded).  Requires PER_SCAN and n >= 1.  The CDF is read through
+ * bit-reproducible (tile carries are summed exactly in 128-bit fixed point
+ * with 60 fractional bits; each tile's sum of p^alpha must stay below 2^44,
+ * else PER_ERR_RANGE is recorded, and a unit sum -- a tile's, or a 512-item
+ * slice's in the streaming scan of large inputs -- is truncated to a
+ * multiple of 2^-60 in the carries, so a unit whose sum is below 2^-60 adds
+ * nothing to the items after it and its own values are clamped to the
+ * carry before it).  Requires PER_SCAN and n >= 1.  The CDF is read through
  * per_cdf_ptr(); cdf[n-1] is the total.
  */
 per_status per_build_cdf(per_ctx* ctx, void* stream);

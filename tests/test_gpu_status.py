@@ -172,3 +172,50 @@ def test_drop_of_a_tile_the_call_does_not_have_changes_nothing():
     check_cdf(ctx, p, 0.6)
     with pytest.raises(per.PerError):
         per.per_debug_drop_tile(ctx.handle, -2)
+
+
+# --------------------------------------------------- exact-carry range ------
+# Carries are 128-bit fixed point with 60 fractional bits: a unit sum (the
+# fp32 sum of a one-wave tile, or of a 512-item slice of the streaming scan)
+# must stay below 2^44, else PER_ERR_RANGE; unit sums below 2^-60 do not reach
+# the carries, so such units are clamped to the carry before them.
+ERR_RANGE = 7
+
+
+@pytest.mark.parametrize("n", [4096, (1 << 21) + 5], ids=["one-wave", "streaming"])
+def test_unit_sum_at_2_44_records_range_error(n):
+    p = np.ones(n, np.float32)
+    p[512:1024] = 2.0 ** 35  # one 512-item block: a unit sum of 2^44 in either kernel
+    ctx = new_ctx(p, 1.0, SCAN)
+    per.per_build_cdf(ctx.handle)
+    assert per.per_check(ctx.handle) == ERR_RANGE
+    assert per.per_check(ctx.handle) == 0  # read and cleared
+    # just below the bound: no error, and the CDF within the usual tolerance
+    p[512:1024] = np.float32(2.0 ** 35 * (1 - 2.0 ** -20))
+    per.per_set_priorities(ctx.handle, dev(p))
+    per.per_build_cdf(ctx.handle)
+    assert per.per_check(ctx.handle) == 0
+    check_cdf(ctx, p, 1.0)
+
+
+@pytest.mark.parametrize("n", [5000, (1 << 21) + 5], ids=["one-wave", "streaming"])
+def test_unit_sums_below_2_minus_60_vanish_from_the_carries(n):
+    # 2^-75: a 2048-item tile or a 512-item slice sums to at most 2^-64
+    tiny = np.float32(2.0 ** -75)
+    # only tiny values: every unit sum is below 2^-60, so the CDF is 0
+    ctx = new_ctx(np.full(n, tiny, np.float32), 1.0, SCAN)
+    per.per_build_cdf(ctx.handle)
+    assert per.per_check(ctx.handle) == 0
+    c = host(per.read_cdf(ctx.handle))[:n]
+    assert np.all(c == 0.0)
+    assert per.per_total_host(ctx.handle, SCAN) == 0.0
+    # one unit item first: the tiny tail stays at 1.0, which is also the fp32
+    # rounding of the exact prefix sums (1 + k 2^-75)
+    p = np.full(n, tiny, np.float32)
+    p[0] = 1.0
+    per.per_set_priorities(ctx.handle, dev(p))
+    per.per_build_cdf(ctx.handle)
+    assert per.per_check(ctx.handle) == 0
+    c = host(per.read_cdf(ctx.handle))[:n]
+    assert np.all(c == 1.0)
+    assert np.array_equal(c, oracle.cdf64(p, 1.0).astype(np.float32))
