@@ -604,6 +604,10 @@ def measure_configs(per, torch, dev, peak, peak_kind, flush, head):
     g_scan = graph_of(torch, lambda: per.per_build_cdf(ctx.handle))
     us_scan = time_graph(torch, g_scan, 30, flush.clean)
     us_scan_dirty = time_graph(torch, g_scan, 30, flush.dirty)
+    # without a flush: 20 calls back to back in one graph (whatever of the
+    # 128 MB working set the 126 MB L2 keeps between calls)
+    us_scan_warm = time_graph(torch, graph_of(torch, lambda: [per.per_build_cdf(ctx.handle) for _ in range(20)]),
+                              15, None, per_replay=20)
     i_st = torch.empty(b, dtype=torch.int32, device=dev)
     per.per_sample(ctx.handle, b, 1, 0, per.PER_SCAN, i_st)
     us_samp = time_graph(torch, graph_of(torch, lambda: per.per_sample(ctx.handle, b, 1, 0, per.PER_SCAN, i_st)),
@@ -621,6 +625,7 @@ def measure_configs(per, torch, dev, peak, peak_kind, flush, head):
         "workload": f"N={n} fp32 uniform(0,1], alpha={S['alpha']} (and 1.0); build_cdf + sample {b} stratified",
         "build_cdf_us": round(us_scan, 2), "build_cdf_us_alpha1": round(us_scan1, 2),
         "build_cdf_us_after_write_only_flush": round(us_scan_dirty, 2),
+        "build_cdf_us_no_flush_back_to_back": round(us_scan_warm, 2),
         "build_cdf_gbs": round(8 * n / (us_scan * 1e-6) / 1e9, 1),
         "build_cdf_frac_of_nominal_8tbs": round(8 * n / (us_scan * 1e-6) / 1e9 / 8000.0, 4),
         "target_frac_of_hbm": 0.70,
@@ -630,7 +635,8 @@ def measure_configs(per, torch, dev, peak, peak_kind, flush, head):
         "roofline": roofline("build_cdf_stream_kernel", 8 * n, us_scan, peak, peak_kind,
                              traffic_for("build_cdf_stress")),
         "l2": "flushed before each rep (512 MiB write + 512 MiB read of other buffers); build_cdf also after a "
-              "write-only flush, whose dirty lines are written back inside the timed call"}
+              "write-only flush, whose dirty lines are written back inside the timed call, and without a flush "
+              "(20 calls back to back per graph replay)"}
 
     # ---- resample: 256 rows x 65536 log-weights N(0, 2^2)
     R = workloads.RESAMPLE
