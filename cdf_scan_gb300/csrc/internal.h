@@ -90,7 +90,7 @@ constexpr int kCoarseStride = 64;
 // exact 128-bit sum as four tagged 32-bit pieces) alone in a 128-byte line
 // (kRecStride words), for up to scan_rec_tiles(n) tiles.
 constexpr int kScanMaxGrid = 1024;
-constexpr int kStreamTile = 8192;
+constexpr int kStreamTile = 16384;
 constexpr int kRecWords = 4;
 constexpr int kRecStride = 16;
 inline int64_t scan_rec_tiles(int64_t n) { return (n + kStreamTile - 1) / kStreamTile + 1; }

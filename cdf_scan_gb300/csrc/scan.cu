@@ -43,30 +43,30 @@ __device__ __forceinline__ void load_tile(const ScanParams& P, unsigned t, float
 // ---- the streaming scan: one pass by persistent CTAs ------------------------
 //
 // For inputs larger than one wave of tiles.  One CTA per SM (co-resident,
-// cooperative launch) takes 8192-item tiles (kStreamTile: sixteen 512-item
-// slices, one per compute warp) in ticket order from a global counter, so an
+// cooperative launch) takes 16384-item tiles (kStreamTile: 32 slices of 512
+// items, two per compute warp) in ticket order from a global counter, so an
 // SM that gets less memory bandwidth simply takes fewer tiles.  The slice is
 // the unit of the exact carries.  Four roles per CTA, all on the CTA's own
 // sequence of tiles k = 0, 1, ...:
 //   producer warp: draws tile t_k = ticket++ and streams it into stage
 //     k mod STAGES of a ring of 1-D bulk copies (TMA) on mbarriers; once the
 //     tickets run out it records how many tiles the CTA got;
-//   16 compute warps, one slice each: the local phase of tile k -- the
-//     slice's p^alpha (the stage goes back to the producer as soon as it has
-//     been read), its fp32 sum (a fixed order), then its local inclusive
-//     scan, which waits in tensor memory (TMEM, 256 KB per SM, otherwise
-//     unused here: room for NX tiles) -- and then the emit phase of tile
-//     k - LAG, whose exclusive prefix has been found meanwhile: the local
-//     scan back from TMEM, written out once with the slice's carry
+//   16 compute warps, two slices each: the local phase of tile k -- per
+//     slice its p^alpha (the stage goes back to the producer as soon as both
+//     have been read), its fp32 sum (a fixed order), then its local
+//     inclusive scan, which waits in tensor memory (TMEM, 256 KB per SM,
+//     otherwise unused here: room for NX tiles) -- and then the emit phase
+//     of tile k - LAG, whose exclusive prefix has been found meanwhile: the
+//     local scans back from TMEM, written out once with each slice's carry
 //     (hi, lo, fl32(E), fl32(E')) added;
 //   publisher warp: the exact 128-bit fixed-point sums of the tile's slices,
 //     their exclusive prefixes within the tile, and the tile's total in its
 //     record, tagged "aggregate";
-//   four lookback warps, taking the CTA's tiles in turn: the tile's exclusive
+//   two lookback warps, taking the CTA's tiles in turn: the tile's exclusive
 //     prefix E from the records of the tiles before it -- the nearest one
 //     tagged "inclusive" plus the aggregates after it (a decoupled
 //     lookback) -- then E + the tile's total into its record, tagged
-//     "inclusive", and the sixteen slice carries.
+//     "inclusive", and the 32 slice carries.
 // A record is four 64-bit words, 32 payload bits each under a 32-bit tag
 // (call epoch << 1 | inclusive), one 32-byte store, alone in a 128-byte line;
 // a reader takes it only when all four tags agree.  All sums are exact
@@ -256,16 +256,19 @@ __device__ __forceinline__ u128 warp_scan_u128(u128 v, int lane) {
 }
 
 
-// Ring stages, the lag (tiles) between a tile's local phase and its emit
-// phase, and the ring of per-tile exchange state and TMEM slots (more than
-// LAG) of the streaming kernel.  The lag covers the latency of a lookback
-// (the records of the tiles before it appear over a few microseconds), four
-// lookback warps its throughput.
-constexpr int kStreamStages = 4;
-constexpr int kStreamLag = 6;
-constexpr int kStreamXring = 8;
-constexpr int kStreamWarps = kStreamTile / 512;  // compute warps, one slice each
-constexpr int kStreamLookback = 4;               // lookback warps
+// Ring stages (3 x 64 KiB), the lag (tiles) between a tile's local phase and
+// its emit phase, and the ring of per-tile exchange state and TMEM slots
+// (more than LAG) of the streaming kernel.  The lag covers the latency of a
+// lookback (the records of the tiles before it appear over a few
+// microseconds), two lookback warps its throughput.  Larger tiles mean fewer
+// records, lookbacks and per-tile handshakes per item.
+constexpr int kStreamStages = 3;
+constexpr int kStreamLag = 3;
+constexpr int kStreamXring = 4;
+constexpr int kStreamSlices = kStreamTile / 512;      // 512-item slices per tile
+constexpr int kStreamSpw = 2;                          // slices per compute warp
+constexpr int kStreamWarps = kStreamSlices / kStreamSpw;  // compute warps
+constexpr int kStreamLookback = 2;               // lookback warps
 constexpr int kStreamThreads = (kStreamWarps + 2 + kStreamLookback) * 32;
 // Records per lane per poll of a lookback: a window of 160 tiles, which
 // reaches the CTA's previous tile (about one tile per CTA back).
@@ -376,9 +379,10 @@ __device__ __forceinline__ u128 lookback(const ScanParams& P, int64_t t, unsigne
 // ---- tensor memory (TMEM) as the lag buffer ----------------------------------
 // TMEM is 128 lanes x 512 columns of 32 bits per SM; a warp reaches only the
 // 32 lanes of its quarter (warp index mod 4).  Compute warp w keeps the 16
-// p^alpha values of each of its lanes of tile k in columns
-// (k mod NX) * 64 + (w / 4) * 16 .. + 15 of lanes 32 (w mod 4) + lane:
-// 16 warps x 16 columns per tile, NX = 8 tiles = all 512 columns.
+// local-scan values of each of its lanes for its slice h (h < 2) of tile k
+// in columns (k mod NX) * 128 + (w / 4) * 32 + h * 16 .. + 15 of lanes
+// 32 (w mod 4) + lane: 32 slices x 16 columns per tile in 4 lane quarters,
+// NX = 4 tiles = all 512 columns.
 constexpr unsigned kTmemCols = 512;
 
 __device__ __forceinline__ void tmem_alloc(unsigned* s_addr) {  // whole warp
@@ -424,25 +428,28 @@ __device__ __forceinline__ void tmem_load16(unsigned taddr, float (&v)[16]) {
     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
 }
 
-// 24 warps: six per SM sub-partition, whose register file (16,384) holds six
-// warps of 80 registers.
-__global__ void __maxnreg__(80) build_cdf_stream_kernel(ScanParams P) {
+// 20 warps: five per SM sub-partition, whose register file (16,384) holds
+// five warps of 96 registers.
+__global__ void __maxnreg__(96) build_cdf_stream_kernel(ScanParams P) {
     constexpr int STAGES = kStreamStages, LAG = kStreamLag, NX = kStreamXring;
-    constexpr int WARPS = kStreamWarps;  // compute warps, one 512-item slice each
-    constexpr int TILE = kStreamTile;    // WARPS slices x 32 lanes x 16 items
+    constexpr int SLICES = kStreamSlices, SPW = kStreamSpw;
+    constexpr int WARPS = kStreamWarps;  // compute warps, SPW 512-item slices each
+    constexpr int TILE = kStreamTile;    // SLICES slices x 32 lanes x 16 items
     constexpr int PRODUCER = WARPS, PUBLISHER = WARPS + 1, LOOKBACK0 = WARPS + 2;
-    static_assert(TILE == WARPS * 32 * 16 && WARPS <= 32, "16 items per lane, a slice per lane of the publisher");
+    constexpr int SLOT = SLICES * 4;     // TMEM columns per tile (16 per slice, 4 lane quarters)
+    static_assert(TILE == SLICES * 512 && SLICES == WARPS * SPW && SLICES <= 32 && WARPS % 4 == 0,
+                  "16 items per lane, a slice per lane of the publisher");
     static_assert(NX > LAG, "exchange / TMEM slots for the lagged tiles, plus the one in its sum phase");
-    static_assert(NX * WARPS * 16 == 4 * kTmemCols, "TMEM: 16 columns per warp per tile, 4 warps per lane quarter");
+    static_assert(NX * SLOT == kTmemCols, "TMEM: NX tile slots");
     extern __shared__ __align__(128) float s_buf[];  // STAGES x TILE
     __shared__ __align__(8) uint64_t s_full[STAGES], s_empty[STAGES], s_sums[NX], s_pub[NX], s_carried[NX];
     __shared__ int64_t s_tile[STAGES];          // tile of each stage
     __shared__ int64_t s_xtile[NX];             // tile of each exchange slot (CTA tile k: slot k % NX),
                                                 // for the publisher and lookback warps
-    __shared__ float s_sum[NX * WARPS];         // slice sums
-    __shared__ ulonglong2 s_pre[NX * WARPS];    // their exact exclusive prefixes within the tile
+    __shared__ float s_sum[NX * SLICES];        // slice sums
+    __shared__ ulonglong2 s_pre[NX * SLICES];   // their exact exclusive prefixes within the tile
     __shared__ ulonglong2 s_agg[NX];            // the tile's exact total
-    __shared__ float4 s_carry[NX * WARPS];      // slice carries (hi, lo, fl32(E), fl32(E'))
+    __shared__ float4 s_carry[NX * SLICES];     // slice carries (hi, lo, fl32(E), fl32(E'))
     __shared__ unsigned s_tmem;                 // TMEM base address
     __shared__ volatile int s_abort;            // a wait ran out: nobody waits any more
     __shared__ volatile int s_count;            // tiles this CTA got (known once the tickets run out)
@@ -515,16 +522,16 @@ __global__ void __maxnreg__(80) build_cdf_stream_kernel(ScanParams P) {
             const int st = k % NX;
             if (!wait_w(&s_sums[st], static_cast<unsigned>(k / NX) & 1u, k)) break;
             bool range_err = false;
-            const u128 f = lane < WARPS ? to_fixed(s_sum[st * WARPS + lane], range_err) : 0;
+            const u128 f = lane < SLICES ? to_fixed(s_sum[st * SLICES + lane], range_err) : 0;
             if (range_err) atomicOr(P.status, ST_RANGE);
             const u128 incl = warp_scan_u128(f, lane);
-            if (lane < WARPS) {
+            if (lane < SLICES) {
                 const u128 ex = incl - f;
-                s_pre[st * WARPS + lane] = make_ulonglong2(static_cast<unsigned long long>(ex),
+                s_pre[st * SLICES + lane] = make_ulonglong2(static_cast<unsigned long long>(ex),
                                                            static_cast<unsigned long long>(ex >> 64));
             }
-            const uint64_t tlo = __shfl_sync(PER_FULL_MASK, static_cast<uint64_t>(incl), WARPS - 1);
-            const uint64_t thi = __shfl_sync(PER_FULL_MASK, static_cast<uint64_t>(incl >> 64), WARPS - 1);
+            const uint64_t tlo = __shfl_sync(PER_FULL_MASK, static_cast<uint64_t>(incl), SLICES - 1);
+            const uint64_t thi = __shfl_sync(PER_FULL_MASK, static_cast<uint64_t>(incl >> 64), SLICES - 1);
             const u128 agg = (static_cast<u128>(thi) << 64) | tlo;
             const int64_t t = s_xtile[st];
             __syncwarp();
@@ -546,30 +553,31 @@ __global__ void __maxnreg__(80) build_cdf_stream_kernel(ScanParams P) {
                 publish_record(P, t, tag_inclusive(epoch), E + ((static_cast<u128>(a.y) << 64) | a.x));
             // carries of the sixteen slices, lane w for slice w: E_w = E + the
             // slices before w; E_w' = E_w + slice w's sum
-            if (lane < WARPS) {
-                const ulonglong2 ep = s_pre[st * WARPS + lane];
+            if (lane < SLICES) {
+                const ulonglong2 ep = s_pre[st * SLICES + lane];
                 const u128 Ew = E + ((static_cast<u128>(ep.y) << 64) | ep.x);
                 bool unused = false;
-                const u128 En = Ew + to_fixed(s_sum[st * WARPS + lane], unused);
+                const u128 En = Ew + to_fixed(s_sum[st * SLICES + lane], unused);
                 float hi, lo;
                 fixed_to_float2(Ew, hi, lo);
-                s_carry[st * WARPS + lane] = make_float4(hi, lo, hi, fixed_to_float(En));
+                s_carry[st * SLICES + lane] = make_float4(hi, lo, hi, fixed_to_float(En));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_carried[st]);
         }
     } else {
         // ======================= compute warps ================================
-        const int ibase = warp * 512 + lane * 8;  // this lane's first item of run 0
-        // this warp's TMEM columns of slot 0 (lanes of its quarter)
-        const unsigned tbase = s_tmem + (static_cast<unsigned>(32 * (warp & 3)) << 16) + static_cast<unsigned>((warp >> 2) * 16);
+        // this warp's slices: warp + WARPS h (h < SPW); its TMEM columns of
+        // slot 0 (lanes of its quarter), 16 per slice
+        const unsigned tbase = s_tmem + (static_cast<unsigned>(32 * (warp & 3)) << 16) +
+                               static_cast<unsigned>((warp >> 2) * 16 * SPW);
         bool bad = false;
         int k_end = 0x7fffffff;  // the CTA's tile count, once its local phases ran out
         // tile of exchange slot x in lane x (slot k % NX holds CTA tile k until
         // this warp has written it)
         int64_t ring_tile = 0;
         for (int k = 0; k - LAG < k_end && !aborted_w(); ++k) {
-            // ---- local phase of tile k: p^alpha, the slice's sum, its local scan to TMEM
+            // ---- local phase of tile k: per slice p^alpha, the sum, the local scan to TMEM
             if (k < k_end) {
                 const int st = k % STAGES, x = k % NX;
                 if (!wait_w(&s_full[st], static_cast<unsigned>(k / STAGES) & 1u, k)) {
@@ -579,60 +587,72 @@ __global__ void __maxnreg__(80) build_cdf_stream_kernel(ScanParams P) {
                     const int64_t tile_base = t * TILE;
                     const int valid = static_cast<int>(P.n - tile_base < TILE ? P.n - tile_base : TILE);
                     const float* buf = s_buf + st * TILE;
-                    float v[16];
-                    float sum = 0.f;
-                    if (valid == TILE && P.pow_mode != 2) {
-                        // full tile: the slice's values at once, one range test;
-                        // the sum in two interleaved chains, then their sum
-                        slice_values<16>(P, buf, ibase, v, bad);
-                        unsigned long long acc = f2_pack(v[0], v[1]);
-#pragma unroll
-                        for (int e = 2; e < 16; e += 2) acc = f2_add(acc, f2_pack(v[e], v[e + 1]));
-                        float a0, a1;
-                        f2_unpack(acc, a0, a1);
-                        sum = a0 + a1;
-                    } else {
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            float(&u)[8] = *reinterpret_cast<float(*)[8]>(v + 8 * r);
-                            run_values<TILE>(P, buf, tile_base, valid, ibase + r * 256, u, bad);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) sum += u[e];
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_empty[st]);  // the stage has been read
-#pragma unroll
-                    for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(PER_FULL_MASK, sum, d);
-                    if (lane == 0) {
-                        s_sum[x * WARPS + warp] = sum;
-                        if (warp == 0) s_xtile[x] = t;
-                    }
+                    if (warp == 0 && lane == 0) s_xtile[x] = t;
                     if (lane == x) ring_tile = t;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_sums[x]);
-                    // the slice's local scan while its carry is being found
-                    scan_pair(*reinterpret_cast<float(*)[8]>(v), *reinterpret_cast<float(*)[8]>(v + 8), lane);
-                    tmem_store16(tbase + static_cast<unsigned>(x * 64), v);
+#pragma unroll 1
+                    for (int h = 0; h < SPW; ++h) {
+                        const int slice = warp + WARPS * h;
+                        const int ibase = slice * 512 + lane * 8;  // this lane's first item of run 0
+                        float v[16];
+                        float sum = 0.f;
+                        if (valid == TILE && P.pow_mode != 2) {
+                            // full tile: the slice's values at once, one range test;
+                            // the sum in two interleaved chains, then their sum
+                            slice_values<16>(P, buf, ibase, v, bad);
+                            unsigned long long acc = f2_pack(v[0], v[1]);
+#pragma unroll
+                            for (int e = 2; e < 16; e += 2) acc = f2_add(acc, f2_pack(v[e], v[e + 1]));
+                            float a0, a1;
+                            f2_unpack(acc, a0, a1);
+                            sum = a0 + a1;
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r) {
+                                float(&u)[8] = *reinterpret_cast<float(*)[8]>(v + 8 * r);
+                                run_values<TILE>(P, buf, tile_base, valid, ibase + r * 256, u, bad);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) sum += u[e];
+                            }
+                        }
+#pragma unroll
+                        for (int d = 16; d > 0; d >>= 1) sum += __shfl_xor_sync(PER_FULL_MASK, sum, d);
+                        if (lane == 0) s_sum[x * SLICES + slice] = sum;
+                        if (h == SPW - 1) {
+                            // the stage has been read and the warp's slice sums are in
+                            __syncwarp();
+                            if (lane == 0) {
+                                mbar_arrive(&s_empty[st]);
+                                mbar_arrive(&s_sums[x]);
+                            }
+                        }
+                        // the slice's local scan while its carry is being found
+                        scan_pair(*reinterpret_cast<float(*)[8]>(v), *reinterpret_cast<float(*)[8]>(v + 8), lane);
+                        tmem_store16(tbase + static_cast<unsigned>(x * SLOT + h * 16), v);
+                    }
                 }
             }
-            // ---- emit phase of tile k - LAG: the carry added, clamped, written once
+            // ---- emit phase of tile k - LAG: the carries added, clamped, written once
             const int ks = k - LAG;
             if (ks >= 0 && ks < k_end) {
                 const int x = ks % NX;
                 if (!wait_w(&s_carried[x], static_cast<unsigned>(ks / NX) & 1u, ks)) break;
                 const int64_t tile_base = __shfl_sync(PER_FULL_MASK, ring_tile, x) * TILE;
                 const int valid = static_cast<int>(P.n - tile_base < TILE ? P.n - tile_base : TILE);
-                const float4 cy = s_carry[x * WARPS + warp];
-                float u[16];
-                tmem_load16(tbase + static_cast<unsigned>(x * 64), u);
+#pragma unroll 1
+                for (int h = 0; h < SPW; ++h) {
+                    const int slice = warp + WARPS * h;
+                    const int ibase = slice * 512 + lane * 8;
+                    const float4 cy = s_carry[x * SLICES + slice];
+                    float u[16];
+                    tmem_load16(tbase + static_cast<unsigned>(x * SLOT + h * 16), u);
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    float(&ur)[8] = *reinterpret_cast<float(*)[8]>(u + 8 * r);
-                    if (valid == TILE && P.cdf_v8)
-                        emit_run<true, TILE>(P, ur, cy, tile_base, ibase + r * 256, TILE, lane);
-                    else
-                        emit_run<false, TILE>(P, ur, cy, tile_base, ibase + r * 256, valid, lane);
+                    for (int r = 0; r < 2; ++r) {
+                        float(&ur)[8] = *reinterpret_cast<float(*)[8]>(u + 8 * r);
+                        if (valid == TILE && P.cdf_v8)
+                            emit_run<true, TILE>(P, ur, cy, tile_base, ibase + r * 256, TILE, lane);
+                        else
+                            emit_run<false, TILE>(P, ur, cy, tile_base, ibase + r * 256, valid, lane);
+                    }
                 }
             }
         }
@@ -805,7 +825,7 @@ per_status launch_build_cdf_of(per_ctx* ctx, const float* p, int64_t n, float* c
 // output CDF and nothing is ever allocated.
 //
 // The array is part of the library image: every GPU that loads the library
-// holds it (about 400 KiB) until the process exits.  All calls on a device
+// holds it (about 260 KiB) until the process exits.  All calls on a device
 // share it and it keeps the previous call's contents: the kernels leave their
 // counters and ticket at rest for the next call even after a bounded wait
 // ran out, and their tile words and records carry a per-call tag, so nothing

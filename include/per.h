@@ -151,7 +151,7 @@ per_status per_build_cdf(per_ctx* ctx, void* stream);
  * same bit-exact result as per_build_cdf, and allocates nothing.
  *
  * Its scratch (tile sums and tile records for the lookbacks and a few
- * counters) is a fixed ~400 KiB array compiled into the library, held by
+ * counters) is a fixed ~260 KiB array compiled into the library, held by
  * every GPU that loads the library
  * until the process exits; hence n <= 16,777,216 (2^24), larger n returns
  * PER_ERR_ARG without launching.  The first call on each device performs a
@@ -325,7 +325,7 @@ per_status per_check(per_ctx* ctx, void* stream);
  * waiting, finish, and leave the context usable for the next call, whose
  * result is correct again.  That call's CDF (and samples) are unspecified.
  * Tiles of the one-wave scan are 2048 items (n <= 2^19) or 4096 items, of
- * the streaming scan 8192 items; a tile the call does not have changes
+ * the streaming scan 16384 items; a tile the call does not have changes
  * nothing.  tile = -1 cancels.  Host-side only; the injection
  * applies to one call and is then cleared.  Never needed outside tests.
  */

@@ -79,11 +79,11 @@ def test_cdf_matches_oracle_ragged_sizes(n):
     assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
 
 
-# Inputs beyond one wave of tiles take the streaming kernel (8192-item tiles
+# Inputs beyond one wave of tiles take the streaming kernel (16384-item tiles
 # by ticket, one CTA per SM): fewer tiles than CTAs, a last tile that ends
 # exactly at n (item n-1 in a full tile), last tiles of 1 item (no bulk copy)
 # and of 7 items (4 copied, 3 read directly), and several tiles per CTA.
-STREAM_SIZES = [1_400_000, 1 << 21, (1 << 21) + 1, (1 << 21) + 7, 2 * 152 * 8192 + 5, 5_000_000]
+STREAM_SIZES = [1_400_000, 1 << 21, (1 << 21) + 1, (1 << 21) + 7, 5_000_000, 4 * 152 * 16384 + 5]
 
 
 @pytest.mark.parametrize("n", STREAM_SIZES)
