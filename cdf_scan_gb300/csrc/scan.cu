@@ -400,7 +400,8 @@ __device__ __forceinline__ void tmem_fence_before() {
 __device__ __forceinline__ void tmem_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// 16 consecutive columns of this lane: store, then wait for the store.
+// 16 consecutive columns of this lane: store (asynchronous: tmem_wait_st
+// before the columns are read back).
 __device__ __forceinline__ void tmem_store16(unsigned taddr, const float (&v)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
@@ -411,8 +412,9 @@ __device__ __forceinline__ void tmem_store16(unsigned taddr, const float (&v)[16
         "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
         "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// Waits for this thread's earlier TMEM stores.
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // 16 consecutive columns of this lane: load, then wait for the load.
 __device__ __forceinline__ void tmem_load16(unsigned taddr, float (&v)[16]) {
     unsigned r[16];
@@ -577,6 +579,9 @@ __global__ void __maxnreg__(96) build_cdf_stream_kernel(ScanParams P) {
         // this warp has written it)
         int64_t ring_tile = 0;
         for (int k = 0; k - LAG < k_end && !aborted_w(); ++k) {
+            // the previous iteration's TMEM stores are complete (long since):
+            // every tile read back below was stored at least one iteration ago
+            tmem_wait_st();
             // ---- local phase of tile k: per slice p^alpha, the sum, the local scan to TMEM
             if (k < k_end) {
                 const int st = k % STAGES, x = k % NX;
@@ -656,6 +661,7 @@ __global__ void __maxnreg__(96) build_cdf_stream_kernel(ScanParams P) {
                 }
             }
         }
+        tmem_wait_st();
         if (__any_sync(PER_FULL_MASK, bad) && lane == 0) atomicOr(P.status, ST_VALUE);
     }
 
