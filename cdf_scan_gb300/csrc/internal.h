@@ -86,7 +86,7 @@ enum : int { TK_ISW = 0, TK_UPD = 1, TK_SAMPLE = 2, TK_STEP = 4, TK_RANK = 5, NU
 constexpr int kCoarseStride = 64;
 
 // Streaming scan (inputs larger than one wave): at most kScanMaxGrid CTAs,
-// 8192-item tiles, and per tile one record of kRecWords 64-bit words (an
+// 16384-item tiles, and per tile one record of kRecWords 64-bit words (an
 // exact 128-bit sum as four tagged 32-bit pieces) alone in a 128-byte line
 // (kRecStride words), for up to scan_rec_tiles(n) tiles.
 constexpr int kScanMaxGrid = 1024;
