@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 *reinterpret_cast<int4*>(s_stage + t0 + 4) = make_int4(-1, -1, -1, -1);
                 __syncthreads();
                 int a = start;
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < kLane; ++e) {
                     if (nend[e] > a && a >= b0 && a < b0 + kChunk) s_stage[a - b0] = i0 + e;
                     a = nend[e];
@@ -366,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 const int4 v0 = *reinterpret_cast<const int4*>(s_stage + t0);
                 const int4 v1 = *reinterpret_cast<const int4*>(s_stage + t0 + 4);
                 int v[kLane] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    #pragma unroll
+#pragma unroll
                 for (int e = 1; e < kLane; ++e) v[e] = max(v[e], v[e - 1]);
                 int x = v[kLane - 1];
-    #pragma unroll
+#pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
                     const int y = __shfl_up_sync(PER_FULL_MASK, x, d);
                     if (lane >= d) x = max(x, y);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 // the maxima of the warps before this one and of all warps: one
                 // max-scan over the kWarps warp maxima (lane w holds warp w's)
                 int wm = lane < kWarps ? s_wmax[lane] : -1;
-    #pragma unroll
+#pragma unroll
                 for (int d = 1; d < kWarps; d <<= 1) {
                     const int y = __shfl_up_sync(PER_FULL_MASK, wm, d);
                     if (lane >= d) wm = max(wm, y);
@@ -390,14 +390,14 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 const int wb = max(started, warp > 0 ? wb_in : -1);
                 const int all = max(started, __shfl_sync(PER_FULL_MASK, wm, kWarps - 1));
                 before = max(before, wb);
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
                 const int j0 = b0 + t0;
                 if (j0 >= j_lo && j0 + kLane <= j_hi) {  // written once: evict-first stores
                     __stcs(reinterpret_cast<int4*>(orow + j0), make_int4(v[0], v[1], v[2], v[3]));
                     __stcs(reinterpret_cast<int4*>(orow + j0 + 4), make_int4(v[4], v[5], v[6], v[7]));
                 } else {
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < kLane; ++e)
                         if (j0 + e >= j_lo && j0 + e < j_hi) orow[j0 + e] = v[e];
                 }
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 *reinterpret_cast<int4*>(stage + t0 + 4) = make_int4(-1, -1, -1, -1);
                 __syncwarp();
                 int a = start;
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < kLane; ++e) {
                     if (nend[e] > a && a >= b0 && a < b0 + kWarpBlock) stage[a - b0] = i0 + e;
                     a = nend[e];
@@ -459,10 +459,10 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 const int4 v0 = *reinterpret_cast<const int4*>(stage + t0);
                 const int4 v1 = *reinterpret_cast<const int4*>(stage + t0 + 4);
                 int v[kLane] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    #pragma unroll
+#pragma unroll
                 for (int e = 1; e < kLane; ++e) v[e] = max(v[e], v[e - 1]);
                 int x = v[kLane - 1];
-    #pragma unroll
+#pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
                     const int y = __shfl_up_sync(PER_FULL_MASK, x, d);
                     if (lane >= d) x = max(x, y);
@@ -471,43 +471,16 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
                 if (lane == 0) before = -1;
                 before = max(before, started);
                 started = max(started, __shfl_sync(PER_FULL_MASK, x, 31));
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < kLane; ++e) v[e] = max(v[e], before);
                 const int j0 = b0 + t0;
                 if (j0 >= w_lo && j0 + kLane <= w_hi) {  // written once: evict-first stores
                     __stcs(reinterpret_cast<int4*>(orow + j0), make_int4(v[0], v[1], v[2], v[3]));
                     __stcs(reinterpret_cast<int4*>(orow + j0 + 4), make_int4(v[4], v[5], v[6], v[7]));
                 } else {
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < kLane; ++e)
                         if (j0 + e >= w_lo && j0 + e < w_hi) orow[j0 + e] = v[e];
-                }
-                if (R.out_state) {
-                    // the block's particles in the staging row, then their states
-                    // copied by consecutive lanes for consecutive outputs
-                    // (coalesced: neighbouring outputs hold neighbouring particles).
-                    // States are read and written once: evict-first loads and
-                    // stores, so that they do not push the rows' log-weights,
-                    // which the row's later passes read again, out of L2.
-                    __syncwarp();  // every lane has read the staging row
-                    *reinterpret_cast<int4*>(stage + t0) = make_int4(v[0], v[1], v[2], v[3]);
-                    *reinterpret_cast<int4*>(stage + t0 + 4) = make_int4(v[4], v[5], v[6], v[7]);
-                    __syncwarp();
-                    const int D = R.D;
-                    const float* srow = R.state + static_cast<size_t>(b) * P * D;
-                    float* drow = R.out_state + static_cast<size_t>(b) * P * D;
-                    const int j_end = min(b0 + kWarpBlock, w_hi);
-                    for (int j = max(b0, w_lo) + lane; j < j_end; j += 32) {
-                        const int i = stage[j - b0];
-                        if ((D & 3) == 0) {
-                            for (int d = 0; d < D; d += 4)
-                                __stcs(reinterpret_cast<float4*>(drow + static_cast<size_t>(j) * D + d),
-                                       __ldcs(reinterpret_cast<const float4*>(srow + static_cast<size_t>(i) * D + d)));
-                        } else {
-                            for (int d = 0; d < D; ++d)
-                                __stcs(drow + static_cast<size_t>(j) * D + d, __ldcs(srow + static_cast<size_t>(i) * D + d));
-                        }
-                    }
                 }
                 __syncwarp();  // the staging row is reused by the next block
             }
