@@ -271,7 +271,8 @@ constexpr int kStreamWarps = kStreamSlices / kStreamSpw;  // compute warps
 constexpr int kStreamLookback = 2;               // lookback warps
 constexpr int kStreamThreads = (kStreamWarps + 2 + kStreamLookback) * 32;
 // Records per lane per poll of a lookback: a window of 160 tiles, which
-// reaches the CTA's previous tile (about one tile per CTA back).
+// reaches back to the CTA's previous tile (about one tile per CTA of the
+// grid earlier).
 constexpr int kLookbackQ = 5;
 
 // Record tags of the current call: "aggregate" (the tile's own sum) and
