@@ -120,6 +120,29 @@ def test_cdf_streaming_path_reports_negative_priority():
     assert per.per_check(ctx.handle) == 0
 
 
+def test_cdf_streaming_path_repeated_calls_and_sizes():
+    # repeated streaming scans on one context, the size changing between
+    # calls: records of earlier calls (more tiles, other sums) carry older
+    # tags and are never taken; every call equals the first one of its size
+    cap = (1 << 22) + 9
+    p = workloads.abs_normal(cap, workloads.rng(106))
+    ctx = make_ctx(p, 0.6, SCAN)
+    first = {}
+    for rep in range(3):
+        for size in (cap, 3 * (1 << 20) + 5, (1 << 21) + 1, cap):
+            per.per_set_size(ctx.handle, size)
+            per.per_build_cdf(ctx.handle)
+            assert per.per_check(ctx.handle) == 0
+            c = host(per.read_cdf(ctx.handle))[:size]
+            if size not in first:
+                C = oracle.cdf64(p[:size], 0.6)
+                assert np.all(np.diff(c) >= 0)
+                assert np.max(np.abs(c - C)) <= 2e-6 * C[-1]
+                first[size] = c
+            else:
+                assert np.array_equal(c, first[size]), (rep, size)
+
+
 def test_cdf_large_tile_path_ragged():
     # lognormal priorities through the streaming kernel; ragged tail included
     n = 3 * 1024 * 1024 + 12345
