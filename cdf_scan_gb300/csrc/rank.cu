@@ -27,7 +27,9 @@
 // order: the sort is stable.  The cross-tile offsets come from
 //   large sizes -- three launches per pass: per-tile digit histograms
 //             (digit-major), one CTA per digit scanning its row across the
-//             tiles, then the tile pass above;
+//             tiles, then the tile pass above (one kernel per kind of pass:
+//             first, middle, last), and after the last pass one launch that
+//             returns rank_of's L2 lines to the normal eviction priority;
 //   small sizes -- one cooperative launch for all four passes: each CTA
 //             publishes its tile's digit counts (16 bits each, digit-major),
 //             and after a grid barrier sums the counts of all tiles itself:
@@ -53,6 +55,18 @@ static_assert(kBigMaxTiles <= 4 * kScanThreads, "the digit scan takes at most 4 
 // Ascending keys = descending priorities: non-negative floats order like
 // their bit patterns, and -0 and +0 share one key.
 __device__ __forceinline__ unsigned rank_key(float p) { return ~__float_as_uint(p + 0.f); }
+
+// The last pass writes rank_of in random order, 4 bytes at a time.  Stored
+// with L2 eviction priority evict_last, a line stays in L2 until its 32
+// entries have arrived instead of going back to DRAM part-written, over and
+// over (16M: 598 -> 540 us for the sort; that pass wrote 370 MB to DRAM for
+// 128 MB of order and rank_of).  restore_l2_priority_kernel then returns the
+// lines to the normal priority, so that they do not hold L2 after the sort.
+__device__ __forceinline__ void store_evict_last(int32_t* a, int32_t v) {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(a), "r"(v), "l"(pol) : "memory");
+}
 
 struct SortParams {
     const float* prio;
@@ -81,6 +95,20 @@ struct PassIO {
     int shift;
     bool first, last;
 };
+
+// What a kernel knows of its pass at compile time: the first (priorities
+// in, indices as values), a middle one, the last (order and rank_of out), or
+// nothing (the one-launch sort, whose pass is a loop variable).
+enum PassKind { kFirstPass, kMiddlePass, kLastPass, kAnyPass };
+
+template <int K>
+__device__ __forceinline__ bool first_pass(const PassIO& io) {
+    return K == kAnyPass ? io.first : K == kFirstPass;
+}
+template <int K>
+__device__ __forceinline__ bool last_pass(const PassIO& io) {
+    return K == kAnyPass ? io.last : K == kLastPass;
+}
 
 __device__ __forceinline__ PassIO pass_io(const SortParams& S, int pass) {
     PassIO io;
@@ -145,10 +173,12 @@ __device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* s_w, u
 
 // Rank step: the warp's keys of this tile and, per key, its position among
 // the warp's keys of the same digit; sm.cnt[warp][d] ends as the warp's count
-// of digit d (sm.cnt zeroed by the caller).
-template <int ITEMS>
+// of digit d (sm.cnt zeroed by the caller).  Positions are below 32 * ITEMS
+// and two share a register (round r in bits 16 * (r & 1) of pos[r / 2]):
+// with one per register the tile pass spilled at 3 CTAs per SM.
+template <int ITEMS, int K>
 __device__ __forceinline__ void warp_rank(const SortParams& S, const PassIO& io, int tile_base,
-                                          unsigned (&key)[ITEMS], unsigned (&pos)[ITEMS], SortSmem<ITEMS>& sm,
+                                          unsigned (&key)[ITEMS], unsigned (&pos)[ITEMS / 2], SortSmem<ITEMS>& sm,
                                           bool& bad) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned lt = (1u << lane) - 1u;
@@ -160,8 +190,10 @@ __device__ __forceinline__ void warp_rank(const SortParams& S, const PassIO& io,
         const int i = base + r * 32 + lane;
         key[r] = 0u;
         if (i < S.n) {
-            if (io.first) {
-                const float p = __ldg(S.prio + i);
+            if (first_pass<K>(io)) {
+                // through L2 only (ld.global.cg): the 16M sort measured 599 us
+                // this way and 641 us with the read-only path (ld.global.nc)
+                const float p = __ldcg(S.prio + i);
                 bad |= !(p >= 0.f);  // negative or NaN
                 key[r] = rank_key(p);
             } else {
@@ -181,7 +213,8 @@ __device__ __forceinline__ void warp_rank(const SortParams& S, const PassIO& io,
             sm.cnt[warp][d] = old + __popc(peers);
         }
         old = __shfl_sync(PER_FULL_MASK, old, leader);
-        pos[r] = old + __popc(peers & lt);
+        const unsigned pr = old + __popc(peers & lt);  // < 32 * ITEMS
+        pos[r >> 1] = (r & 1) ? (pos[r >> 1] | (pr << 16)) : pr;
         __syncwarp();
     }
 }
@@ -203,9 +236,9 @@ __device__ __forceinline__ unsigned warp_offsets(SortSmem<ITEMS>& sm) {
 
 // Place and write steps.  On entry sm.cnt[w][d] is the local slot of warp
 // w's first key of digit d and sm.off[d] = global position - local slot.
-template <int ITEMS>
+template <int ITEMS, int K>
 __device__ __forceinline__ void place_and_write(const SortParams& S, const PassIO& io, int tile_base,
-                                                const unsigned (&key)[ITEMS], const unsigned (&pos)[ITEMS],
+                                                const unsigned (&key)[ITEMS], const unsigned (&pos)[ITEMS / 2],
                                                 SortSmem<ITEMS>& sm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int base = tile_base + warp * 32 * ITEMS;
@@ -213,14 +246,14 @@ __device__ __forceinline__ void place_and_write(const SortParams& S, const PassI
 #pragma unroll
     for (int r = 0; r < ITEMS; ++r) {  // loads first, all in flight together
         const int i = base + r * 32 + lane;
-        val[r] = io.first ? i : (i < S.n ? __ldcg(io.vals_in + i) : 0);
+        val[r] = first_pass<K>(io) ? i : (i < S.n ? __ldcg(io.vals_in + i) : 0);
     }
 #pragma unroll
     for (int r = 0; r < ITEMS; ++r) {
         const int i = base + r * 32 + lane;
         if (i >= S.n) continue;
         const unsigned d = (key[r] >> io.shift) & 255u;
-        const unsigned slot = sm.cnt[warp][d] + pos[r];
+        const unsigned slot = sm.cnt[warp][d] + ((pos[r >> 1] >> (16 * (r & 1))) & 0xffffu);
         if (slot >= static_cast<unsigned>(kSortThreads * ITEMS)) continue;  // only if the counts were inconsistent
         sm.keys[slot] = key[r];
         sm.vals[slot] = val[r];
@@ -237,9 +270,9 @@ __device__ __forceinline__ void place_and_write(const SortParams& S, const PassI
             bad = true;
             continue;
         }
-        if (io.keys_out) io.keys_out[dst] = k;
+        if (!last_pass<K>(io)) io.keys_out[dst] = k;
         io.vals_out[dst] = v;
-        if (io.last) S.rank_of[v] = static_cast<int32_t>(dst);
+        if (last_pass<K>(io)) store_evict_last(S.rank_of + v, static_cast<int32_t>(dst));
     }
     if (bad) atomicOr(S.status, ST_RANGE);
 }
@@ -249,15 +282,20 @@ __device__ __forceinline__ void place_and_write(const SortParams& S, const PassI
 // Per-tile digit counts, stored digit-major: counts[d][tile], from per-warp
 // sub-histograms of shared-memory atomics (plain atomics measured faster here
 // than adding once per peer group found with ballots or __match_any_sync).
+template <bool FIRST>
 __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) {
     __shared__ unsigned h[kSortWarps][kRadixDigits];
     const int warp = threadIdx.x >> 5;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the digit scan may be scheduled
     for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&h[0][0])[i] = 0u;
     __syncthreads();
     // launched as a programmatic dependent of the previous pass's tile pass
-    // (passes 1-3): its keys are complete only once that launch is done
+    // (passes 1-3): its keys are complete only once that launch is done.
+    // The digit scan may be scheduled only after this wait: the next tile
+    // pass, scheduled once every digit-scan CTA has started, loads the keys
+    // written by the previous tile pass before its own wait, and that launch
+    // is two launches back -- a wait covers the launch directly before only.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const PassIO io = pass_io(S, S.pass);
     const int tile_base = blockIdx.x * kRankTile;
     bool bad = false;
@@ -267,7 +305,7 @@ __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) 
     for (int e = 0; e < kBigItems / 4; ++e) {  // all loads first, in flight together
         const int i0 = tile_base + (e * kSortThreads + threadIdx.x) * 4;
         if (i0 + 3 < S.n) {
-            if (io.first) {
+            if (FIRST) {
                 const float4 p = __ldg(reinterpret_cast<const float4*>(S.prio + i0));
                 bad |= !(p.x >= 0.f) || !(p.y >= 0.f) || !(p.z >= 0.f) || !(p.w >= 0.f);
                 k[4 * e] = rank_key(p.x); k[4 * e + 1] = rank_key(p.y);
@@ -285,7 +323,7 @@ __global__ void __launch_bounds__(kSortThreads) radix_hist_kernel(SortParams S) 
                 ok[4 * e + c] = i < S.n;
                 k[4 * e + c] = 0u;
                 if (i < S.n) {
-                    if (io.first) {
+                    if (FIRST) {
                         const float p = __ldg(S.prio + i);
                         bad |= !(p >= 0.f);
                         k[4 * e + c] = rank_key(p);
@@ -313,7 +351,8 @@ __global__ void __launch_bounds__(kScanThreads) radix_digit_scan_kernel(unsigned
                                                                         int tiles) {
     __shared__ unsigned s_w[kScanThreads / 32];
     // the tile pass may start now: it loads and ranks its keys before it
-    // waits for these offsets
+    // waits for these offsets (those keys are complete: every histogram CTA
+    // passed its wait for the previous tile pass before this launch began)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the histogram launch's counts
     unsigned* row = counts + static_cast<int64_t>(blockIdx.x) * tiles;
@@ -352,6 +391,7 @@ __global__ void __launch_bounds__(kScanThreads) radix_digit_scan_kernel(unsigned
 
 // The tile pass of large sizes: rank, place against the offsets of the
 // histogram and digit-scan launches, write.
+template <int K>
 __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(SortParams S) {
     __shared__ SortSmem<kBigItems> sm;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the next histogram may be scheduled
@@ -360,9 +400,9 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(SortPara
     for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&sm.cnt[0][0])[i] = 0u;
     __syncthreads();
     const int tile_base = blockIdx.x * kRankTile;
-    unsigned key[kBigItems], pos[kBigItems];
+    unsigned key[kBigItems], pos[kBigItems / 2];
     bool bad = false;  // reported by the histogram launch
-    warp_rank<kBigItems>(S, io, tile_base, key, pos, sm, bad);
+    warp_rank<kBigItems, K>(S, io, tile_base, key, pos, sm, bad);
     __syncthreads();
     const unsigned cnt_d = warp_offsets(sm);
     unsigned tile_total = 0u, all = 0u;
@@ -376,7 +416,7 @@ __global__ void __launch_bounds__(kSortThreads, 3) radix_scatter_kernel(SortPara
     for (int w = 0; w < kSortWarps; ++w) sm.cnt[w][d] += start_d;
     sm.off[d] = static_cast<int>(gbase) - static_cast<int>(start_d);
     __syncthreads();
-    place_and_write<kBigItems>(S, io, tile_base, key, pos, sm);
+    place_and_write<kBigItems, K>(S, io, tile_base, key, pos, sm);
 }
 
 // ---- small sizes: all four passes in one cooperative launch ----------------
@@ -395,8 +435,8 @@ __global__ void __launch_bounds__(kSortThreads) radix_sort_small_kernel(SortPara
         const PassIO io = pass_io(S, pass);
         for (int i = threadIdx.x; i < kSortWarps * kRadixDigits; i += kSortThreads) (&sm.cnt[0][0])[i] = 0u;
         __syncthreads();
-        unsigned key[kSmallItems], pos[kSmallItems];
-        warp_rank<kSmallItems>(S, io, tile_base, key, pos, sm, bad);
+        unsigned key[kSmallItems], pos[kSmallItems / 2];
+        warp_rank<kSmallItems, kAnyPass>(S, io, tile_base, key, pos, sm, bad);
         __syncthreads();
         const unsigned cnt_d = warp_offsets(sm);
         unsigned tile_total = 0u, all = 0u;
@@ -426,10 +466,22 @@ __global__ void __launch_bounds__(kSortThreads) radix_sort_small_kernel(SortPara
         for (int w = 0; w < kSortWarps; ++w) sm.cnt[w][d] += start_d;
         sm.off[d] = static_cast<int>(digit_start + before) - static_cast<int>(start_d);
         __syncthreads();
-        place_and_write<kSmallItems>(S, io, tile_base, key, pos, sm);
+        place_and_write<kSmallItems, kAnyPass>(S, io, tile_base, key, pos, sm);
         if (pass < 3 && !grid_barrier(S.ticket, S.status, ST_TIMEOUT)) return;
     }
     if (bad) atomicOr(S.status, ST_VALUE);
+}
+
+// Normal L2 eviction priority again for the 128-byte lines of a[0, n) (a
+// 128-byte aligned; the last line lies in the same allocation).  Launched as a
+// programmatic dependent of the last tile pass.
+__global__ void __launch_bounds__(256) restore_l2_priority_kernel(const int32_t* a, int n) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t lines = (static_cast<int64_t>(n) * 4 + 127) / 128;
+    for (int64_t l = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; l < lines;
+         l += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(a + l * 32) : "memory");
 }
 
 // q[r] = fl32(1 / (r + 1)), correctly rounded (r + 1 <= 2^24 is exact in fp32).
@@ -485,7 +537,9 @@ per_status launch_rank_build(per_ctx* ctx, cudaStream_t s) {
         // Each launch is a programmatic dependent of the one before it (but
         // the first, which follows whatever the stream ran before): it is
         // scheduled while that launch finishes and waits for it
-        // (griddepcontrol.wait) before its first dependent read.
+        // (griddepcontrol.wait) before its first dependent read.  The tile
+        // pass reads the keys of the tile pass before it early; the histogram
+        // launch between them lets its dependents start only after its wait.
         auto launch = [&](auto kernel, unsigned grid, unsigned block, bool dependent, auto... args) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(grid);
@@ -503,13 +557,22 @@ per_status launch_rank_build(per_ctx* ctx, cudaStream_t s) {
         for (int pass = 0; pass < 4 && e == cudaSuccess; ++pass) {
             S.pass = pass;
             const unsigned tiles = static_cast<unsigned>(S.tiles);
-            if ((e = launch(radix_hist_kernel, tiles, kSortThreads, pass > 0, S)) != cudaSuccess) break;
+            if ((e = launch(pass == 0 ? radix_hist_kernel<true> : radix_hist_kernel<false>, tiles, kSortThreads,
+                            pass > 0, S)) != cudaSuccess)
+                break;
             ++launched;
             if ((e = launch(radix_digit_scan_kernel, static_cast<unsigned>(kRadixDigits), kScanThreads, true,
                             ctx->rank_counts, ctx->rank_totals, S.tiles)) != cudaSuccess)
                 break;
             ++launched;
-            if ((e = launch(radix_scatter_kernel, tiles, kSortThreads, true, S)) != cudaSuccess) break;
+            auto scatter = pass == 0 ? radix_scatter_kernel<kFirstPass>
+                                     : pass == 3 ? radix_scatter_kernel<kLastPass> : radix_scatter_kernel<kMiddlePass>;
+            if ((e = launch(scatter, tiles, kSortThreads, true, S)) != cudaSuccess) break;
+            ++launched;
+        }
+        if (e == cudaSuccess) {
+            e = launch(restore_l2_priority_kernel, static_cast<unsigned>(ctx->num_sms * 4), 256u, true,
+                       static_cast<const int32_t*>(ctx->rank_of), n);
             ++launched;
         }
         per_note_launch(launched);

@@ -65,6 +65,24 @@ def test_rank_order_and_cdf_match_oracle(n):
     assert per.per_check(ctx.handle) == 0
 
 
+@pytest.mark.parametrize("n", [262_145, 300_001, 600_000, 2_000_003])
+def test_rank_order_back_to_back_builds(n):
+    """Sizes just above the one-launch sort, where every launch of a pass can
+    be resident at once: several builds queued without a host sync, the
+    priorities switched between them, each order bit-exact."""
+    pa = tied_priorities(n, 305)
+    pb = workloads.lognormal(n, workloads.rng(306, n))
+    want = {0: oracle.rank_order(pa), 1: oracle.rank_order(pb)}
+    ctx = per.PerContext(n, 0.6, RANK)
+    da, db = dev(pa), dev(pb)
+    for k in range(4):
+        per.per_set_priorities(ctx.handle, da if k % 2 == 0 else db)
+        for _ in range(3):
+            per.per_rank_build(ctx.handle)
+        assert np.array_equal(host(per.read_rank_order(ctx.handle)), want[k % 2])
+    assert per.per_check(ctx.handle) == 0
+
+
 def test_rank_order_distinct_values_and_rebuild_after_updates():
     n = 70_001
     p = workloads.lognormal(n, workloads.rng(302))
