@@ -124,15 +124,22 @@ __device__ __forceinline__ PassIO pass_io(const SortParams& S, int pass) {
     return io;
 }
 
+// The tile pass's table of one lane per warp and digit (see warp_rank); the
+// one-launch sort has none.
 template <int ITEMS>
-struct SortSmem {
+struct RankRep {};
+template <>
+struct RankRep<kBigItems> {
+    unsigned char rep[kSortWarps][kRadixDigits + 4];
+};
+
+template <int ITEMS>
+struct SortSmem : RankRep<ITEMS> {
     unsigned keys[kSortThreads * ITEMS];         // the tile, sorted by digit
     int32_t vals[kSortThreads * ITEMS];
     unsigned cnt[kSortWarps][kRadixDigits];      // per-warp digit counts, then local offsets
     int off[kRadixDigits];                       // global position - local slot, per digit
     unsigned w[kSortWarps];
-    // per warp and digit: one lane holding it (the tile pass of large sizes only)
-    unsigned char rep[ITEMS == kBigItems ? kSortWarps : 1][kRadixDigits + 4];
 };
 
 // The lanes of the warp whose digit equals this lane's (valid lanes), or the
@@ -188,8 +195,8 @@ __device__ __forceinline__ unsigned block_excl_scan(unsigned v, unsigned* s_w, u
 // lanes with equal representatives, a 5-bit value: five ballots instead of
 // eight.  The group's lanes read its running count together, and the
 // representative adds the group's size.  16M sort: 553 -> 514 us.  The
-// one-launch sort keeps the eight ballots and a leader's read (it measured
-// 46.1 against 45.4 us at 262,144 the other way).
+// one-launch sort keeps the eight ballots and a leader's read (the other way
+// it measured 47.5 against 46.8 us at 262,144).
 template <int ITEMS, int K>
 __device__ __forceinline__ void warp_rank(const SortParams& S, const PassIO& io, int tile_base,
                                           unsigned (&key)[ITEMS], unsigned (&pos)[ITEMS / 2], SortSmem<ITEMS>& sm,
@@ -219,32 +226,35 @@ __device__ __forceinline__ void warp_rank(const SortParams& S, const PassIO& io,
     for (int r = 0; r < ITEMS; ++r) {
         const bool ok = base + r * 32 + lane < S.n;
         const unsigned d = ok ? (key[r] >> io.shift) & 255u : 0u;
-        unsigned old = 0u, peers = PER_FULL_MASK;
         if constexpr (K == kAnyPass) {
-            peers = digit_peers(d, ok);
+            const unsigned peers = digit_peers(d, ok);
             const int leader = __ffs(peers) - 1;
+            unsigned old = 0u;
             if (ok && lane == leader) {
                 old = sm.cnt[warp][d];
                 sm.cnt[warp][d] = old + __popc(peers);
             }
             old = __shfl_sync(PER_FULL_MASK, old, leader);
+            const unsigned pr = old + __popc(peers & lt);  // < 32 * ITEMS
+            pos[r >> 1] = (r & 1) ? (pos[r >> 1] | (pr << 16)) : pr;
         } else {
             unsigned char* slot = &sm.rep[warp][ok ? d : kRadixDigits];  // invalid lanes: a group of their own
             *slot = static_cast<unsigned char>(lane);
             __syncwarp();
             const int rep = *slot;
+            unsigned peers = PER_FULL_MASK;
 #pragma unroll
             for (int b = 0; b < 5; ++b) {
                 const bool bit = ((rep >> b) & 1) != 0;
                 const unsigned m = __ballot_sync(PER_FULL_MASK, bit);
                 peers &= bit ? m : ~m;
             }
-            old = sm.cnt[warp][d];  // the group's lanes read one word
+            const unsigned old = sm.cnt[warp][d];  // the group's lanes read one word
             __syncwarp();
             if (ok && lane == rep) sm.cnt[warp][d] = old + __popc(peers);
+            const unsigned pr = old + __popc(peers & lt);  // < 32 * ITEMS
+            pos[r >> 1] = (r & 1) ? (pos[r >> 1] | (pr << 16)) : pr;
         }
-        const unsigned pr = old + __popc(peers & lt);  // < 32 * ITEMS
-        pos[r >> 1] = (r & 1) ? (pos[r >> 1] | (pr << 16)) : pr;
         __syncwarp();
     }
 }
