@@ -117,16 +117,29 @@ __device__ __forceinline__ int count_le_pow2(float c, float U, int P, float fP) 
 }
 
 // w = exp(x - m) as the hardware ex2 of (x - m) * log2(e); -inf gives 0.
-__device__ __forceinline__ float exp_rel(float x, float m) { return hw_ex2(__fmul_rn(__fsub_rn(x, m), kLog2e)); }
+// The flush-to-zero form (one instruction) differs from the other only for
+// a subnormal argument (x within ~1e-38 of m, the result 1 either way up to
+// the approximation) or a result below 2^-126, which fix40w maps to 0 in
+// both: 97.8 against 98.9 us for the resample.
+__device__ __forceinline__ float exp_rel(float x, float m) {
+    return hw_ex2_ftz(__fmul_rn(__fsub_rn(x, m), kLog2e));
+}
 
 // floor(w * 2^40) for w in [0, 1], from the float's exponent and mantissa
-// with integer shifts (no 64-bit conversion).
+// (no 64-bit conversion): w * 2^40 = mant * 2^sh with sh = e - 110 <= 17, so
+// it is (mant >> -sh) for sh < 0 (0 from sh <= -24: below 2^-40, zero,
+// subnormal) and mant * 2^sh otherwise -- one 32 x 32 -> 64-bit multiply
+// instead of 64-bit shifts (resample 100.8 -> 96.8 us; the same value for
+// every float in [0, 1], checked exhaustively against the shift form).
 __device__ __forceinline__ unsigned long long fix40w(float w) {
     const unsigned bits = __float_as_uint(w);
-    const int sh = static_cast<int>(bits >> 23) - 110;  // w * 2^40 = mant * 2^(e - 150 + 40)
-    const unsigned long long mant = (bits & 0x7fffffu) | 0x800000u;
-    if (sh <= -24) return 0ull;  // below 2^-40, or zero / subnormal
-    return sh >= 0 ? mant << sh : mant >> (-sh);
+    const int sh = static_cast<int>(bits >> 23) - 110;
+    const unsigned mant = (bits & 0x7fffffu) | 0x800000u;
+    const unsigned sl = static_cast<unsigned>(max(sh, 0));            // <= 17 for w <= 1
+    const unsigned sr = static_cast<unsigned>(min(max(-sh, 0), 31));  // mant < 2^24: 0 from 24 on
+    unsigned p2;  // 2^sl; PTX shl clamps the shift, so a NaN or inf w (sl > 31) gives 0
+    asm("shl.b32 %0, %1, %2;" : "=r"(p2) : "r"(1u), "r"(sl));
+    return static_cast<unsigned long long>(mant >> sr) * p2;
 }
 
 // Monotone fp32 value of E < 2^56: the high half (below 2^24) is exact in
