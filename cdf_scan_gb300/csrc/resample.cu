@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
     __shared__ unsigned long long s_cq;     // this segment's exact total, read by the cluster
     __shared__ float s_rmax;
     __shared__ unsigned long long s_rq[2];  // the row's total; the segments' before this one
-    __shared__ unsigned long long s_off[kWarps + 1];
+    __shared__ unsigned long long s_cw[2][kWarps];  // per chunk (by parity): the warps' inclusive totals
     __shared__ __align__(16) int s_stage[kChunk];  // one block of outputs (per warp: kWarpBlock of them): run starts, then filled
     __shared__ int s_wmax[kWarps];                  // resample step only: the block-wide max-scan
     __shared__ int s_range[2];                      // resample step only: the chunk's outputs [j_lo, j_hi)
@@ -314,17 +314,19 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
             r[4 * h + 3] = run;
         }
         const unsigned long long x = warp_incl_u64(run, lane);
-        if (lane == 31) s_u[warp] = x;
+        const int par = ((c0 - s0) / kChunk) & 1;
+        if (lane == 31) s_cw[par][warp] = x;
+        // One barrier per chunk: every warp scans the kWarps warp totals itself
+        // (instead of warp 0 scanning them between two barriers).  A warp
+        // writes this parity's slots again two chunks later, past the next
+        // chunk's barrier, which every warp reaches only after its reads here.
         __syncthreads();
-        if (warp == 0) {
-            const unsigned long long t = lane < kWarps ? s_u[lane] : 0ull;
-            const unsigned long long wi = warp_incl_u64(t, lane);
-            if (lane < kWarps) s_off[lane] = wi - t;
-            if (lane == kWarps - 1) s_off[kWarps] = wi;
-        }
-        __syncthreads();
-        const unsigned long long base = carry + s_off[warp] + (x - run);  // E before this lane's first particle
-        carry += s_off[kWarps];
+        const unsigned long long t = lane < kWarps ? s_cw[par][lane] : 0ull;
+        const unsigned long long wi = warp_incl_u64(t, lane);
+        const unsigned long long wb = __shfl_sync(PER_FULL_MASK, wi, warp > 0 ? warp - 1 : 0);
+        const unsigned long long before_w = warp > 0 ? wb : 0ull;
+        const unsigned long long base = carry + before_w + (x - run);  // E before this lane's first particle
+        carry += __shfl_sync(PER_FULL_MASK, wi, kWarps - 1);
         float cv[kLane];
 #pragma unroll
         for (int e = 0; e < kLane; ++e) cv[e] = __fmul_rn(u64_to_f32(base + r[e]), inv);
