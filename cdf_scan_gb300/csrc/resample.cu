@@ -97,21 +97,16 @@ __device__ __forceinline__ int count_le(float c, float U, int P, float fP, float
 
 // count_le for a power-of-two P without loops.  u_j <= c exactly when
 // fl32(j + U) <= C = c * P (both products by a power of two are exact).  With
-// f = floor(C): every j <= f - 2 counts, since fl32(j + U) <= j + 1 <= C (j + 1
-// is exact below 2^24 and U < 1); every j >= f + 1 does not, since
-// fl32(j + U) >= j > C.  So two exact tests, at j = f - 1 and j = f, settle
-// the count (the test is monotone in j, so the two indicators add up).
-//
-// In floats: F = floor(C) and F - 1 are exact, so the tests are
-// fl32((F - 1) + U) <= C and fl32(F + U) <= C.  For F = 0 the first test
-// (j = -1) always holds and stands in for the missing j <= -2 term; for
-// F >= P the count is clamped to P (the tests are monotone in j, so the
-// second cannot hold without the first).  NaN gives 0.
+// f = floor(C): every j <= f - 1 counts, since fl32(j + U) <= j + 1 <= C (j + 1
+// is exact below 2^24, U < 1, and rounding to nearest cannot pass the
+// representable j + 1); every j >= f + 1 does not, since fl32(j + U) >= j > C.
+// So one exact test, at j = f, settles the count: n = f + [fl32(F + U) <= C]
+// with F = floor(C) in floats (exact), clamped to [0, P].  NaN gives 0.  (A
+// second test at j = f - 1, always true, went out: 95.0-95.6 -> 94.6 us.)
 __device__ __forceinline__ int count_le_pow2(float c, float U, int P, float fP) {
     const float C = __fmul_rn(c, fP);
     const float F = floorf(C);
-    int n = __float2int_rz(F) - 1;
-    if (__fadd_rn(__fsub_rn(F, 1.0f), U) <= C) ++n;
+    int n = __float2int_rz(F);
     if (__fadd_rn(F, U) <= C) ++n;
     return min(max(n, 0), P);
 }
