@@ -157,8 +157,11 @@ __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long x
 
 // STEP: the whole resample step (states copied, log-weights reset).  Its state
 // copy is memory-bound and gains from a third CTA per SM (40 registers, a few
-// spilled); the indices alone run faster at two (64 registers, no spills).
-template <bool STEP>
+// spilled); the indices alone run faster at two (62 registers, no spills).
+// POW2: P is a power of two, so the threshold count is count_le_pow2's one
+// test, compiled in instead of chosen per particle (95 -> 90.7 us at
+// 256 x 65536; the step 206 -> 203 us).
+template <bool STEP, bool POW2>
 __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(ResampleParams R) {
     __shared__ float s_f[kWarps];
     __shared__ unsigned long long s_u[kWarps];
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
     // c = fl32(E) * fl32(1 / Q): monotone in E, c(Q) ~= 1
     const float inv = __fdiv_rn(1.0f, u64_to_f32(Q));
     const float fP = static_cast<float>(P);
-    const bool pow2 = (P & (P - 1)) == 0;
+    constexpr bool pow2 = POW2;
     const float inv_p = __fdiv_rn(1.0f, fP);
     const float U = R.u_rows ? R.u_rows[b] : u01_closed_open(R.seed, R.offset + static_cast<uint64_t>(b));
 
@@ -332,7 +335,10 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
         }
         // run ends: particle i owns outputs [n(c_{i-1}), n(c_i)), the last
         // particle's run extending to P (the clamp)
-        auto n_of = [&](float c) { return pow2 ? count_le_pow2(c, U, P, fP) : count_le(c, U, P, fP, inv_p, pow2); };
+        auto n_of = [&](float c) {
+            if constexpr (POW2) return count_le_pow2(c, U, P, fP);
+            else return count_le(c, U, P, fP, inv_p, false);
+        };
         int start = 0;  // n(c) of the particle before this lane's first
         if (i0 >= P) start = P;
         else if (i0 > 0) start = n_of(__fmul_rn(u64_to_f32(base), inv));
@@ -544,8 +550,12 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     if (R.staged) {
         static DeviceCache cache;
         const int ok = device_cached(cache, [&]() {
-            return cudaFuncSetAttribute(resample_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem)) == cudaSuccess ? 1 : 2;
+            return cudaFuncSetAttribute(resample_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem)) == cudaSuccess &&
+                           cudaFuncSetAttribute(resample_kernel<false, false>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(smem)) == cudaSuccess
+                       ? 1 : 2;
         });
         if (ok != 1) return PER_ERR_CUDA;
     }
@@ -562,8 +572,11 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = step ? cudaLaunchKernelEx(&cfg, resample_kernel<true>, R)
-                               : cudaLaunchKernelEx(&cfg, resample_kernel<false>, R);
+    const bool pow2 = (P & (P - 1)) == 0;
+    const cudaError_t e = step ? (pow2 ? cudaLaunchKernelEx(&cfg, resample_kernel<true, true>, R)
+                                       : cudaLaunchKernelEx(&cfg, resample_kernel<true, false>, R))
+                               : (pow2 ? cudaLaunchKernelEx(&cfg, resample_kernel<false, true>, R)
+                                       : cudaLaunchKernelEx(&cfg, resample_kernel<false, false>, R));
     per_note_launch();
     return cuda_status(e);
 }
