@@ -160,8 +160,11 @@ __device__ __forceinline__ unsigned long long warp_incl_u64(unsigned long long x
 // spilled); the indices alone run faster at two (62 registers, no spills).
 // POW2: P is a power of two, so the threshold count is count_le_pow2's one
 // test, compiled in instead of chosen per particle (95 -> 90.7 us at
-// 256 x 65536; the step 206 -> 203 us).
-template <bool STEP, bool POW2>
+// 256 x 65536; the step 206 -> 203 us).  STAGED: the segment lives in shared
+// memory (the index kernel's usual case); compiled in, it drops the unstaged
+// path's loads and registers (90.8 -> 88.6 us; the step, never staged, 203
+// -> 199 us with fewer spills).
+template <bool STEP, bool POW2, bool STAGED>
 __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(ResampleParams R) {
     __shared__ float s_f[kWarps];
     __shared__ unsigned long long s_u[kWarps];
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
     __shared__ __align__(16) int s_stage[kChunk];  // one block of outputs (per warp: kWarpBlock of them): run starts, then filled
     __shared__ int s_wmax[kWarps];                  // resample step only: the block-wide max-scan
     __shared__ int s_range[2];                      // resample step only: the chunk's outputs [j_lo, j_hi)
-    extern __shared__ __align__(16) float s_seg[];  // the staged segment (kStageMax floats when R.staged)
+    extern __shared__ __align__(16) float s_seg[];  // the staged segment (kStageMax floats when STAGED)
     cg::cluster_group cluster = cg::this_cluster();
     const int K = static_cast<int>(cluster.num_blocks()), k = static_cast<int>(cluster.block_rank());
     const int b = blockIdx.x / K;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
             const int i = i0 + u * kThreads * 4;
             q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
-        if (R.staged) {  // the whole segment, -inf past its end (one iteration)
+        if (STAGED) {  // the whole segment, -inf past its end (one iteration)
 #pragma unroll
             for (int u = 0; u < kBatch; ++u)
                 *reinterpret_cast<float4*>(s_seg + (i0 - s0) + u * kThreads * 4) = q[u];
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int i = i0 + u * kThreads * 4;
-            if (R.staged)  // this thread's own pass-1 stores
+            if (STAGED)  // this thread's own pass-1 stores
                 q[u] = *reinterpret_cast<const float4*>(s_seg + (i0 - s0) + u * kThreads * 4);
             else
                 q[u] = i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
         for (int u = 0; u < kBatch; ++u) {
             const float4 w = make_float4(exp_rel(q[u].x, rmax), exp_rel(q[u].y, rmax), exp_rel(q[u].z, rmax),
                                          exp_rel(q[u].w, rmax));
-            if (R.staged) *reinterpret_cast<float4*>(s_seg + (i0 - s0) + u * kThreads * 4) = w;
+            if (STAGED) *reinterpret_cast<float4*>(s_seg + (i0 - s0) + u * kThreads * 4) = w;
             acc += fix40w(w.x) + fix40w(w.y) + fix40w(w.z) + fix40w(w.w);
         }
     }
@@ -279,13 +282,13 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
 #pragma unroll
     for (int h = 0; h < kLane / 4; ++h) {
         const int i = s0 + threadIdx.x * kLane + 4 * h;
-        nxt[h] = !R.staged && i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        nxt[h] = !STAGED && i < s1 ? ld_f4(row + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
     unsigned long long carry = s_rq[1];  // the exact total of the segments before this one
     for (int c0 = s0; c0 < s1; c0 += kChunk) {
         const int i0 = c0 + threadIdx.x * kLane;
         float4 cur[kLane / 4];
-        if (R.staged) {
+        if (STAGED) {
 #pragma unroll
             for (int h = 0; h < kLane / 4; ++h)
                 cur[h] = *reinterpret_cast<const float4*>(s_seg + (i0 - s0) + 4 * h);
@@ -550,9 +553,10 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     if (R.staged) {
         static DeviceCache cache;
         const int ok = device_cached(cache, [&]() {
-            return cudaFuncSetAttribute(resample_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            return cudaFuncSetAttribute(resample_kernel<false, true, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem)) == cudaSuccess &&
-                           cudaFuncSetAttribute(resample_kernel<false, false>,
+                           cudaFuncSetAttribute(resample_kernel<false, false, true>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 static_cast<int>(smem)) == cudaSuccess
                        ? 1 : 2;
@@ -573,10 +577,14 @@ per_status launch_resample(const float* logw, int rows, int P, uint64_t seed, ui
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool pow2 = (P & (P - 1)) == 0;
-    const cudaError_t e = step ? (pow2 ? cudaLaunchKernelEx(&cfg, resample_kernel<true, true>, R)
-                                       : cudaLaunchKernelEx(&cfg, resample_kernel<true, false>, R))
-                               : (pow2 ? cudaLaunchKernelEx(&cfg, resample_kernel<false, true>, R)
-                                       : cudaLaunchKernelEx(&cfg, resample_kernel<false, false>, R));
+    auto go = [&](auto kernel) { return cudaLaunchKernelEx(&cfg, kernel, R); };
+    cudaError_t e;
+    if (step)
+        e = pow2 ? go(resample_kernel<true, true, false>) : go(resample_kernel<true, false, false>);
+    else if (R.staged)
+        e = pow2 ? go(resample_kernel<false, true, true>) : go(resample_kernel<false, false, true>);
+    else
+        e = pow2 ? go(resample_kernel<false, true, false>) : go(resample_kernel<false, false, false>);
     per_note_launch();
     return cuda_status(e);
 }
