@@ -187,6 +187,11 @@ per_status per_build_cdf_noalloc(const float* d_prio, int64_t n, float alpha, fl
  * PER_ERR_STATE when the size changed since the last per_rank_build (a
  * per_update without a new per_rank_build samples from the previous order).
  * Requires PER_RANK and size >= 1 (PER_ERR_EMPTY).
+ * Above 262,144 items the last radix pass stores the inverse permutation
+ * (rank of each item, used by per_is_weights) with L2 eviction priority
+ * evict_last, and the call's last launch returns those lines to the normal
+ * priority: once the call's work is done, L2 holds nothing at a raised
+ * priority.
  */
 per_status per_rank_build(per_ctx* ctx, void* stream);
 
