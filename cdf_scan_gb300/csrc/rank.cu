@@ -57,15 +57,16 @@ static_assert(kBigMaxTiles <= 4 * kScanThreads, "the digit scan takes at most 4 
 // their bit patterns, and -0 and +0 share one key.
 __device__ __forceinline__ unsigned rank_key(float p) { return ~__float_as_uint(p + 0.f); }
 
-// The last pass writes rank_of in random order, 4 bytes at a time.  Stored
+// The last tile pass of large sizes writes rank_of in random order, 4 bytes
+// at a time (the one-launch sort's at most 1 MiB stays in L2 anyway).  Stored
 // with L2 eviction priority evict_last, a line stays in L2 until its 32
 // entries have arrived instead of going back to DRAM part-written, over and
 // over (16M: 598 -> 540 us for the sort; that pass wrote 370 MB to DRAM for
 // 128 MB of order and rank_of).  restore_l2_priority_kernel then returns the
 // lines to the normal priority, so that they do not hold L2 after the sort.
 __device__ __forceinline__ void store_evict_last(int32_t* a, int32_t v) {
-    unsigned long long pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    unsigned long long pol;  // a pure value: the compiler may create it once per thread
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(a), "r"(v), "l"(pol) : "memory");
 }
 
@@ -312,7 +313,11 @@ __device__ __forceinline__ void place_and_write(const SortParams& S, const PassI
         }
         if (!last_pass<K>(io)) io.keys_out[dst] = k;
         io.vals_out[dst] = v;
-        if (last_pass<K>(io)) store_evict_last(S.rank_of + v, static_cast<int32_t>(dst));
+        if constexpr (K == kLastPass) {
+            store_evict_last(S.rank_of + v, static_cast<int32_t>(dst));  // restored after the pass
+        } else {
+            if (last_pass<K>(io)) S.rank_of[v] = static_cast<int32_t>(dst);  // the one-launch sort: 1 MiB at most
+        }
     }
     if (bad) atomicOr(S.status, ST_RANGE);
 }
