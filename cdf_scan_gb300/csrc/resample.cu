@@ -270,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, STEP ? 3 : 2) resample_kernel(Resamp
     // c = fl32(E) * fl32(1 / Q): monotone in E, c(Q) ~= 1
     const float inv = __fdiv_rn(1.0f, u64_to_f32(Q));
     const float fP = static_cast<float>(P);
-    constexpr bool pow2 = POW2;
     const float inv_p = __fdiv_rn(1.0f, fP);
     const float U = R.u_rows ? R.u_rows[b] : u01_closed_open(R.seed, R.offset + static_cast<uint64_t>(b));
 
