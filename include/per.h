@@ -26,7 +26,8 @@
  *     they must stay valid until the stream work that uses them completes.
  *     Host pointers are marked "h_".
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
- *     stream).  Every call except per_total_host, per_check, per_destroy and
+ *     stream).  Every call except per_create (which allocates the context's
+ *     device memory), per_total_host, per_check, per_destroy and
  *     per_build_cdf_noalloc (whose own note below governs it) is asynchronous
  *     and stream-ordered: it allocates nothing, never synchronises the host,
  *     and may be captured in a CUDA graph.
