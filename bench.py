@@ -662,7 +662,7 @@ def measure_configs(per, torch, dev, peak, peak_kind, flush, head):
         "resample_step_d4_us": round(us_rs, 2),
         "resample_step_d4_gbs": round(sbytes / (us_rs * 1e-6) / 1e9, 1),
         "resample_step_d4_frac": round(sbytes / (us_rs * 1e-6) / 1e9 / peak, 4),
-        "roofline": roofline("resample_kernel<0>", rbytes, us_r, peak, peak_kind, traffic_for("resample")),
+        "roofline": roofline("resample_kernel<0, 1, 1> (indices; P a power of two, segments staged)", rbytes, us_r, peak, peak_kind, traffic_for("resample")),
         "l2": "flushed before each rep (512 MiB write + 512 MiB read of other buffers)"}
 
     extras.update(rank_and_gather_extras(per, torch, dev, peak, flush, tensor))
